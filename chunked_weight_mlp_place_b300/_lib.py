@@ -1,0 +1,197 @@
+"""ctypes binding of libipttt (include/ipttt.h): argument marshalling only.
+
+Every function takes torch tensors that live on the current CUDA device,
+passes their data pointers, sizes and the current torch stream to the C entry
+point of the same name, and raises :class:`IptttError` on a non-OK status.  No
+step of the layer runs in Python or PyTorch; if ``libipttt.so`` is missing,
+loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libipttt.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALLOC, ERR_LAUNCH, ERR_TIMEOUT, ERR_CUDA = range(7)
+FP32, BF16 = 0, 1
+RULE_MSE, RULE_ADD = 0, 1
+_RULES = {"mse": RULE_MSE, "add": RULE_ADD, RULE_MSE: RULE_MSE, RULE_ADD: RULE_ADD}
+
+# Every symbol include/ipttt.h declares (checked by the ABI tests).
+EXPORTS = (
+    "ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
+    "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
+    "ipttt_status_string", "ipttt_version",
+)
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("d", ctypes.c_int64), ("d_ff", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("w0_per_seq", ctypes.c_int32)]
+
+
+class IptttError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libipttt.so (built by chunked_weight_mlp_place_b300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run `python -m chunked_weight_mlp_place_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int32
+        dp = ctypes.POINTER(Dims)
+        L.ipttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
+        L.ipttt_make_targets.argtypes = [vp, vp, vp, vp, i64, i64, dp, vp]
+        L.ipttt_gate_up.argtypes = [vp, vp, vp, vp, i64, dp, vp]
+        L.ipttt_chunk_forward.argtypes = [vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
+        L.ipttt_workspace_size.argtypes = [dp, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_size_t)]
+        L.ipttt_sync_status.argtypes = [vp]
+        L.ipttt_release.argtypes = []
+        L.ipttt_last_launch_count.argtypes = []
+        L.ipttt_last_launch_count.restype = i64
+        L.ipttt_status_string.argtypes = [i32]
+        L.ipttt_status_string.restype = ctypes.c_char_p
+        L.ipttt_version.argtypes = []
+        for name in ("ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
+                     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().ipttt_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().ipttt_version())
+
+
+def last_launch_count() -> int:
+    """Kernels the last call from this thread queued."""
+    return int(lib().ipttt_last_launch_count())
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise IptttError(status, where)
+
+
+# ------------------------------------------------------------- tensor helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"activations must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t, name: str, dtype=None) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def dims(batch: int, d: int, d_ff: int, dtype: int, w0_per_seq: int = 0) -> Dims:
+    return Dims(int(batch), int(d), int(d_ff), int(dtype), int(w0_per_seq))
+
+
+# ------------------------------------------------------------------ entry points
+def layer_forward(X, E, W_g, W_u, W_o0, conv_w, P, L: int, B: int, eta: float, rule, O, W_final,
+                  stream=None) -> None:
+    """ipttt_layer_forward on tensors: X, E (batch*L, d); W_g, W_u (d, d_ff);
+    W_o0 (d_ff, d) or (batch, d_ff, d) fp32; conv_w (d, 4) fp32; P (d, d);
+    O (batch*L, d) out; W_final (batch, d_ff, d) fp32 out."""
+    torch = _torch()
+    act = X.dtype
+    d, d_ff = W_g.shape
+    batch = X.shape[0] // L if L else W_final.shape[0]
+    dm = dims(batch, d, d_ff, _dtype_code(X), 1 if W_o0.dim() == 3 else 0)
+    st = lib().ipttt_layer_forward(
+        _ptr(X, "X", act), _ptr(E, "E", act), _ptr(W_g, "W_g", act), _ptr(W_u, "W_u", act),
+        _ptr(W_o0, "W_o0", torch.float32), _ptr(conv_w, "conv_w", torch.float32), _ptr(P, "P", act),
+        int(L), int(B), float(eta), _RULES[rule], _ptr(O, "O", act), _ptr(W_final, "W_final", torch.float32),
+        ctypes.byref(dm), _stream(stream))
+    _check(st, "ipttt_layer_forward")
+
+
+def make_targets(E, conv_w, P, V, L: int, B: int, stream=None) -> None:
+    """ipttt_make_targets: V = Proj(Conv(E)) with chunk-end padding."""
+    torch = _torch()
+    act = E.dtype
+    d = E.shape[1]
+    dm = dims(E.shape[0] // L if L else 0, d, 8, _dtype_code(E))
+    st = lib().ipttt_make_targets(_ptr(E, "E", act), _ptr(conv_w, "conv_w", torch.float32), _ptr(P, "P", act),
+                                  _ptr(V, "V", act), int(L), int(B), ctypes.byref(dm), _stream(stream))
+    _check(st, "ipttt_make_targets")
+
+
+def gate_up(X, W_g, W_u, Z, stream=None) -> None:
+    """ipttt_gate_up: Z = SiLU(X W_g) * (X W_u)."""
+    act = X.dtype
+    d, d_ff = W_g.shape
+    dm = dims(1, d, d_ff, _dtype_code(X))
+    st = lib().ipttt_gate_up(_ptr(X, "X", act), _ptr(W_g, "W_g", act), _ptr(W_u, "W_u", act), _ptr(Z, "Z", act),
+                             int(X.shape[0]), ctypes.byref(dm), _stream(stream))
+    _check(st, "ipttt_gate_up")
+
+
+def chunk_forward(Z, V, W_o0, L: int, B: int, eta: float, rule, O, W_final, stream=None) -> None:
+    """ipttt_chunk_forward on precomputed Z (batch*L, d_ff) and V (batch*L, d)."""
+    torch = _torch()
+    act = Z.dtype
+    d_ff = Z.shape[1]
+    d = V.shape[1]
+    batch = Z.shape[0] // L if L else W_final.shape[0]
+    dm = dims(batch, d, d_ff, _dtype_code(Z), 1 if W_o0.dim() == 3 else 0)
+    st = lib().ipttt_chunk_forward(_ptr(Z, "Z", act), _ptr(V, "V", act), _ptr(W_o0, "W_o0", torch.float32),
+                                   int(L), int(B), float(eta), _RULES[rule], _ptr(O, "O", act),
+                                   _ptr(W_final, "W_final", torch.float32), ctypes.byref(dm), _stream(stream))
+    _check(st, "ipttt_chunk_forward")
+
+
+def workspace_size(batch: int, d: int, d_ff: int, dtype: int, L: int, B: int, rule, with_activations=True) -> int:
+    out = ctypes.c_size_t(0)
+    dm = dims(batch, d, d_ff, dtype)
+    _check(lib().ipttt_workspace_size(ctypes.byref(dm), int(L), int(B), _RULES[rule], int(bool(with_activations)),
+                                      ctypes.byref(out)), "ipttt_workspace_size")
+    return int(out.value)
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise the stream and return the device status (OK, ERR_TIMEOUT, ...)."""
+    return int(lib().ipttt_sync_status(_stream(stream)))
+
+
+def release() -> None:
+    _check(lib().ipttt_release(), "ipttt_release")

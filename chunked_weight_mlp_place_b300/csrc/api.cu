@@ -1,0 +1,588 @@
+// C-ABI of libipttt: argument checks, the per-device scratch pool, and the
+// order of kernel launches that makes up the In-Place TTT fast-weight layer.
+//
+// Layer (In-Place TTT write-ups: gated MLP itsolotime §2.1, target §2.3,
+// chunk-wise apply-then-update §2.2 / Fig. 1, su666666 "third axe"):
+//   Z = SiLU(X W_g) * (X W_u)                          one GEMM, gate epilogue
+//   V = Conv(E) P                                      conv kernel + GEMM
+//   MSE rule, for k = 0 .. K-1 (sequential):
+//     apply     O_acc = Z_k W_k          (bf16 W copy, split over d_ff, fp32 atomics)
+//     residual  O_k = O_acc; R_k = O_acc - V_k; O_acc = 0
+//     update    W_{k+1} = W_k - (eta/B) Z_k^T R_k; bf16 copy of W_{k+1}
+//   additive rule, chunk-parallel scan over G groups of g chunks (G*g = K):
+//     group sums   S_j = Z_{group j}^T V_{group j}           (all groups at once)
+//     scan         W^(j) = W_0 + (eta/B) sum_{i<j} S_i; W_final = W^(G)
+//     within every group at once, for its g chunks:
+//       apply O_k = Z_k W; update W += (eta/B) Z_k^T V_k (not after the last)
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "ipttt.h"
+#include "gemm.h"
+#include "launch.h"
+
+namespace ipttt {
+
+namespace {
+thread_local int64_t t_launches = 0;
+}
+
+void count_launch() { ++t_launches; }
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+// ------------------------------------------------------------------- pool
+struct Pool {
+  void* ptr = nullptr;
+  size_t size = 0;
+};
+std::mutex g_pool_mu;
+Pool g_pools[64];
+
+ipttt_status pool_reserve(size_t bytes, void** out) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return IPTTT_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_pool_mu);
+  Pool& p = g_pools[dev];
+  if (bytes > p.size) {
+    if (p.ptr) {
+      // The old block may still be read by queued kernels of earlier calls.
+      if (cudaDeviceSynchronize() != cudaSuccess) return IPTTT_ERR_CUDA;
+      cudaFree(p.ptr);
+      p.ptr = nullptr;
+      p.size = 0;
+    }
+    const size_t want = (bytes + (64u << 20) - 1) & ~static_cast<size_t>((64u << 20) - 1);
+    if (cudaMalloc(&p.ptr, want) != cudaSuccess) {
+      cudaGetLastError();
+      p.ptr = nullptr;
+      return IPTTT_ERR_ALLOC;
+    }
+    p.size = want;
+  }
+  *out = p.ptr;
+  return IPTTT_OK;
+}
+
+// Bump allocator over one pool block (256-byte aligned pieces).
+struct Carve {
+  size_t off = 0;
+  template <typename T>
+  size_t take(int64_t count) {
+    const size_t at = off;
+    off += (static_cast<size_t>(count) * sizeof(T) + 255) & ~static_cast<size_t>(255);
+    return at;
+  }
+};
+
+// ------------------------------------------------------------- checks
+ipttt_status from_cuda(cudaError_t e) {
+  switch (e) {
+    case cudaSuccess:
+      return IPTTT_OK;
+    case cudaErrorMemoryAllocation:
+      return IPTTT_ERR_ALLOC;
+    case cudaErrorInvalidValue:
+    case cudaErrorInvalidConfiguration:
+      return IPTTT_ERR_INVALID_ARG;
+    case cudaErrorNoKernelImageForDevice:
+    case cudaErrorInvalidDevice:
+    case cudaErrorNoDevice:
+    case cudaErrorInsufficientDriver:
+    case cudaErrorNotSupported:
+      return IPTTT_ERR_UNSUPPORTED;
+    case cudaErrorLaunchFailure:
+    case cudaErrorLaunchOutOfResources:
+    case cudaErrorInvalidDeviceFunction:
+      return IPTTT_ERR_LAUNCH;
+    default:
+      return IPTTT_ERR_CUDA;
+  }
+}
+
+#define IPTTT_TRY(expr)                        \
+  do {                                         \
+    const ipttt_status _s = (expr);            \
+    if (_s != IPTTT_OK) return _s;             \
+  } while (0)
+#define IPTTT_CUDA(expr)                       \
+  do {                                         \
+    const cudaError_t _e = (expr);             \
+    if (_e != cudaSuccess) {                   \
+      cudaGetLastError();                      \
+      return from_cuda(_e);                    \
+    }                                          \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ipttt_status check_dims(const ipttt_dims* dims, bool need_batch) {
+  if (!dims) return IPTTT_ERR_INVALID_ARG;
+  if (dims->dtype != IPTTT_FP32 && dims->dtype != IPTTT_BF16) return IPTTT_ERR_INVALID_ARG;
+  if (dims->d < 1 || dims->d_ff < 1) return IPTTT_ERR_INVALID_ARG;
+  if (need_batch && dims->batch < 0) return IPTTT_ERR_INVALID_ARG;
+  if (dims->w0_per_seq != 0 && dims->w0_per_seq != 1) return IPTTT_ERR_INVALID_ARG;
+  if (dims->d > (1 << 20) || dims->d_ff > (1 << 20)) return IPTTT_ERR_INVALID_ARG;
+  if (dims->dtype == IPTTT_BF16 && (dims->d % 8 || dims->d_ff % 8)) return IPTTT_ERR_INVALID_ARG;
+  return IPTTT_OK;
+}
+
+ipttt_status check_chunking(const ipttt_dims* dims, int64_t L, int64_t B) {
+  if (L < 0 || B < 1 || L % B) return IPTTT_ERR_INVALID_ARG;
+  if (dims->dtype == IPTTT_BF16 && B % 16) return IPTTT_ERR_INVALID_ARG;
+  // token rows and fast-weight rows are TMA coordinates (int32)
+  if (dims->batch > 0 && L > (int64_t{1} << 31) / dims->batch) return IPTTT_ERR_INVALID_ARG;
+  if (dims->batch > 0 && dims->d_ff * dims->batch > (int64_t{1} << 31)) return IPTTT_ERR_INVALID_ARG;
+  return IPTTT_OK;
+}
+
+// Pointer must be non-null, 16-byte aligned and reachable from the device.
+ipttt_status check_ptr_host(const void* p) {
+  if (!p || !aligned16(p)) return IPTTT_ERR_INVALID_ARG;
+  return IPTTT_OK;
+}
+ipttt_status check_ptr_device(const void* p) {
+  cudaPointerAttributes a;
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return IPTTT_ERR_INVALID_ARG;
+  return IPTTT_OK;
+}
+
+ipttt_status check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return IPTTT_ERR_UNSUPPORTED;
+  }
+  if (major != 10 || minor != 3) return IPTTT_ERR_UNSUPPORTED;
+  return IPTTT_OK;
+}
+
+// All pointers: host-side checks first (no CUDA call), then the device checks.
+template <size_t N>
+ipttt_status check_ptrs(const void* const (&ps)[N]) {
+  for (const void* p : ps) IPTTT_TRY(check_ptr_host(p));
+  IPTTT_TRY(check_device());
+  for (const void* p : ps) IPTTT_TRY(check_ptr_device(p));
+  return IPTTT_OK;
+}
+
+cudaError_t gemm(const GemmProblem& p, bool bf16, cudaStream_t st) {
+  return bf16 ? launch_gemm_tc(p, st) : launch_gemm_simt(p, st);
+}
+
+Operand mat(const void* ptr, int64_t rows, int64_t cols, int mn_major, int64_t y0 = 0, int64_t ys1 = 0,
+            int64_t ys2 = 0) {
+  Operand o;
+  o.ptr = ptr;
+  o.rows = rows;
+  o.cols = cols;
+  o.ld = cols;
+  o.mn_major = mn_major;
+  o.y0 = y0;
+  o.ys1 = ys1;
+  o.ys2 = ys2;
+  return o;
+}
+OutRef out(void* ptr, int64_t ld, int64_t y0 = 0, int64_t ys1 = 0, int64_t ys2 = 0) {
+  OutRef o;
+  o.ptr = ptr;
+  o.ld = ld;
+  o.y0 = y0;
+  o.ys1 = ys1;
+  o.ys2 = ys2;
+  return o;
+}
+
+size_t act_size(const ipttt_dims* d) { return d->dtype == IPTTT_BF16 ? 2 : 4; }
+
+// ---------------------------------------------------------------- steps
+ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, int64_t T, const ipttt_dims* dm,
+                      cudaStream_t st) {
+  const bool bf16 = dm->dtype == IPTTT_BF16;
+  GemmProblem p;
+  p.M = T;
+  p.N = dm->d_ff;
+  p.K = dm->d;
+  p.A = mat(X, T, dm->d, 0);
+  p.B = mat(W_g, dm->d, dm->d_ff, 1);
+  p.B2 = mat(W_u, dm->d, dm->d_ff, 1);
+  p.epi = EPI_GATE;
+  p.out_bf16 = bf16;
+  p.D = out(Z, dm->d_ff);
+  IPTTT_CUDA(gemm(p, bf16, st));
+  return IPTTT_OK;
+}
+
+ipttt_status run_targets(const void* E, const float* conv_w, const void* P, void* V, void* C, int64_t rows,
+                         int64_t L, int64_t B, const ipttt_dims* dm, cudaStream_t st) {
+  const bool bf16 = dm->dtype == IPTTT_BF16;
+  IPTTT_CUDA(launch_conv(E, conv_w, C, rows, L, B, dm->d, bf16, st));
+  GemmProblem p;
+  p.M = rows;
+  p.N = dm->d;
+  p.K = dm->d;
+  p.A = mat(C, rows, dm->d, 0);
+  p.B = mat(P, dm->d, dm->d, 1);
+  p.epi = EPI_STORE;
+  p.out_bf16 = bf16;
+  p.D = out(V, dm->d);
+  IPTTT_CUDA(gemm(p, bf16, st));
+  return IPTTT_OK;
+}
+
+// Number of groups of the additive scan: the largest divisor of K not above 8.
+int64_t scan_groups(int64_t K) {
+  for (int64_t G = std::min<int64_t>(8, K); G > 1; --G)
+    if (K % G == 0) return G;
+  return 1;
+}
+
+struct EngineLayout {
+  size_t o_acc = 0, r = 0, wb = 0, d = 0, db = 0, total = 0;
+};
+
+EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rule rule, size_t base) {
+  EngineLayout e;
+  Carve c;
+  c.off = base;
+  const bool bf16 = dm->dtype == IPTTT_BF16;
+  const int64_t K = L / B;
+  const int64_t nw = dm->d_ff * dm->d;
+  if (rule == IPTTT_RULE_MSE) {
+    e.o_acc = c.take<float>(dm->batch * B * dm->d);
+    e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
+    if (bf16) e.wb = c.take<uint16_t>(dm->batch * nw);
+  } else {
+    const int64_t G = scan_groups(K);
+    e.o_acc = c.take<float>(G * dm->batch * B * dm->d);
+    e.d = c.take<float>(G * dm->batch * nw);
+    if (bf16) e.db = c.take<uint16_t>(G * dm->batch * nw);
+  }
+  e.total = c.off;
+  return e;
+}
+
+ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L, int64_t B, float eta,
+                        ipttt_rule rule, void* O, float* Wf, const ipttt_dims* dm, uint8_t* ws, const EngineLayout& lay,
+                        cudaStream_t st) {
+  const bool bf16 = dm->dtype == IPTTT_BF16;
+  const int64_t batch = dm->batch, d = dm->d, dff = dm->d_ff, K = L / B, nw = dff * d;
+  const int64_t w0s = dm->w0_per_seq ? nw : 0;  // element stride between sequences' W_o0
+  const int64_t w0r = dm->w0_per_seq ? dff : 0;  // same, in rows
+  const int bint = static_cast<int>(batch);
+  float* o_acc = reinterpret_cast<float*>(ws + lay.o_acc);
+
+  if (rule == IPTTT_RULE_MSE) {
+    void* R = ws + lay.r;
+    __nv_bfloat16* Wb = bf16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.wb) : nullptr;
+    if (bf16) IPTTT_CUDA(launch_to_bf16(W0, w0s, Wb, batch, nw, st));
+    IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * B * d, st));
+    for (int64_t k = 0; k < K; ++k) {
+      // apply: O_acc[s] = Z_k[s] W_k[s]
+      GemmProblem a;
+      a.M = B;
+      a.N = d;
+      a.K = dff;
+      a.nb1 = bint;
+      a.A = mat(Z, batch * L, dff, 0, k * B, L);
+      if (bf16)
+        a.B = mat(Wb, batch * dff, d, 1, 0, dff);
+      else
+        a.B = (k == 0) ? mat(W0, (dm->w0_per_seq ? batch : 1) * dff, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
+      a.epi = EPI_ACCUM;
+      a.D = out(o_acc, d, 0, B);
+      a.split_k = 1;
+      IPTTT_CUDA(gemm(a, bf16, st));
+      // residual: O_k = O_acc, R_k = O_acc - V_k, O_acc = 0
+      ResidualArgs ra;
+      ra.acc = o_acc;
+      ra.V = V;
+      ra.O = O;
+      ra.R = R;
+      ra.B = B;
+      ra.d = d;
+      ra.nb1 = bint;
+      ra.o_y0 = k * B;
+      ra.o_ys1 = L;
+      IPTTT_CUDA(launch_residual(ra, bf16, st));
+      // update: W_{k+1} = W_k - (eta/B) Z_k^T R_k
+      GemmProblem u;
+      u.M = dff;
+      u.N = d;
+      u.K = B;
+      u.nb1 = bint;
+      u.A = mat(Z, batch * L, dff, 1, k * B, L);
+      u.B = mat(R, batch * B, d, 1, 0, B);
+      u.epi = EPI_AXPY;
+      u.D = out(Wf, d, 0, dff);
+      u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r) : out(Wf, d, 0, dff);
+      if (bf16 && k + 1 < K) u.Db = out(Wb, d, 0, dff);
+      u.alpha = -eta / static_cast<float>(B);
+      IPTTT_CUDA(gemm(u, bf16, st));
+    }
+    return IPTTT_OK;
+  }
+
+  // additive rule: chunk-parallel scan
+  const int64_t G = scan_groups(K), g = K / G;
+  const int gint = static_cast<int>(G);
+  float* D = reinterpret_cast<float*>(ws + lay.d);
+  __nv_bfloat16* Db = bf16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.db) : nullptr;
+  const float alpha = eta / static_cast<float>(B);
+  // group sums, all groups of all sequences at once
+  GemmProblem s;
+  s.M = dff;
+  s.N = d;
+  s.K = g * B;
+  s.nb1 = bint;
+  s.nb2 = gint;
+  s.A = mat(Z, batch * L, dff, 1, 0, L, g * B);
+  s.B = mat(V, batch * L, d, 1, 0, L, g * B);
+  s.epi = EPI_STORE;
+  s.out_bf16 = 0;
+  s.D = out(D, d, 0, dff, batch * dff);
+  IPTTT_CUDA(gemm(s, bf16, st));
+  // exclusive scan over groups -> the fast weight at the start of each group
+  IPTTT_CUDA(launch_group_scan(D, Db, W0, w0s, Wf, G, batch, nw, alpha, st));
+  IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * G * batch * B * d, st));
+  for (int64_t i = 0; i < g; ++i) {
+    GemmProblem a;
+    a.M = B;
+    a.N = d;
+    a.K = dff;
+    a.nb1 = bint;
+    a.nb2 = gint;
+    a.A = mat(Z, batch * L, dff, 0, i * B, L, g * B);
+    a.B = bf16 ? mat(Db, G * batch * dff, d, 1, 0, dff, batch * dff) : mat(D, G * batch * dff, d, 1, 0, dff, batch * dff);
+    a.epi = EPI_ACCUM;
+    a.D = out(o_acc, d, 0, B, batch * B);
+    a.split_k = 1;
+    IPTTT_CUDA(gemm(a, bf16, st));
+    ResidualArgs ra;
+    ra.acc = o_acc;
+    ra.O = O;
+    ra.B = B;
+    ra.d = d;
+    ra.nb1 = bint;
+    ra.nb2 = gint;
+    ra.o_y0 = i * B;
+    ra.o_ys1 = L;
+    ra.o_ys2 = g * B;
+    IPTTT_CUDA(launch_residual(ra, bf16, st));
+    if (i + 1 < g) {
+      GemmProblem u;
+      u.M = dff;
+      u.N = d;
+      u.K = B;
+      u.nb1 = bint;
+      u.nb2 = gint;
+      u.A = mat(Z, batch * L, dff, 1, i * B, L, g * B);
+      u.B = mat(V, batch * L, d, 1, i * B, L, g * B);
+      u.epi = EPI_AXPY;
+      u.D = out(D, d, 0, dff, batch * dff);
+      u.src = u.D;
+      if (bf16) u.Db = out(Db, d, 0, dff, batch * dff);
+      u.alpha = alpha;
+      IPTTT_CUDA(gemm(u, bf16, st));
+    }
+  }
+  return IPTTT_OK;
+}
+
+struct LaunchScope {
+  LaunchScope() { t_launches = 0; }
+};
+
+}  // namespace
+}  // namespace ipttt
+
+using namespace ipttt;
+
+extern "C" {
+
+ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, ipttt_rule rule,
+                                  int32_t with_activations, size_t* bytes) {
+  IPTTT_TRY(check_dims(dims, true));
+  IPTTT_TRY(check_chunking(dims, L, B));
+  if (!bytes || (rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD)) return IPTTT_ERR_INVALID_ARG;
+  size_t base = 0;
+  if (with_activations) {
+    Carve c;
+    const int64_t T = dims->batch * L;
+    const size_t es = act_size(dims);
+    c.off += (static_cast<size_t>(T * dims->d_ff) * es + 255) & ~size_t(255);  // Z
+    c.off += (static_cast<size_t>(T * dims->d) * es + 255) & ~size_t(255);     // V
+    c.off += (static_cast<size_t>(T * dims->d) * es + 255) & ~size_t(255);     // conv output
+    base = c.off;
+  }
+  *bytes = (L == 0 || dims->batch == 0) ? 0 : engine_layout(dims, L, B, rule, base).total;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_gate_up(const void* X, const void* W_g, const void* W_u, void* Z, int64_t n_tokens,
+                           const ipttt_dims* dims, ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, false));
+  if (n_tokens < 0 || n_tokens > (int64_t{1} << 31)) return IPTTT_ERR_INVALID_ARG;
+  if (n_tokens == 0) return IPTTT_OK;
+  IPTTT_TRY(check_ptrs({X, W_g, W_u, static_cast<const void*>(Z)}));
+  return run_gate(X, W_g, W_u, Z, n_tokens, dims, static_cast<cudaStream_t>(stream));
+}
+
+ipttt_status ipttt_make_targets(const void* E, const float* conv_w, const void* P, void* V, int64_t L, int64_t B,
+                                const ipttt_dims* dims, ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, true));
+  IPTTT_TRY(check_chunking(dims, L, B));
+  const int64_t rows = dims->batch * L;
+  if (rows == 0) return IPTTT_OK;
+  IPTTT_TRY(check_ptrs({E, static_cast<const void*>(conv_w), P, static_cast<const void*>(V)}));
+  void* ws = nullptr;
+  IPTTT_TRY(pool_reserve(static_cast<size_t>(rows * dims->d) * act_size(dims), &ws));
+  return run_targets(E, conv_w, P, V, ws, rows, L, B, dims, static_cast<cudaStream_t>(stream));
+}
+
+ipttt_status ipttt_chunk_forward(const void* Z, const void* V, const float* W_o0, int64_t L, int64_t B, float eta,
+                                 ipttt_rule rule, void* O, float* W_final, const ipttt_dims* dims,
+                                 ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, true));
+  IPTTT_TRY(check_chunking(dims, L, B));
+  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
+  if (dims->batch == 0) return IPTTT_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t nw = dims->d_ff * dims->d;
+  if (L == 0) {
+    IPTTT_TRY(check_ptrs({static_cast<const void*>(W_o0), static_cast<const void*>(W_final)}));
+    IPTTT_CUDA(launch_copy_w(W_o0, dims->w0_per_seq ? nw : 0, W_final, dims->batch, nw, st));
+    return IPTTT_OK;
+  }
+  IPTTT_TRY(check_ptrs({Z, V, static_cast<const void*>(W_o0), static_cast<const void*>(O),
+                        static_cast<const void*>(W_final)}));
+  const EngineLayout lay = engine_layout(dims, L, B, rule, 0);
+  void* ws = nullptr;
+  IPTTT_TRY(pool_reserve(lay.total, &ws));
+  return run_engine(Z, V, W_o0, L, B, eta, rule, O, W_final, dims, static_cast<uint8_t*>(ws), lay, st);
+}
+
+ipttt_status ipttt_layer_forward(const void* X, const void* E, const void* W_g, const void* W_u, const float* W_o0,
+                                 const float* conv_w, const void* P, int64_t L, int64_t B, float eta,
+                                 ipttt_rule rule, void* O, float* W_final, const ipttt_dims* dims,
+                                 ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, true));
+  IPTTT_TRY(check_chunking(dims, L, B));
+  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
+  if (dims->batch == 0) return IPTTT_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t nw = dims->d_ff * dims->d;
+  if (L == 0) {
+    IPTTT_TRY(check_ptrs({static_cast<const void*>(W_o0), static_cast<const void*>(W_final)}));
+    IPTTT_CUDA(launch_copy_w(W_o0, dims->w0_per_seq ? nw : 0, W_final, dims->batch, nw, st));
+    return IPTTT_OK;
+  }
+  IPTTT_TRY(check_ptrs({X, E, W_g, W_u, static_cast<const void*>(W_o0), static_cast<const void*>(conv_w), P,
+                        static_cast<const void*>(O), static_cast<const void*>(W_final)}));
+  const int64_t T = dims->batch * L;
+  const size_t es = act_size(dims);
+  Carve c;
+  const size_t z_off = c.take<uint8_t>(T * dims->d_ff * static_cast<int64_t>(es));
+  const size_t v_off = c.take<uint8_t>(T * dims->d * static_cast<int64_t>(es));
+  const size_t c_off = c.take<uint8_t>(T * dims->d * static_cast<int64_t>(es));
+  const EngineLayout lay = engine_layout(dims, L, B, rule, c.off);
+  void* wsv = nullptr;
+  IPTTT_TRY(pool_reserve(lay.total, &wsv));
+  uint8_t* ws = static_cast<uint8_t*>(wsv);
+  IPTTT_TRY(run_gate(X, W_g, W_u, ws + z_off, T, dims, st));
+  IPTTT_TRY(run_targets(E, conv_w, P, ws + v_off, ws + c_off, T, L, B, dims, st));
+  return run_engine(ws + z_off, ws + v_off, W_o0, L, B, eta, rule, O, W_final, dims, ws, lay, st);
+}
+
+ipttt_status ipttt_sync_status(ipttt_stream stream) {
+  const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return from_cuda(e);
+  }
+  int code = 0;
+  if (read_clear_device_error(&code) != cudaSuccess) {
+    cudaGetLastError();
+    return IPTTT_ERR_CUDA;
+  }
+  return code ? IPTTT_ERR_TIMEOUT : IPTTT_OK;
+}
+
+ipttt_status ipttt_release(void) {
+  std::lock_guard<std::mutex> g(g_pool_mu);
+  int cur = -1;
+  cudaGetDevice(&cur);
+  for (int dev = 0; dev < 64; ++dev) {
+    if (!g_pools[dev].ptr) continue;
+    cudaSetDevice(dev);
+    cudaFree(g_pools[dev].ptr);
+    g_pools[dev].ptr = nullptr;
+    g_pools[dev].size = 0;
+  }
+  if (cur >= 0) cudaSetDevice(cur);
+  cudaGetLastError();
+  return IPTTT_OK;
+}
+
+int64_t ipttt_last_launch_count(void) { return t_launches; }
+
+const char* ipttt_status_string(ipttt_status s) {
+  switch (s) {
+    case IPTTT_OK:
+      return "ok";
+    case IPTTT_ERR_INVALID_ARG:
+      return "invalid argument";
+    case IPTTT_ERR_UNSUPPORTED:
+      return "unsupported device (needs compute capability 10.3)";
+    case IPTTT_ERR_ALLOC:
+      return "scratch allocation failed";
+    case IPTTT_ERR_LAUNCH:
+      return "kernel launch failed";
+    case IPTTT_ERR_TIMEOUT:
+      return "a device-side wait ran out of time";
+    case IPTTT_ERR_CUDA:
+      return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+int ipttt_version(void) { return IPTTT_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,275 @@
+// Memory-bound kernels of the layer: the chunk-padded depthwise conv of the
+// target builder, the residual / output epilogue of the apply step, the bf16
+// copy of the fast weight and the group scan of the additive rule.  All are
+// grid-stride loops over 16-byte vectors, sized to a multiple of the SM count.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ipttt {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(int64_t work_items) {
+  const int64_t per_wave = static_cast<int64_t>(device_sm_count()) * (2048 / kThreads);
+  int64_t g = (work_items + kThreads - 1) / kThreads;
+  if (g > per_wave * 4) g = per_wave * 4;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+// ---------------------------------------------------------------------- conv
+// C[t, c] = sum_{j<4} w[c, j] * E[t+j, c], with E[t+j] read as zero once t+j
+// leaves the chunk of B tokens holding t (In-Place TTT target, itsolotime §2.3).
+// One thread: VEC channels x TT consecutive tokens, sliding a 4-row window.
+template <typename T, int VEC, int TT>
+__global__ void __launch_bounds__(kThreads) conv_kernel(const T* __restrict__ E, const float* __restrict__ w,
+                                                        T* __restrict__ C, int64_t rows, int64_t L, int64_t B,
+                                                        int64_t d) {
+  const int64_t cgroups = d / VEC;
+  const int64_t tblocks = (rows + TT - 1) / TT;
+  const int64_t total = cgroups * tblocks;
+  for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
+       item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t cg = item % cgroups, tb = item / cgroups;
+    const int64_t c0 = cg * VEC, r0 = tb * TT;
+    float wt[4][VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      const float4 q = *reinterpret_cast<const float4*>(w + (c0 + v) * 4);
+      wt[0][v] = q.x;
+      wt[1][v] = q.y;
+      wt[2][v] = q.z;
+      wt[3][v] = q.w;
+    }
+    // window of rows r0 .. r0+TT+2 (rows past their chunk end are masked per output)
+    float win[TT + 3][VEC];
+#pragma unroll
+    for (int i = 0; i < TT + 3; ++i) {
+      const int64_t r = r0 + i;
+      if (r < rows) {
+        const T* src = E + r * d + c0;
+        if constexpr (VEC == 8 && sizeof(T) == 2) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(src);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float2 f = __bfloat1622float2(h[v]);
+            win[i][2 * v] = f.x;
+            win[i][2 * v + 1] = f.y;
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) win[i][v] = to_f32<T>(src[v]);
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) win[i][v] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < TT; ++i) {
+      const int64_t r = r0 + i;
+      if (r >= rows) break;
+      const int64_t t = r % L;                      // position in its sequence
+      const int64_t room = (t / B + 1) * B - t;     // rows left in the chunk, counting t
+      float acc[VEC];
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) acc[v] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < room) {
+#pragma unroll
+          for (int v = 0; v < VEC; ++v) acc[v] = fmaf(wt[j][v], win[i + j][v], acc[v]);
+        }
+      }
+      T* dst = C + r * d + c0;
+      if constexpr (VEC == 8 && sizeof(T) == 2) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(dst) = o;
+      } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) dst[v] = from_f32<T>(acc[v]);
+      }
+    }
+  }
+}
+
+// Scalar-weight variant for fp32 mode with any d: one channel per thread.
+__global__ void __launch_bounds__(kThreads) conv_kernel_scalar(const float* __restrict__ E,
+                                                               const float* __restrict__ w, float* __restrict__ C,
+                                                               int64_t rows, int64_t L, int64_t B, int64_t d) {
+  const int64_t total = rows * d;
+  for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
+       item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t c = item % d, r = item / d;
+    const int64_t t = r % L;
+    const int64_t room = (t / B + 1) * B - t;
+    float acc = 0.0f;
+    for (int j = 0; j < 4 && j < room; ++j) acc = fmaf(w[c * 4 + j], E[(r + j) * d + c], acc);
+    C[r * d + c] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ residual
+template <typename T>
+__global__ void __launch_bounds__(kThreads) residual_kernel(const ResidualArgs a) {
+  const int64_t per_entry = a.B * a.d;
+  const int64_t total = per_entry * a.nb1 * a.nb2;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = idx / per_entry, rem = idx % per_entry;
+    const int64_t i = rem / a.d, c = rem % a.d;
+    const int b1 = static_cast<int>(e % a.nb1), b2 = static_cast<int>(e / a.nb1);
+    const int64_t orow = a.o_y0 + b1 * a.o_ys1 + b2 * a.o_ys2 + i;
+    const float v = a.acc[idx];
+    a.acc[idx] = 0.0f;
+    static_cast<T*>(a.O)[orow * a.d + c] = from_f32<T>(v);
+    if (a.R) static_cast<T*>(a.R)[idx] = from_f32<T>(v - to_f32<T>(static_cast<const T*>(a.V)[orow * a.d + c]));
+  }
+}
+
+// Vectorised bf16 variant (d % 8 == 0): 8 columns per thread.
+__global__ void __launch_bounds__(kThreads) residual_kernel_bf16x8(const ResidualArgs a) {
+  const int64_t dv = a.d / 8;
+  const int64_t per_entry = a.B * dv;
+  const int64_t total = per_entry * a.nb1 * a.nb2;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = idx / per_entry, rem = idx % per_entry;
+    const int64_t i = rem / dv, c = (rem % dv) * 8;
+    const int b1 = static_cast<int>(e % a.nb1), b2 = static_cast<int>(e / a.nb1);
+    const int64_t orow = a.o_y0 + b1 * a.o_ys1 + b2 * a.o_ys2 + i;
+    float4* accp = reinterpret_cast<float4*>(a.acc + (e * a.B + i) * a.d + c);
+    const float4 x0 = accp[0], x1 = accp[1];
+    accp[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    accp[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    uint4 o;
+    o.x = pack_bf16x2(x0.x, x0.y);
+    o.y = pack_bf16x2(x0.z, x0.w);
+    o.z = pack_bf16x2(x1.x, x1.y);
+    o.w = pack_bf16x2(x1.z, x1.w);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + orow * a.d + c) = o;
+    if (a.R) {
+      const uint4 vr = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.V) + orow * a.d + c);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr);
+      const float2 v0 = __bfloat1622float2(h[0]), v1 = __bfloat1622float2(h[1]), v2 = __bfloat1622float2(h[2]),
+                   v3 = __bfloat1622float2(h[3]);
+      uint4 r;
+      r.x = pack_bf16x2(x0.x - v0.x, x0.y - v0.y);
+      r.y = pack_bf16x2(x0.z - v1.x, x0.w - v1.y);
+      r.z = pack_bf16x2(x1.x - v2.x, x1.y - v2.y);
+      r.w = pack_bf16x2(x1.z - v3.x, x1.w - v3.y);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.R) + (e * a.B + i) * a.d + c) = r;
+    }
+  }
+}
+
+// -------------------------------------------------------------- fast weight
+__global__ void __launch_bounds__(kThreads) to_bf16_kernel(const float* __restrict__ W0, int64_t w0_stride,
+                                                           __nv_bfloat16* __restrict__ Wb, int64_t batch,
+                                                           int64_t n) {
+  const int64_t nq = n / 4;
+  const int64_t total = nq * batch;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t s = idx / nq, q = idx % nq;
+    const float4 x = reinterpret_cast<const float4*>(W0 + s * w0_stride)[q];
+    uint2 o;
+    o.x = pack_bf16x2(x.x, x.y);
+    o.y = pack_bf16x2(x.z, x.w);
+    reinterpret_cast<uint2*>(Wb + s * n)[q] = o;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) copy_w_kernel(const float* __restrict__ W0, int64_t w0_stride,
+                                                          float* __restrict__ W, int64_t batch, int64_t n) {
+  const int64_t total = n * batch;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t s = idx / n, q = idx % n;
+    W[idx] = W0[s * w0_stride + q];
+  }
+}
+
+// Exclusive prefix over the G group sums of the additive rule, turning each
+// sum into the fast weight at the start of its group.
+__global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict__ D, __nv_bfloat16* __restrict__ Db,
+                                                              const float* __restrict__ W0, int64_t w0_stride,
+                                                              float* __restrict__ Wf, int64_t G, int64_t batch,
+                                                              int64_t n, float alpha) {
+  const int64_t total = n * batch;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t s = idx / n, q = idx % n;
+    float S = W0[s * w0_stride + q];
+    for (int64_t g = 0; g < G; ++g) {
+      const int64_t at = g * total + idx;
+      const float t = D[at];
+      D[at] = S;
+      if (Db) Db[at] = __float2bfloat16_rn(S);
+      S = fmaf(alpha, t, S);
+    }
+    Wf[idx] = S;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t rows, int64_t L, int64_t B, int64_t d,
+                        bool bf16, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  count_launch();
+  if (bf16) {
+    constexpr int TT = 8;
+    const int64_t items = (d / 8) * ((rows + TT - 1) / TT);
+    conv_kernel<__nv_bfloat16, 8, TT><<<grid_for(items), kThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(E), conv_w, static_cast<__nv_bfloat16*>(C), rows, L, B, d);
+  } else {
+    conv_kernel_scalar<<<grid_for(rows * d), kThreads, 0, stream>>>(static_cast<const float*>(E), conv_w,
+                                                                     static_cast<float*>(C), rows, L, B, d);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t stream) {
+  const int64_t total = a.B * a.d * a.nb1 * a.nb2;
+  if (total <= 0) return cudaSuccess;
+  count_launch();
+  if (bf16 && a.d % 8 == 0)
+    residual_kernel_bf16x8<<<grid_for(total / 8), kThreads, 0, stream>>>(a);
+  else if (bf16)
+    residual_kernel<__nv_bfloat16><<<grid_for(total), kThreads, 0, stream>>>(a);
+  else
+    residual_kernel<float><<<grid_for(total), kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16(const float* W0, int64_t w0_stride, __nv_bfloat16* Wb, int64_t batch, int64_t n,
+                           cudaStream_t stream) {
+  if (n % 4) return cudaErrorInvalidValue;
+  count_launch();
+  to_bf16_kernel<<<grid_for(n / 4 * batch), kThreads, 0, stream>>>(W0, w0_stride, Wb, batch, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
+                          cudaStream_t stream) {
+  count_launch();
+  copy_w_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(W0, w0_stride, W, batch, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_scan(float* D, __nv_bfloat16* Db, const float* W0, int64_t w0_stride, float* W_final,
+                              int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream) {
+  count_launch();
+  group_scan_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(D, Db, W0, w0_stride, W_final, G, batch, n,
+                                                                  alpha);
+  return cudaGetLastError();
+}
+
+}  // namespace ipttt

@@ -1,0 +1,535 @@
+// Tensor-core back end of the batched GEMM (IPTTT_BF16 mode) for sm_103a.
+//
+// One persistent kernel template serves the four contractions of the layer:
+//   gate   Z = SiLU(X W_g) * (X W_u)       A = X   (K-major)  B = W_g, W_u (MN-major)
+//   proj   V = C P                          A = C   (K-major)  B = P        (MN-major)
+//   apply  O_k += Z_k W_k  (split over K)   A = Z_k (K-major)  B = W_k bf16 (MN-major)
+//   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k      (MN-major)
+//
+// Each CTA (one per SM) runs six warps:
+//   warp 0      TMA producer: 128x64 A tiles and 64-wide B tiles into a ring of
+//               shared-memory stages (128-byte swizzle), completion on mbarriers;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, K=16) into a
+//               TMEM accumulator, and tcgen05.commit frees each stage;
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output
+//               row) and apply the fused epilogue straight to global memory.
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
+// the main loop of the next.  Work is either whole output tiles, strided over
+// the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
+// share of the (tile, k-block) iteration space per CTA whose partial sums are
+// added into an fp32 buffer with vector atomics.
+//
+// Every mbarrier wait is capped (common.cuh); a CTA whose wait runs out flags
+// the others, drains its in-flight TMA copies and MMAs, frees its TMEM and
+// returns, leaving a code in the device error word.
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "launch.h"
+
+namespace ipttt {
+
+// Error word written by kernels whose capped waits ran out (0 = none); read
+// and cleared through read_clear_device_error().  Codes: 1 = TMA-producer
+// wait, 2 = MMA-issuer wait, 3 = epilogue wait, 4 = teardown drain.
+__device__ int g_device_error = 0;
+
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kAccStride = 256;  // TMEM columns between the two accumulator buffers
+
+template <int BN, int NB>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr int STAGES = (196 * 1024) / STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(BN * NB <= kAccStride, "accumulator too wide");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(STAGES >= 2, "stages");
+};
+
+struct Seg {
+  int64_t tile;
+  int kb0, kb1;
+};
+
+// Work decomposition shared by the three roles (each walks it independently).
+struct Sched {
+  int64_t n_mt, n_nt, tiles_per_batch, total_tiles;
+  int kb_total;
+  int group_m;
+  int split;
+  int64_t total_iters;
+
+  __device__ void tile_coords(int64_t t, int& bi, int64_t& mt, int64_t& nt) const {
+    bi = static_cast<int>(t / tiles_per_batch);
+    const int64_t r = t % tiles_per_batch;
+    const int64_t gsz = static_cast<int64_t>(group_m) * n_nt;
+    const int64_t g = r / gsz;
+    const int64_t first_m = g * group_m;
+    const int64_t gm = min(static_cast<int64_t>(group_m), n_mt - first_m);
+    const int64_t q = r % gsz;
+    mt = first_m + q % gm;
+    nt = q / gm;
+  }
+};
+
+struct SegIter {
+  const Sched* s;
+  int64_t t, it, it_end;
+  __device__ void init(const Sched* sc) {
+    s = sc;
+    if (s->split) {
+      const int64_t G = gridDim.x;
+      it = s->total_iters * blockIdx.x / G;
+      it_end = s->total_iters * (blockIdx.x + 1) / G;
+    } else {
+      t = blockIdx.x;
+    }
+  }
+  __device__ bool next(Seg& g) {
+    if (s->split) {
+      if (it >= it_end) return false;
+      g.tile = it / s->kb_total;
+      g.kb0 = static_cast<int>(it % s->kb_total);
+      const int64_t rem = it_end - it;
+      g.kb1 = static_cast<int>(min(static_cast<int64_t>(s->kb_total), g.kb0 + rem));
+      it += g.kb1 - g.kb0;
+      return true;
+    }
+    if (t >= s->total_tiles) return false;
+    g.tile = t;
+    g.kb0 = 0;
+    g.kb1 = s->kb_total;
+    t += gridDim.x;
+    return true;
+  }
+};
+
+struct KParams {
+  GemmProblem p;
+  Sched s;
+};
+
+__device__ __forceinline__ int64_t row_of(const Operand& o, int b1, int b2) {
+  return o.y0 + b1 * o.ys1 + b2 * o.ys2;
+}
+__device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) {
+  return o.y0 + b1 * o.ys1 + b2 * o.ys2;
+}
+
+// Issue the TMA copies of one operand tile (extent `ext` along M or N, BK along K).
+template <bool MN, int EXT>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int64_t row0,
+                                             int64_t i0, int64_t k0) {
+  if constexpr (MN) {
+#pragma unroll
+    for (int j = 0; j < EXT / 64; ++j)
+      tma_load_2d(dst + j * (64 * BK * 2), map, bar, static_cast<int>(i0 + 64 * j), static_cast<int>(row0 + k0));
+  } else {
+    tma_load_2d(dst, map, bar, static_cast<int>(k0), static_cast<int>(row0 + i0));
+  }
+}
+
+// Shared-memory descriptor of the k-th 16-wide K step of an operand tile.
+//  K-major: rows of 128 bytes (64 K elements), 8-row groups 1024 bytes apart;
+//           the K step advances the start by 32 bytes inside the swizzle atom.
+//  MN-major: 64-element column blocks of 64 K rows (8 KB) side by side; 8-row
+//           K groups 1024 bytes apart (SBO), column blocks 8 KB apart (LBO);
+//           the K step advances the start by 16 rows = 2048 bytes.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kstep) {
+  if constexpr (MN)
+    return make_smem_desc_sw128(base + kstep * 2048, 64 * BK * 2, 1024);
+  else
+    return make_smem_desc_sw128(base + kstep * 32, 16, 1024);
+}
+
+template <int EPI, bool OUT_BF16>
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
+                                               const uint32_t (&r)[32], const uint32_t (&u)[32]) {
+  const bool full = (n + 32 <= p.N);
+  if constexpr (EPI == EPI_STORE || EPI == EPI_GATE) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = __uint_as_float(r[i]);
+      if constexpr (EPI == EPI_GATE)
+        v[i] = silu_f(a) * __uint_as_float(u[i]);
+      else
+        v[i] = a;
+    }
+    const int64_t row = row_of(p.D, b1, b2) + m;
+    if constexpr (OUT_BF16) {
+      __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D.ptr) + row * p.D.ld + n;
+      if (full) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+          w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+          w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+          w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+          reinterpret_cast<uint4*>(d)[q] = w;
+        }
+      } else {
+        for (int i = 0; i < 32 && n + i < p.N; ++i) d[i] = __float2bfloat16_rn(v[i]);
+      }
+    } else {
+      float* d = static_cast<float*>(p.D.ptr) + row * p.D.ld + n;
+      if (full) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<float4*>(d)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else {
+        for (int i = 0; i < 32 && n + i < p.N; ++i) d[i] = v[i];
+      }
+    }
+  } else if constexpr (EPI == EPI_ACCUM) {
+    const int64_t row = row_of(p.D, b1, b2) + m;
+    float* d = static_cast<float*>(p.D.ptr) + row * p.D.ld + n;
+    if (full) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        atomicAdd(reinterpret_cast<float4*>(d) + q,
+                  make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                              __uint_as_float(r[4 * q + 3])));
+    } else {
+      for (int i = 0; i < 32 && n + i < p.N; ++i) atomicAdd(d + i, __uint_as_float(r[i]));
+    }
+  } else {  // EPI_AXPY
+    const int64_t row = row_of(p.D, b1, b2) + m;
+    const int64_t srow = row_of(p.src, b1, b2) + m;
+    float* d = static_cast<float*>(p.D.ptr) + row * p.D.ld + n;
+    const float* s = static_cast<const float*>(p.src.ptr) + srow * p.src.ld + n;
+    __nv_bfloat16* db = nullptr;
+    if (p.Db.ptr) db = static_cast<__nv_bfloat16*>(p.Db.ptr) + (row_of(p.Db, b1, b2) + m) * p.Db.ld + n;
+    if (full) {
+      float w[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = reinterpret_cast<const float4*>(s)[q];
+        w[4 * q + 0] = fmaf(p.alpha, __uint_as_float(r[4 * q + 0]), x.x);
+        w[4 * q + 1] = fmaf(p.alpha, __uint_as_float(r[4 * q + 1]), x.y);
+        w[4 * q + 2] = fmaf(p.alpha, __uint_as_float(r[4 * q + 2]), x.z);
+        w[4 * q + 3] = fmaf(p.alpha, __uint_as_float(r[4 * q + 3]), x.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(d)[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      if (db) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 o;
+          o.x = pack_bf16x2(w[8 * q + 0], w[8 * q + 1]);
+          o.y = pack_bf16x2(w[8 * q + 2], w[8 * q + 3]);
+          o.z = pack_bf16x2(w[8 * q + 4], w[8 * q + 5]);
+          o.w = pack_bf16x2(w[8 * q + 6], w[8 * q + 7]);
+          reinterpret_cast<uint4*>(db)[q] = o;
+        }
+      }
+    } else {
+      for (int i = 0; i < 32 && n + i < p.N; ++i) {
+        const float w = fmaf(p.alpha, __uint_as_float(r[i]), s[i]);
+        d[i] = w;
+        if (db) db[i] = __float2bfloat16_rn(w);
+      }
+    }
+  }
+}
+
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ KParams kp) {
+  using C = Cfg<BN, NB>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full_bar = bars;                       // [STAGES]
+  uint64_t* empty_bar = bars + C::STAGES;          // [STAGES]
+  uint64_t* tfull_bar = bars + 2 * C::STAGES;      // [2]
+  uint64_t* tempty_bar = bars + 2 * C::STAGES + 2; // [2]
+  uint64_t* drain_bar = bars + 2 * C::STAGES + 4;  // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const GemmProblem& p = kp.p;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < C::STAGES; ++i) {
+        mbar_init(&full_bar[i], 1);
+        mbar_init(&empty_bar[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&tfull_bar[i], 1);
+        mbar_init(&tempty_bar[i], 128);
+      }
+      mbar_init(drain_bar, 1);
+      *abort_flag = 0;
+      fence_mbarrier_init();
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      if constexpr (NB == 2) tma_prefetch_desc(&tmB2);
+    }
+    __syncwarp();
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  SegIter iter;
+  iter.init(&kp.s);
+  Seg seg;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kc = 0;
+      uint32_t issued_mask = 0;
+      bool ok = true;
+      while (ok && iter.next(seg)) {
+        int bi;
+        int64_t mt, nt;
+        kp.s.tile_coords(seg.tile, bi, mt, nt);
+        const int b1 = bi % p.nb1, b2 = bi / p.nb1;
+        const int64_t ra = row_of(p.A, b1, b2), rb = row_of(p.B, b1, b2), rb2 = row_of(p.B2, b1, b2);
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++kc) {
+          const uint32_t st = kc % C::STAGES, ph = (kc / C::STAGES) & 1;
+          if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1, abort_flag, 1, &g_device_error)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + st * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
+          issued_mask |= 1u << st;
+          const int64_t k0 = static_cast<int64_t>(kb) * BK;
+          load_operand<A_MN, BM>(sa, &tmA, &full_bar[st], ra, mt * BM, k0);
+          load_operand<B_MN, BN>(sb, &tmB, &full_bar[st], rb, nt * BN, k0);
+          if constexpr (NB == 2) load_operand<B_MN, BN>(sb + C::B_BYTES, &tmB2, &full_bar[st], rb2, nt * BN, k0);
+        }
+      }
+      // Teardown: make sure every copy this thread issued has landed before the
+      // CTA's shared memory can be released (matters only after an abort).
+      for (uint32_t st = 0; st < C::STAGES; ++st) {
+        if (!(issued_mask & (1u << st))) continue;
+        // The last fill of stage st was fill number f with kc-1 >= st + f*STAGES.
+        const uint32_t f = (kc - 1 - st) / C::STAGES;
+        mbar_wait_bounded(&full_bar[st], f & 1, abort_flag, 4, &g_device_error);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    // The whole role runs on one thread: tcgen05.mma and tcgen05.commit are
+    // issued by a single thread, and a lone waiter cannot diverge from itself.
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, A_MN, B_MN);
+      uint32_t kc = 0, ls = 0;
+      bool ok = true;
+      while (ok && iter.next(seg)) {
+        const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kAccStride;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++kc) {
+          const uint32_t st = kc % C::STAGES, ph = (kc / C::STAGES) & 1;
+          if (!mbar_wait_bounded(&full_bar[st], ph, abort_flag, 2, &g_device_error)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + st * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+          const int64_t krem = p.K - static_cast<int64_t>(kb) * BK;
+          const int ksteps = static_cast<int>(min(static_cast<int64_t>(BK / 16), (krem + 15) / 16));
+          for (int ks = 0; ks < ksteps; ++ks) {
+            const uint32_t accum = (kb > seg.kb0 || ks > 0) ? 1u : 0u;
+            const uint64_t ad = operand_desc<A_MN>(sa, ks);
+            umma_bf16(d_tmem, ad, operand_desc<B_MN>(sb, ks), idesc, accum);
+            if constexpr (NB == 2) umma_bf16(d_tmem + BN, ad, operand_desc<B_MN>(sb + C::B_BYTES, ks), idesc, accum);
+          }
+          umma_commit(&empty_bar[st]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        ++ls;
+      }
+      // Teardown: wait for every MMA issued here before TMEM is freed.
+      umma_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp % 4;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    uint32_t ls = 0;
+    while (iter.next(seg)) {
+      const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
+      // Every lane waits (each needs the acquire); the warp leaves together if any gave up,
+      // because the TMEM loads below are warp-collective.
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error))) break;
+      tc_fence_after();
+      int bi;
+      int64_t mt, nt;
+      kp.s.tile_coords(seg.tile, bi, mt, nt);
+      const int b1 = bi % p.nb1, b2 = bi / p.nb1;
+      const int64_t m = mt * BM + quarter * 32 + lane;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32], u[32];
+        tmem_ld_32x32b_x32(tbase + c * 32, r);
+        if constexpr (NB == 2) tmem_ld_32x32b_x32(tbase + BN + c * 32, u);
+        tmem_wait_ld();
+        const int64_t n = nt * BN + c * 32;
+        if (m < p.M && n < p.N) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      ++ls;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+static bool make_map(CUtensorMap* map, const Operand& o, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.cols), static_cast<cuuint64_t>(o.rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ld) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(o.ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
+static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
+  using C = Cfg<BN, NB>;
+  auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16>;
+  static std::mutex mu;
+  static uint64_t attr_done = 0;  // bit per device: shared-memory size attribute set
+  {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!(attr_done & (1ull << dev))) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      attr_done |= 1ull << dev;
+    }
+  }
+
+  CUtensorMap mA, mB, mB2;
+  if (!make_map(&mA, p.A, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mB, p.B, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
+  if (NB == 2) {
+    if (!make_map(&mB2, p.B2, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
+  } else {
+    mB2 = mB;
+  }
+
+  KParams kp;
+  kp.p = p;
+  Sched& s = kp.s;
+  s.n_mt = (p.M + BM - 1) / BM;
+  s.n_nt = (p.N + BN - 1) / BN;
+  s.tiles_per_batch = s.n_mt * s.n_nt;
+  s.total_tiles = s.tiles_per_batch * p.nb1 * p.nb2;
+  s.kb_total = static_cast<int>((p.K + BK - 1) / BK);
+  s.group_m = static_cast<int>(s.n_mt < 16 ? s.n_mt : 16);
+  s.split = p.split_k ? 1 : 0;
+  s.total_iters = s.total_tiles * s.kb_total;
+  const int sms = device_sm_count();
+  int64_t grid = s.split ? std::min<int64_t>(sms, s.total_iters) : std::min<int64_t>(sms, s.total_tiles);
+  if (grid <= 0) return cudaSuccess;
+  count_launch();
+  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, stream>>>(mA, mB, mB2, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t read_clear_device_error(int* code) {
+  const int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+  return e;
+}
+
+cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
+  using namespace tc;
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0 || p.nb1 <= 0 || p.nb2 <= 0) return cudaSuccess;
+  // K tails: the MMA issuer only issues the 16-wide K steps that start below K.
+  // Inside the last step, elements past K must read as zero in at least one
+  // operand; TMA zero-fills them when K ends at the edge of that operand's
+  // matrix (gate, proj, apply).  Where K is a window of rows that continue
+  // past it in both operands (update and group sums, K = a multiple of the
+  // chunk), the caller guarantees K % 16 == 0.
+  const bool a_mn = p.A.mn_major != 0, b_mn = p.B.mn_major != 0;
+  if (p.split_k && p.epi != EPI_ACCUM) return cudaErrorInvalidValue;
+  switch (p.epi) {
+    case EPI_GATE:
+      if (!a_mn && b_mn)
+        return p.out_bf16 ? run<128, 2, false, true, EPI_GATE, true>(p, stream)
+                          : run<128, 2, false, true, EPI_GATE, false>(p, stream);
+      break;
+    case EPI_STORE:
+      if (!a_mn && b_mn)
+        return p.out_bf16 ? run<256, 1, false, true, EPI_STORE, true>(p, stream)
+                          : run<256, 1, false, true, EPI_STORE, false>(p, stream);
+      if (a_mn && b_mn && !p.out_bf16) return run<256, 1, true, true, EPI_STORE, false>(p, stream);
+      break;
+    case EPI_ACCUM:
+      if (!a_mn && b_mn) return run<256, 1, false, true, EPI_ACCUM, false>(p, stream);
+      break;
+    case EPI_AXPY:
+      if (a_mn && b_mn) return run<256, 1, true, true, EPI_AXPY, false>(p, stream);
+      break;
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace ipttt

@@ -1,0 +1,53 @@
+// Host-side entry points of the kernel files, used by the C-ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm.h"
+
+namespace ipttt {
+
+// Launch bookkeeping: every kernel launch of the library calls count_launch().
+void count_launch();
+int current_device();     // cudaGetDevice, -1 on error
+int device_sm_count();    // SMs of the current device (cached)
+
+// Read the device error word of the current device (0 = no capped wait ran out) and clear it.
+cudaError_t read_clear_device_error(int* code);
+
+cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream);    // bf16 operands, tcgen05
+cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream);  // fp32 operands, CUDA cores
+
+// C = chunk-padded depthwise conv of E (width 4, taps t..t+3), rows = batch*L.
+cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t rows, int64_t L, int64_t B, int64_t d,
+                        bool bf16, cudaStream_t stream);
+
+// Per batch entry e = b1 + nb1*b2 and chunk row i < B:
+//   O[orow] = act(acc[e*B+i]);  R[e*B+i] = act(acc[e*B+i] - V[vrow])  (if R);  acc[e*B+i] = 0
+// with orow = o_y0 + b1*o_ys1 + b2*o_ys2 + i (V rows likewise).
+struct ResidualArgs {
+  float* acc = nullptr;
+  const void* V = nullptr;
+  void* O = nullptr;
+  void* R = nullptr;
+  int64_t B = 0, d = 0;
+  int nb1 = 1, nb2 = 1;
+  int64_t o_y0 = 0, o_ys1 = 0, o_ys2 = 0;
+};
+cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t stream);
+
+// Wb[s] = bf16(W0[s or 0]) for s < batch; n = d_ff*d.
+cudaError_t launch_to_bf16(const float* W0, int64_t w0_stride, __nv_bfloat16* Wb, int64_t batch, int64_t n,
+                           cudaStream_t stream);
+// W[s] = W0[s or 0] (fp32 copy) for s < batch.
+cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
+                          cudaStream_t stream);
+
+// Exclusive scan over G group sums, element-wise over batch*n:
+//   S = W0; for g: t = D[g]; D[g] = S; Db[g] = bf16(S) (if Db); S += alpha*t;  W_final = S
+cudaError_t launch_group_scan(float* D, __nv_bfloat16* Db, const float* W0, int64_t w0_stride, float* W_final,
+                              int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream);
+
+}  // namespace ipttt

@@ -1,0 +1,173 @@
+/*
+ * libipttt -- the fast-weight hot path of In-Place Test-Time Training, for
+ * NVIDIA B300 (sm_103a).
+ *
+ * The method (In-Place TTT write-ups: itsolotime §2.1-2.3 and Fig. 1;
+ * su666666 "first/second/third axe") reuses the final projection W_o of a
+ * gated MLP as a fast weight.  Per layer and per sequence of L tokens:
+ *
+ *   Z = SiLU(X W_g) * (X W_u)                  gated activation, W_g W_u frozen
+ *   V = Proj(Conv(E))                          target from token embeddings E
+ *   for each chunk k of B tokens (K = L/B):
+ *       O_k     = Z_k W_k                      apply the current fast weight
+ *       W_{k+1} = W_k - (eta/B) Z_k^T (Z_k W_k - V_k)     MSE rule, or
+ *       W_{k+1} = W_k + (eta/B) Z_k^T V_k                 additive rule
+ *
+ * Conv is depthwise, width 4, tap j multiplies E[t+j], no bias, and reads
+ * zeros past the end of the token's own chunk (no update reads past its
+ * chunk).  Row-vector convention: x is 1 x d, W_g and W_u are d x d_ff, W_o is
+ * d_ff x d.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array pointer is a DEVICE pointer owned by the caller, row-major and
+ *   contiguous, aligned to 16 bytes.  Token-major activations hold sequence s
+ *   in rows s*L .. s*L+L-1.  Nothing passed in is freed or kept.
+ * - "act" arrays (X, E, W_g, W_u, P, Z, V, O) have the element type given by
+ *   dims->dtype: IPTTT_BF16 (bfloat16) or IPTTT_FP32 (float).  The fast weight
+ *   (W_o0, W_final) and the conv weights are always float32.
+ * - IPTTT_BF16 computes on the tensor cores (bf16 operands, fp32 accumulation,
+ *   fp32 master fast weight).  IPTTT_FP32 computes every product in fp32 on
+ *   the CUDA cores; it is the exact-arithmetic mode.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and never synchronise it.  A call returns IPTTT_OK once its
+ *   kernels are queued; a device-side failure (a capped wait that ran out) is
+ *   recorded on the device and reported by ipttt_sync_status().
+ * - Scratch memory (activations Z and V inside ipttt_layer_forward, partial
+ *   sums, the bf16 copy of the fast weight, group states of the additive
+ *   scan) comes from a per-device pool owned by the library: grown with
+ *   cudaMalloc on first need (a call that needs to grow it synchronises the
+ *   device), reused by later calls, freed by ipttt_release().  Calls that share
+ *   the pool must be ordered (one stream, or the caller's own events).
+ * - No call aborts, throws or traps.  Errors come back as an ipttt_status.
+ *   Arguments are checked before any launch: null pointers, non-positive or
+ *   inconsistent sizes, L not a multiple of B, misaligned pointers, host
+ *   pointers where device pointers are required, a device that is not
+ *   compute capability 10.3.
+ * - Constraints of the IPTTT_BF16 mode: d and d_ff multiples of 8 (16-byte row
+ *   strides for the tensor-memory-accelerator copies) and B a multiple of 16
+ *   (the tensor-core K step over tokens).  IPTTT_FP32 takes any sizes >= 1.
+ */
+#ifndef IPTTT_H
+#define IPTTT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IPTTT_VERSION 100 /* 0.1.0 */
+
+typedef enum ipttt_status {
+  IPTTT_OK = 0,
+  IPTTT_ERR_INVALID_ARG = 1, /* null/misaligned/host pointer, bad size, L % B != 0, ... */
+  IPTTT_ERR_UNSUPPORTED = 2, /* no CUDA device, or not compute capability 10.3 */
+  IPTTT_ERR_ALLOC = 3,       /* the scratch pool could not grow */
+  IPTTT_ERR_LAUNCH = 4,      /* a kernel launch was rejected */
+  IPTTT_ERR_TIMEOUT = 5,     /* a capped device-side wait ran out (from ipttt_sync_status) */
+  IPTTT_ERR_CUDA = 6         /* another CUDA runtime error (sticky context errors included) */
+} ipttt_status;
+
+typedef enum ipttt_dtype { IPTTT_FP32 = 0, IPTTT_BF16 = 1 } ipttt_dtype;
+
+typedef enum ipttt_rule {
+  IPTTT_RULE_MSE = 0, /* W <- W - (eta/B) Z_k^T (Z_k W - V_k): sequential over chunks */
+  IPTTT_RULE_ADD = 1  /* W <- W + (eta/B) Z_k^T V_k: chunk-parallel prefix scan */
+} ipttt_rule;
+
+/* Sizes shared by the calls.  batch = independent sequences; d = model width;
+ * d_ff = gated-MLP hidden width; dtype = ipttt_dtype of the "act" arrays;
+ * w0_per_seq = 0: W_o0 is one d_ff x d matrix shared by all sequences,
+ *              1: W_o0 is batch x d_ff x d (for example the W_final of a
+ *                 previous call, to resume a sequence where it stopped). */
+typedef struct ipttt_dims {
+  int64_t batch;
+  int64_t d;
+  int64_t d_ff;
+  int32_t dtype;
+  int32_t w0_per_seq;
+} ipttt_dims;
+
+typedef void* ipttt_stream; /* a cudaStream_t */
+
+/*
+ * Whole layer: gated activation, targets and the chunk loop, for dims->batch
+ * sequences of L tokens.  (In-Place TTT: gated MLP itsolotime §2.1, target
+ * §2.3, chunk-wise apply-then-update §2.2 / Fig. 1.)
+ *
+ *   X      [batch*L, d]      act   hidden states entering the MLP
+ *   E      [batch*L, d]      act   token embeddings of the same tokens
+ *   W_g    [d, d_ff]         act   frozen gate projection
+ *   W_u    [d, d_ff]         act   frozen up projection
+ *   W_o0   [d_ff, d] fp32          initial fast weight (or [batch, d_ff, d] if
+ *                                  dims->w0_per_seq); not modified
+ *   conv_w [d, 4] fp32             depthwise conv taps, conv_w[c][j] for E[t+j][c]
+ *   P      [d, d]            act   target projection
+ *   L, B                           tokens per sequence, tokens per chunk; L % B == 0
+ *   eta                            step size (the step is eta/B times the chunk sum)
+ *   rule                           IPTTT_RULE_MSE or IPTTT_RULE_ADD
+ *   O      [batch*L, d]      act   out: O_k = Z_k W_k, chunk by chunk
+ *   W_final[batch, d_ff, d] fp32   out: the fast weight after the last chunk
+ *
+ * O and W_final must not overlap any input.  L == 0 copies W_o0 to W_final.
+ */
+ipttt_status ipttt_layer_forward(const void* X, const void* E, const void* W_g, const void* W_u,
+                                 const float* W_o0, const float* conv_w, const void* P, int64_t L,
+                                 int64_t B, float eta, ipttt_rule rule, void* O, float* W_final,
+                                 const ipttt_dims* dims, ipttt_stream stream);
+
+/*
+ * Targets only: V = Proj(Conv(E)) with the conv zero-padded at every chunk's
+ * end (itsolotime §2.3; the next-token case is conv one-hot at tap 1, P = I).
+ *
+ *   E [batch*L, d] act, conv_w [d, 4] fp32, P [d, d] act, V [batch*L, d] act (out).
+ */
+ipttt_status ipttt_make_targets(const void* E, const float* conv_w, const void* P, void* V,
+                                int64_t L, int64_t B, const ipttt_dims* dims, ipttt_stream stream);
+
+/*
+ * Gated activation only: Z = SiLU(X W_g) * (X W_u) (itsolotime §2.1), for
+ * n_tokens rows.  X [n_tokens, d] act, W_g W_u [d, d_ff] act, Z [n_tokens, d_ff]
+ * act (out).  dims->batch is ignored.
+ */
+ipttt_status ipttt_gate_up(const void* X, const void* W_g, const void* W_u, void* Z,
+                           int64_t n_tokens, const ipttt_dims* dims, ipttt_stream stream);
+
+/*
+ * Chunk engine only, on precomputed Z [batch*L, d_ff] act and V [batch*L, d]
+ * act: the apply / residual / update loop (MSE rule) or the chunk-parallel
+ * prefix scan (additive rule) of itsolotime §2.2 and §2.3.  Other arguments as
+ * in ipttt_layer_forward.
+ */
+ipttt_status ipttt_chunk_forward(const void* Z, const void* V, const float* W_o0, int64_t L,
+                                 int64_t B, float eta, ipttt_rule rule, void* O, float* W_final,
+                                 const ipttt_dims* dims, ipttt_stream stream);
+
+/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or
+ * ipttt_chunk_forward (with_activations = 0) needs for these sizes.  Host only. */
+ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, ipttt_rule rule,
+                                  int32_t with_activations, size_t* bytes);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device: IPTTT_ERR_TIMEOUT if a capped wait ran out since the last
+ * check, IPTTT_ERR_CUDA for a CUDA error, else IPTTT_OK. */
+ipttt_status ipttt_sync_status(ipttt_stream stream);
+
+/* Free the scratch pool of every device the library has used.  The caller
+ * must make sure no queued call still uses it (synchronise first). */
+ipttt_status ipttt_release(void);
+
+/* Kernels queued by the last call made from this host thread (a count of this
+ * library's launches, for profiling).  Host only. */
+int64_t ipttt_last_launch_count(void);
+
+const char* ipttt_status_string(ipttt_status status);
+int ipttt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IPTTT_H */

@@ -1,0 +1,132 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments with a status code before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunked_weight_mlp_place_b300 import _lib
+from chunked_weight_mlp_place_b300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return _lib.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ipttt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ipttt_\w+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert _declared() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert _lib.version() == 100
+    for s in range(7):
+        assert _lib.status_string(s)
+    assert "unknown" in _lib.status_string(99)
+
+
+def _dims(batch=1, d=64, d_ff=256, dtype=_lib.BF16, w0=0):
+    return _lib.dims(batch, d, d_ff, dtype, w0)
+
+
+FAKE = 1 << 20  # aligned, non-null, never dereferenced: host checks fail first or no device is found
+
+
+def _layer(L, dm, Lseq=256, B=64, eta=0.1, rule=0, ptrs=None, pdims=True):
+    p = ptrs if ptrs is not None else [FAKE] * 9
+    return L.ipttt_layer_forward(p[0], p[1], p[2], p[3], p[4], p[5], p[6], Lseq, B, eta, rule, p[7], p[8],
+                                 ctypes.byref(dm) if pdims else None, None)
+
+
+def test_invalid_arguments_are_rejected_on_the_host(L):
+    E = _lib.ERR_INVALID_ARG
+    assert _layer(L, _dims(), pdims=False) == E                        # no dims
+    assert _layer(L, _dims(), Lseq=250, B=64) == E                     # L % B != 0
+    assert _layer(L, _dims(), B=0) == E                                # B < 1
+    assert _layer(L, _dims(), Lseq=-64) == E                           # L < 0
+    assert _layer(L, _dims(d=60)) == E                                 # bf16 needs d % 8 == 0
+    assert _layer(L, _dims(d_ff=100)) == E                             # bf16 needs d_ff % 8 == 0
+    assert _layer(L, _dims(), Lseq=240, B=24) == E                     # bf16 needs B % 16 == 0
+    assert _layer(L, _dims(dtype=7)) == E                              # unknown dtype
+    assert _layer(L, _dims(d=0)) == E
+    assert _layer(L, _dims(batch=-1)) == E
+    assert _layer(L, _dims(w0=2)) == E
+    assert _layer(L, _dims(), rule=5) == E                             # unknown rule
+    assert _layer(L, _dims(), eta=float("nan")) == E
+    ptrs = [FAKE] * 9
+    ptrs[3] = 0
+    assert _layer(L, _dims(), ptrs=ptrs) == E                          # null pointer
+    ptrs[3] = FAKE + 4
+    assert _layer(L, _dims(), ptrs=ptrs) == E                          # misaligned pointer
+    dm = _dims()
+    assert L.ipttt_make_targets(FAKE, FAKE, FAKE, FAKE, 100, 64, ctypes.byref(dm), None) == E
+    assert L.ipttt_gate_up(FAKE, FAKE, FAKE, FAKE, -1, ctypes.byref(dm), None) == E
+    assert L.ipttt_chunk_forward(FAKE, FAKE, FAKE, 256, 48, 0.1, 0, FAKE, FAKE, ctypes.byref(dm), None) == E
+
+
+def test_fp32_mode_takes_any_sizes_on_the_host_checks(L):
+    # fp32 accepts ragged sizes; with valid arguments the call reaches the device
+    # check, which on a machine without a B300 says "unsupported".
+    dm = _dims(d=37, d_ff=90, dtype=_lib.FP32)
+    st = _layer(L, dm, Lseq=30, B=5)
+    assert st in (_lib.ERR_UNSUPPORTED, _lib.OK, _lib.ERR_INVALID_ARG)
+    try:
+        import torch
+        if not torch.cuda.is_available():
+            assert st == _lib.ERR_UNSUPPORTED
+    except ImportError:
+        pass
+
+
+def test_empty_inputs_are_no_ops(L):
+    dm = _dims(batch=0)
+    assert _layer(L, dm) == _lib.OK
+    assert L.ipttt_gate_up(0, 0, 0, 0, 0, ctypes.byref(_dims()), None) == _lib.OK
+    assert L.ipttt_make_targets(0, 0, 0, 0, 256, 64, ctypes.byref(_dims(batch=0)), None) == _lib.OK
+
+
+def test_workspace_size_is_host_only(L):
+    out = ctypes.c_size_t()
+    dm = _dims(batch=1, d=2560, d_ff=9728)
+    assert L.ipttt_workspace_size(ctypes.byref(dm), 131072, 1024, 0, 1, ctypes.byref(out)) == _lib.OK
+    T = 131072
+    act = T * 9728 * 2 + 2 * T * 2560 * 2
+    eng = 1024 * 2560 * 4 + 1024 * 2560 * 2 + 9728 * 2560 * 2
+    assert act + eng <= out.value <= act + eng + 4096
+    assert L.ipttt_workspace_size(ctypes.byref(dm), 131072, 1024, 0, 0, ctypes.byref(out)) == _lib.OK
+    assert eng <= out.value <= eng + 4096
+    # additive scan: 8 groups of fp32 + bf16 states
+    assert L.ipttt_workspace_size(ctypes.byref(dm), 32768, 64, 1, 0, ctypes.byref(out)) == _lib.OK
+    assert out.value >= 8 * 9728 * 2560 * 6
+    assert L.ipttt_workspace_size(ctypes.byref(dm), 100, 64, 0, 0, ctypes.byref(out)) == _lib.ERR_INVALID_ARG
+    assert L.ipttt_workspace_size(None, 128, 64, 0, 0, ctypes.byref(out)) == _lib.ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        _lib.gate_up(x, torch.zeros(8, 8, dtype=torch.bfloat16), torch.zeros(8, 8, dtype=torch.bfloat16),
+                     torch.zeros(4, 8, dtype=torch.bfloat16))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libipttt.so"))
+    with pytest.raises(ImportError):
+        _lib.lib()
