@@ -5,6 +5,7 @@ the C-ABI of ``include/ipttt.h``); this package holds its ctypes binding, the
 in-tree build script and the seeded synthetic input generator.
 """
 from ._lib import (  # noqa: F401
-    BF16, FP32, RULE_ADD, RULE_MSE, IptttError, chunk_forward, gate_up, last_launch_count, layer_forward,
+    BF16, FP32, RULE_ADD, RULE_MSE, IptttError, chunk_forward, gate_up, kernel_timing, kernel_timing_read,
+    last_launch_count, layer_forward,
     lib, make_targets, release, status_string, sync_status, version, workspace_size,
 )

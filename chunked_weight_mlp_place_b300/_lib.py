@@ -24,8 +24,10 @@ _RULES = {"mse": RULE_MSE, "add": RULE_ADD, RULE_MSE: RULE_MSE, RULE_ADD: RULE_A
 EXPORTS = (
     "ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
-    "ipttt_status_string", "ipttt_version",
+    "ipttt_status_string", "ipttt_version", "ipttt_kernel_timing", "ipttt_kernel_timing_read",
+    "ipttt_kernel_name",
 )
+KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy")
 
 
 class Dims(ctypes.Structure):
@@ -63,6 +65,12 @@ def lib() -> ctypes.CDLL:
         L.ipttt_status_string.argtypes = [i32]
         L.ipttt_status_string.restype = ctypes.c_char_p
         L.ipttt_version.argtypes = []
+        L.ipttt_kernel_timing.argtypes = [i32]
+        L.ipttt_kernel_timing.restype = i32
+        L.ipttt_kernel_timing_read.argtypes = [i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
+        L.ipttt_kernel_timing_read.restype = i32
+        L.ipttt_kernel_name.argtypes = [i32]
+        L.ipttt_kernel_name.restype = ctypes.c_char_p
         for name in ("ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
                      "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release"):
             getattr(L, name).restype = i32
@@ -191,6 +199,22 @@ def workspace_size(batch: int, d: int, d_ff: int, dtype: int, L: int, B: int, ru
 def sync_status(stream=None) -> int:
     """Synchronise the stream and return the device status (OK, ERR_TIMEOUT, ...)."""
     return int(lib().ipttt_sync_status(_stream(stream)))
+
+
+def kernel_timing(enable: bool) -> None:
+    """Start (clearing the totals) or stop per-kernel CUDA-event timing."""
+    _check(lib().ipttt_kernel_timing(1 if enable else 0), "ipttt_kernel_timing")
+
+
+def kernel_timing_read() -> dict:
+    """{kernel name: (launches, total device ms)} since timing was started."""
+    out = {}
+    for k, name in enumerate(KERNEL_KINDS):
+        n, ms = ctypes.c_int64(0), ctypes.c_double(0.0)
+        _check(lib().ipttt_kernel_timing_read(k, ctypes.byref(n), ctypes.byref(ms)), "ipttt_kernel_timing_read")
+        if n.value:
+            out[name] = (int(n.value), float(ms.value))
+    return out
 
 
 def release() -> None:

@@ -20,6 +20,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "ipttt.h"
 #include "gemm.h"
@@ -29,9 +30,69 @@ namespace ipttt {
 
 namespace {
 thread_local int64_t t_launches = 0;
+
+// Optional per-kernel timing: CUDA events recorded around every launch while
+// enabled, reduced to per-kind totals when read.
+struct TimingRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<TimingRec> g_timing_pending;
+std::vector<cudaEvent_t> g_event_pool;
+int64_t g_timing_launches[K_COUNT] = {0};
+double g_timing_ms[K_COUNT] = {0};
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
 }
 
-void count_launch() { ++t_launches; }
+// Fold every pending record into the totals (waits for its events).
+void drain_timing_locked() {
+  for (const TimingRec& r : g_timing_pending) {
+    float ms = 0.0f;
+    if (r.start && r.stop && cudaEventSynchronize(r.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+      g_timing_launches[r.kind] += 1;
+      g_timing_ms[r.kind] += ms;
+    }
+    cudaGetLastError();
+    if (r.start) g_event_pool.push_back(r.start);
+    if (r.stop) g_event_pool.push_back(r.stop);
+  }
+  g_timing_pending.clear();
+}
+}  // namespace
+
+LaunchMark::LaunchMark(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
+  ++t_launches;
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  if (!g_timing_on || k < 0 || k >= K_COUNT) return;
+  TimingRec r{k, take_event(), take_event()};
+  if (r.start) cudaEventRecord(r.start, s);
+  g_timing_pending.push_back(r);
+  slot = static_cast<int>(g_timing_pending.size()) - 1;
+}
+
+LaunchMark::~LaunchMark() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  if (slot < static_cast<int>(g_timing_pending.size()) && g_timing_pending[slot].stop)
+    cudaEventRecord(g_timing_pending[slot].stop, stream);
+  // keep memory bounded on long runs
+  if (g_timing_pending.size() > 65536) drain_timing_locked();
+}
 
 int current_device() {
   int dev = -1;
@@ -216,13 +277,14 @@ Operand mat(const void* ptr, int64_t rows, int64_t cols, int mn_major, int64_t y
   o.ys2 = ys2;
   return o;
 }
-OutRef out(void* ptr, int64_t ld, int64_t y0 = 0, int64_t ys1 = 0, int64_t ys2 = 0) {
+OutRef out(void* ptr, int64_t ld, int64_t y0 = 0, int64_t ys1 = 0, int64_t ys2 = 0, int64_t rows = 0) {
   OutRef o;
   o.ptr = ptr;
   o.ld = ld;
   o.y0 = y0;
   o.ys1 = ys1;
   o.ys2 = ys2;
+  o.rows = rows;
   return o;
 }
 
@@ -240,6 +302,7 @@ ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, 
   p.B = mat(W_g, dm->d, dm->d_ff, 1);
   p.B2 = mat(W_u, dm->d, dm->d_ff, 1);
   p.epi = EPI_GATE;
+  p.kind = K_GATE;
   p.out_bf16 = bf16;
   p.D = out(Z, dm->d_ff);
   IPTTT_CUDA(gemm(p, bf16, st));
@@ -257,6 +320,7 @@ ipttt_status run_targets(const void* E, const float* conv_w, const void* P, void
   p.A = mat(C, rows, dm->d, 0);
   p.B = mat(P, dm->d, dm->d, 1);
   p.epi = EPI_STORE;
+  p.kind = K_PROJ;
   p.out_bf16 = bf16;
   p.D = out(V, dm->d);
   IPTTT_CUDA(gemm(p, bf16, st));
@@ -271,8 +335,14 @@ int64_t scan_groups(int64_t K) {
 }
 
 struct EngineLayout {
-  size_t o_acc = 0, r = 0, wb = 0, d = 0, db = 0, total = 0;
+  size_t o_acc = 0, r = 0, wb = 0, d = 0, db = 0, counters = 0, total = 0;
+  int64_t n_counters = 0;
 };
+
+// Output tiles of the apply GEMM (128 x 256), one split-K counter each.
+int64_t apply_tiles(const ipttt_dims* dm, int64_t B, int64_t entries) {
+  return ((B + 127) / 128) * ((dm->d + 255) / 256) * entries;
+}
 
 EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rule rule, size_t base) {
   EngineLayout e;
@@ -285,12 +355,15 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
     e.o_acc = c.take<float>(dm->batch * B * dm->d);
     e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
     if (bf16) e.wb = c.take<uint16_t>(dm->batch * nw);
+    e.n_counters = apply_tiles(dm, B, dm->batch);
   } else {
     const int64_t G = scan_groups(K);
     e.o_acc = c.take<float>(G * dm->batch * B * dm->d);
     e.d = c.take<float>(G * dm->batch * nw);
     if (bf16) e.db = c.take<uint16_t>(G * dm->batch * nw);
+    e.n_counters = apply_tiles(dm, B, G * dm->batch);
   }
+  e.counters = c.take<int>(e.n_counters);
   e.total = c.off;
   return e;
 }
@@ -307,11 +380,15 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
 
   if (rule == IPTTT_RULE_MSE) {
     void* R = ws + lay.r;
+    int* counters = reinterpret_cast<int*>(ws + lay.counters);
     __nv_bfloat16* Wb = bf16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.wb) : nullptr;
     if (bf16) IPTTT_CUDA(launch_to_bf16(W0, w0s, Wb, batch, nw, st));
     IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * B * d, st));
+    if (bf16) IPTTT_CUDA(cudaMemsetAsync(counters, 0, sizeof(int) * lay.n_counters, st));
+    const int64_t w0_rows = (dm->w0_per_seq ? batch : 1) * dff;
     for (int64_t k = 0; k < K; ++k) {
-      // apply: O_acc[s] = Z_k[s] W_k[s]
+      // apply: O_acc[s] = Z_k[s] W_k[s]; on the tensor cores the last split
+      // contributor of each tile also writes O_k and R_k = O_k - V_k
       GemmProblem a;
       a.M = B;
       a.N = d;
@@ -321,23 +398,32 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       if (bf16)
         a.B = mat(Wb, batch * dff, d, 1, 0, dff);
       else
-        a.B = (k == 0) ? mat(W0, (dm->w0_per_seq ? batch : 1) * dff, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
+        a.B = (k == 0) ? mat(W0, w0_rows, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
       a.epi = EPI_ACCUM;
+      a.kind = K_APPLY;
       a.D = out(o_acc, d, 0, B);
       a.split_k = 1;
+      if (bf16) {
+        a.fix.counters = counters;
+        a.fix.O = out(O, d, k * B, L);
+        a.fix.V = out(const_cast<void*>(V), d, k * B, L);
+        a.fix.R = out(R, d, 0, B);
+      }
       IPTTT_CUDA(gemm(a, bf16, st));
-      // residual: O_k = O_acc, R_k = O_acc - V_k, O_acc = 0
-      ResidualArgs ra;
-      ra.acc = o_acc;
-      ra.V = V;
-      ra.O = O;
-      ra.R = R;
-      ra.B = B;
-      ra.d = d;
-      ra.nb1 = bint;
-      ra.o_y0 = k * B;
-      ra.o_ys1 = L;
-      IPTTT_CUDA(launch_residual(ra, bf16, st));
+      if (!bf16) {
+        // residual: O_k = O_acc, R_k = O_acc - V_k, O_acc = 0
+        ResidualArgs ra;
+        ra.acc = o_acc;
+        ra.V = V;
+        ra.O = O;
+        ra.R = R;
+        ra.B = B;
+        ra.d = d;
+        ra.nb1 = bint;
+        ra.o_y0 = k * B;
+        ra.o_ys1 = L;
+        IPTTT_CUDA(launch_residual(ra, bf16, st));
+      }
       // update: W_{k+1} = W_k - (eta/B) Z_k^T R_k
       GemmProblem u;
       u.M = dff;
@@ -347,8 +433,9 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.A = mat(Z, batch * L, dff, 1, k * B, L);
       u.B = mat(R, batch * B, d, 1, 0, B);
       u.epi = EPI_AXPY;
-      u.D = out(Wf, d, 0, dff);
-      u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r) : out(Wf, d, 0, dff);
+      u.kind = K_UPDATE;
+      u.D = out(Wf, d, 0, dff, 0, batch * dff);
+      u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r, 0, w0_rows) : out(Wf, d, 0, dff, 0, batch * dff);
       if (bf16 && k + 1 < K) u.Db = out(Wb, d, 0, dff);
       u.alpha = -eta / static_cast<float>(B);
       IPTTT_CUDA(gemm(u, bf16, st));
@@ -372,12 +459,15 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   s.A = mat(Z, batch * L, dff, 1, 0, L, g * B);
   s.B = mat(V, batch * L, d, 1, 0, L, g * B);
   s.epi = EPI_STORE;
+  s.kind = K_GROUP_SUM;
   s.out_bf16 = 0;
   s.D = out(D, d, 0, dff, batch * dff);
   IPTTT_CUDA(gemm(s, bf16, st));
   // exclusive scan over groups -> the fast weight at the start of each group
   IPTTT_CUDA(launch_group_scan(D, Db, W0, w0s, Wf, G, batch, nw, alpha, st));
   IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * G * batch * B * d, st));
+  int* counters = reinterpret_cast<int*>(ws + lay.counters);
+  if (bf16) IPTTT_CUDA(cudaMemsetAsync(counters, 0, sizeof(int) * lay.n_counters, st));
   for (int64_t i = 0; i < g; ++i) {
     GemmProblem a;
     a.M = B;
@@ -388,20 +478,27 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     a.A = mat(Z, batch * L, dff, 0, i * B, L, g * B);
     a.B = bf16 ? mat(Db, G * batch * dff, d, 1, 0, dff, batch * dff) : mat(D, G * batch * dff, d, 1, 0, dff, batch * dff);
     a.epi = EPI_ACCUM;
+    a.kind = K_APPLY;
     a.D = out(o_acc, d, 0, B, batch * B);
     a.split_k = 1;
+    if (bf16) {
+      a.fix.counters = counters;
+      a.fix.O = out(O, d, i * B, L, g * B);
+    }
     IPTTT_CUDA(gemm(a, bf16, st));
-    ResidualArgs ra;
-    ra.acc = o_acc;
-    ra.O = O;
-    ra.B = B;
-    ra.d = d;
-    ra.nb1 = bint;
-    ra.nb2 = gint;
-    ra.o_y0 = i * B;
-    ra.o_ys1 = L;
-    ra.o_ys2 = g * B;
-    IPTTT_CUDA(launch_residual(ra, bf16, st));
+    if (!bf16) {
+      ResidualArgs ra;
+      ra.acc = o_acc;
+      ra.O = O;
+      ra.B = B;
+      ra.d = d;
+      ra.nb1 = bint;
+      ra.nb2 = gint;
+      ra.o_y0 = i * B;
+      ra.o_ys1 = L;
+      ra.o_ys2 = g * B;
+      IPTTT_CUDA(launch_residual(ra, bf16, st));
+    }
     if (i + 1 < g) {
       GemmProblem u;
       u.M = dff;
@@ -412,7 +509,8 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.A = mat(Z, batch * L, dff, 1, i * B, L, g * B);
       u.B = mat(V, batch * L, d, 1, i * B, L, g * B);
       u.epi = EPI_AXPY;
-      u.D = out(D, d, 0, dff, batch * dff);
+      u.kind = K_UPDATE;
+      u.D = out(D, d, 0, dff, batch * dff, G * batch * dff);
       u.src = u.D;
       if (bf16) u.Db = out(Db, d, 0, dff, batch * dff);
       u.alpha = alpha;
@@ -562,6 +660,34 @@ ipttt_status ipttt_release(void) {
 }
 
 int64_t ipttt_last_launch_count(void) { return t_launches; }
+
+ipttt_status ipttt_kernel_timing(int32_t enable) {
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  if (enable) {
+    g_timing_pending.clear();
+    for (int k = 0; k < K_COUNT; ++k) {
+      g_timing_launches[k] = 0;
+      g_timing_ms[k] = 0.0;
+    }
+  }
+  g_timing_on = enable != 0;
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_kernel_timing_read(int32_t kind, int64_t* launches, double* total_ms) {
+  if (kind < 0 || kind >= K_COUNT || !launches || !total_ms) return IPTTT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(g_timing_mu);
+  drain_timing_locked();
+  *launches = g_timing_launches[kind];
+  *total_ms = g_timing_ms[kind];
+  return IPTTT_OK;
+}
+
+const char* ipttt_kernel_name(int32_t kind) {
+  static const char* names[K_COUNT] = {"gate_up", "conv", "proj", "apply", "residual",
+                                       "update", "group_sum", "scan", "weight_copy"};
+  return (kind >= 0 && kind < K_COUNT) ? names[kind] : "unknown";
+}
 
 const char* ipttt_status_string(ipttt_status s) {
   switch (s) {

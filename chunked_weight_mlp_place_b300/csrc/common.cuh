@@ -41,6 +41,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Arrive on `bar` only once `dep` is available: the arrive takes `dep` as an
+// operand, so it cannot issue before the loads that produce `dep` completed.
+__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float dep) {
+  asm volatile(
+      "{\n\t.reg .b32 t;\n\t"
+      "mov.b32 t, %1;\n\t"
+      "mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "f"(dep)
+      : "memory");
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

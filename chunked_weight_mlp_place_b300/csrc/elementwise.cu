@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict_
 cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t rows, int64_t L, int64_t B, int64_t d,
                         bool bf16, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  count_launch();
+  LaunchMark mark(K_CONV, stream);
   if (bf16) {
     constexpr int TT = 8;
     const int64_t items = (d / 8) * ((rows + TT - 1) / TT);
@@ -239,7 +239,7 @@ cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t row
 cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t stream) {
   const int64_t total = a.B * a.d * a.nb1 * a.nb2;
   if (total <= 0) return cudaSuccess;
-  count_launch();
+  LaunchMark mark(K_RESIDUAL, stream);
   if (bf16 && a.d % 8 == 0)
     residual_kernel_bf16x8<<<grid_for(total / 8), kThreads, 0, stream>>>(a);
   else if (bf16)
@@ -252,21 +252,21 @@ cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t strea
 cudaError_t launch_to_bf16(const float* W0, int64_t w0_stride, __nv_bfloat16* Wb, int64_t batch, int64_t n,
                            cudaStream_t stream) {
   if (n % 4) return cudaErrorInvalidValue;
-  count_launch();
+  LaunchMark mark(K_WEIGHT, stream);
   to_bf16_kernel<<<grid_for(n / 4 * batch), kThreads, 0, stream>>>(W0, w0_stride, Wb, batch, n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream) {
-  count_launch();
+  LaunchMark mark(K_WEIGHT, stream);
   copy_w_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(W0, w0_stride, W, batch, n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_group_scan(float* D, __nv_bfloat16* Db, const float* W0, int64_t w0_stride, float* W_final,
                               int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream) {
-  count_launch();
+  LaunchMark mark(K_SCAN, stream);
   group_scan_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(D, Db, W0, w0_stride, W_final, G, batch, n,
                                                                   alpha);
   return cudaGetLastError();

@@ -33,6 +33,16 @@ struct OutRef {
   void* ptr = nullptr;
   int64_t ld = 0;
   int64_t y0 = 0, ys1 = 0, ys2 = 0;  // row = y0 + b1*ys1 + b2*ys2 + m, column n
+  int64_t rows = 0;                  // rows of the whole matrix (needed where it is read by TMA)
+};
+
+// Split-K fix-up of EPI_ACCUM on the tensor-core path: the CTA that adds the
+// last partial sum of an output tile turns the tile's fp32 sums into the chunk
+// outputs, O = act(acc) and, if V is given, R = act(acc - V), and clears the
+// sums and the tile's counter for the next launch.  No CTA waits for another.
+struct Fixup {
+  int* counters = nullptr;  // one int per output tile, zero between launches; null = no fix-up
+  OutRef O, V, R;           // act-dtype rows, indexed like D
 };
 
 struct GemmProblem {
@@ -46,6 +56,8 @@ struct GemmProblem {
   OutRef Db;         // AXPY: optional bf16 copy
   float alpha = 1.0f;
   int split_k = 0;   // tensor-core path: 1 = balance (tile, k-block) work over CTAs (needs EPI_ACCUM)
+  Fixup fix;         // tensor-core path, EPI_ACCUM with split_k
+  int kind = 0;      // KernelKind label (launch counting / timing)
 };
 
 }  // namespace ipttt

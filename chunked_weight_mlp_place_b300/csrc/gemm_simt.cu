@@ -116,7 +116,7 @@ cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream) {
   const int64_t gx = (p.N + kBN - 1) / kBN, gy = (p.M + kBM - 1) / kBM, gz = static_cast<int64_t>(p.nb1) * p.nb2;
   if (gy > 65535 || gz > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz));
-  count_launch();
+  LaunchMark mark(p.kind, stream);
   if (p.epi == EPI_GATE)
     simt_gemm_kernel<true><<<grid, kThreads, 0, stream>>>(p);
   else

@@ -1,23 +1,27 @@
 // Tensor-core back end of the batched GEMM (IPTTT_BF16 mode) for sm_103a.
 //
 // One persistent kernel template serves the four contractions of the layer:
-//   gate   Z = SiLU(X W_g) * (X W_u)       A = X   (K-major)  B = W_g, W_u (MN-major)
-//   proj   V = C P                          A = C   (K-major)  B = P        (MN-major)
-//   apply  O_k += Z_k W_k  (split over K)   A = Z_k (K-major)  B = W_k bf16 (MN-major)
-//   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k      (MN-major)
+//   gate   Z = SiLU(X W_g) * (X W_u)       A = X   (K-major)  B = [W_g | W_u] (MN-major)
+//   proj   V = C P                          A = C   (K-major)  B = P           (MN-major)
+//   apply  O_k = Z_k W_k  (split over K)    A = Z_k (K-major)  B = W_k bf16    (MN-major)
+//   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k         (MN-major)
 //
-// Each CTA (one per SM) runs six warps:
+// Each CTA (one per SM) runs these warps:
 //   warp 0      TMA producer: 128x64 A tiles and 64-wide B tiles into a ring of
 //               shared-memory stages (128-byte swizzle), completion on mbarriers;
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, K=16) into a
-//               TMEM accumulator, and tcgen05.commit frees each stage;
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16)
+//               into a TMEM accumulator; tcgen05.commit frees each stage;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output
-//               row) and apply the fused epilogue straight to global memory.
+//               row) and apply the fused epilogue straight to global memory;
+//   warp 6      (update only) fast-weight loader: streams the fp32 W tile the
+//               epilogue will read-modify-write into swizzled shared memory
+//               slots ahead of time, so the epilogue never waits on HBM.
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next.  Work is either whole output tiles, strided over
 // the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
-// share of the (tile, k-block) iteration space per CTA whose partial sums are
-// added into an fp32 buffer with vector atomics.
+// share of the (tile, k-block) iteration space per CTA; partial sums are added
+// into an fp32 buffer with vector atomics, and the CTA that adds the last
+// partial sum of a tile finishes it (O and the residual R = O - V).
 //
 // Every mbarrier wait is capped (common.cuh); a CTA whose wait runs out flags
 // the others, drains its in-flight TMA copies and MMAs, frees its TMEM and
@@ -32,28 +36,35 @@ namespace ipttt {
 
 // Error word written by kernels whose capped waits ran out (0 = none); read
 // and cleared through read_clear_device_error().  Codes: 1 = TMA-producer
-// wait, 2 = MMA-issuer wait, 3 = epilogue wait, 4 = teardown drain.
+// wait, 2 = MMA-issuer wait, 3 = epilogue wait, 4 = teardown drain,
+// 5 = fast-weight loader wait.
 __device__ int g_device_error = 0;
 
 namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns between the two accumulator buffers
+constexpr int kEpiThreads = 128;
+constexpr int kEpiBarrier = 1;   // named barrier of the four epilogue warps
 
-template <int BN, int NB>
+template <int BN, int NB, int EPI>
 struct Cfg {
+  static constexpr bool W_LOAD = (EPI == EPI_AXPY);
+  static constexpr int THREADS = W_LOAD ? 224 : 192;
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;  // per B operand
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
-  static constexpr int STAGES = (196 * 1024) / STAGE_BYTES;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-  static_assert(BN * NB <= kAccStride, "accumulator too wide");
+  static constexpr int N_MMA = BN * NB;        // the B operands sit side by side: one MMA covers them
+  static constexpr int W_SLOT_BYTES = BM * 32 * 4;  // 128 rows x 32 fp32 columns
+  static constexpr int W_SLOTS = W_LOAD ? 4 : 0;
+  static constexpr int STAGES = W_LOAD ? 3 : 4;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + W_SLOTS * W_SLOT_BYTES + BAR_BYTES;
+  static_assert(N_MMA <= kAccStride && N_MMA % 16 == 0, "accumulator width");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(STAGES >= 2, "stages");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 struct Seg {
@@ -61,7 +72,7 @@ struct Seg {
   int kb0, kb1;
 };
 
-// Work decomposition shared by the three roles (each walks it independently).
+// Work decomposition shared by all roles (each walks it independently).
 struct Sched {
   int64_t n_mt, n_nt, tiles_per_batch, total_tiles;
   int kb_total;
@@ -79,6 +90,12 @@ struct Sched {
     const int64_t q = r % gsz;
     mt = first_m + q % gm;
     nt = q / gm;
+  }
+  // Split mode: CTA c owns iterations [floor(c*T/G), floor((c+1)*T/G)); the
+  // owner of iteration i is floor(((i+1)*G - 1) / T).
+  __device__ int64_t owner(int64_t i) const { return ((i + 1) * gridDim.x - 1) / total_iters; }
+  __device__ int segments_of(int64_t t) const {
+    return static_cast<int>(owner((t + 1) * kb_total - 1) - owner(t * kb_total) + 1);
   }
 };
 
@@ -126,7 +143,11 @@ __device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) {
   return o.y0 + b1 * o.ys1 + b2 * o.ys2;
 }
 
-// Issue the TMA copies of one operand tile (extent `ext` along M or N, BK along K).
+__device__ __forceinline__ void epi_barrier() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
+}
+
+// Issue the TMA copies of one operand tile (extent EXT along M or N, BK along K).
 template <bool MN, int EXT>
 __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int64_t row0,
                                              int64_t i0, int64_t k0) {
@@ -153,9 +174,21 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kstep) {
     return make_smem_desc_sw128(base + kstep * 32, 16, 1024);
 }
 
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 w;
+  w.x = pack_bf16x2(v[0], v[1]);
+  w.y = pack_bf16x2(v[2], v[3]);
+  w.z = pack_bf16x2(v[4], v[5]);
+  w.w = pack_bf16x2(v[6], v[7]);
+  return w;
+}
+
+// Epilogue of 32 consecutive columns n.. of row m.  `s` is the fp32 source row
+// (AXPY only: 32 values already staged in registers).
 template <int EPI, bool OUT_BF16>
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
-                                               const uint32_t (&r)[32], const uint32_t (&u)[32]) {
+                                               const uint32_t (&r)[32], const uint32_t (&u)[32],
+                                               const float (&s)[32]) {
   const bool full = (n + 32 <= p.N);
   if constexpr (EPI == EPI_STORE || EPI == EPI_GATE) {
     float v[32];
@@ -172,14 +205,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
       __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D.ptr) + row * p.D.ld + n;
       if (full) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-          w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-          w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-          w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-          reinterpret_cast<uint4*>(d)[q] = w;
-        }
+        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(d)[q] = pack8_bf16(v + 8 * q);
       } else {
         for (int i = 0; i < 32 && n + i < p.N; ++i) d[i] = __float2bfloat16_rn(v[i]);
       }
@@ -207,62 +233,91 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
     }
   } else {  // EPI_AXPY
     const int64_t row = row_of(p.D, b1, b2) + m;
-    const int64_t srow = row_of(p.src, b1, b2) + m;
     float* d = static_cast<float*>(p.D.ptr) + row * p.D.ld + n;
-    const float* s = static_cast<const float*>(p.src.ptr) + srow * p.src.ld + n;
     __nv_bfloat16* db = nullptr;
     if (p.Db.ptr) db = static_cast<__nv_bfloat16*>(p.Db.ptr) + (row_of(p.Db, b1, b2) + m) * p.Db.ld + n;
-    if (full) {
-      float w[32];
+    float w[32];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = reinterpret_cast<const float4*>(s)[q];
-        w[4 * q + 0] = fmaf(p.alpha, __uint_as_float(r[4 * q + 0]), x.x);
-        w[4 * q + 1] = fmaf(p.alpha, __uint_as_float(r[4 * q + 1]), x.y);
-        w[4 * q + 2] = fmaf(p.alpha, __uint_as_float(r[4 * q + 2]), x.z);
-        w[4 * q + 3] = fmaf(p.alpha, __uint_as_float(r[4 * q + 3]), x.w);
-      }
+    for (int i = 0; i < 32; ++i) w[i] = fmaf(p.alpha, __uint_as_float(r[i]), s[i]);
+    if (full) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         reinterpret_cast<float4*>(d)[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       if (db) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 o;
-          o.x = pack_bf16x2(w[8 * q + 0], w[8 * q + 1]);
-          o.y = pack_bf16x2(w[8 * q + 2], w[8 * q + 3]);
-          o.z = pack_bf16x2(w[8 * q + 4], w[8 * q + 5]);
-          o.w = pack_bf16x2(w[8 * q + 6], w[8 * q + 7]);
-          reinterpret_cast<uint4*>(db)[q] = o;
-        }
+        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(db)[q] = pack8_bf16(w + 8 * q);
       }
     } else {
       for (int i = 0; i < 32 && n + i < p.N; ++i) {
-        const float w = fmaf(p.alpha, __uint_as_float(r[i]), s[i]);
-        d[i] = w;
-        if (db) db[i] = __float2bfloat16_rn(w);
+        d[i] = w[i];
+        if (db) db[i] = __float2bfloat16_rn(w[i]);
       }
     }
   }
 }
 
+// Split-K fix-up of one output row: O = bf16(acc), R = bf16(acc - V), acc = 0.
+// The sums were added by other SMs' atomics in L2, so they are read past L1.
+template <int BN>
+__device__ __forceinline__ void fixup_row(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n0) {
+  float* acc = static_cast<float*>(p.D.ptr) + (row_of(p.D, b1, b2) + m) * p.D.ld;
+  __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.fix.O.ptr) + (row_of(p.fix.O, b1, b2) + m) * p.fix.O.ld;
+  const __nv_bfloat16* V =
+      p.fix.V.ptr ? static_cast<const __nv_bfloat16*>(p.fix.V.ptr) + (row_of(p.fix.V, b1, b2) + m) * p.fix.V.ld
+                  : nullptr;
+  __nv_bfloat16* R =
+      p.fix.R.ptr ? static_cast<__nv_bfloat16*>(p.fix.R.ptr) + (row_of(p.fix.R, b1, b2) + m) * p.fix.R.ld : nullptr;
+  const int64_t n_end = min(n0 + BN, p.N);
+  int64_t n = n0;
+  for (; n + 8 <= n_end; n += 8) {
+    float4* a4 = reinterpret_cast<float4*>(acc + n);
+    const float4 x0 = __ldcg(a4), x1 = __ldcg(a4 + 1);
+    a4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    a4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    *reinterpret_cast<uint4*>(O + n) = pack8_bf16(v);
+    if (R) {
+      const uint4 vr = *reinterpret_cast<const uint4*>(V + n);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        v[2 * q] -= f.x;
+        v[2 * q + 1] -= f.y;
+      }
+      *reinterpret_cast<uint4*>(R + n) = pack8_bf16(v);
+    }
+  }
+  for (; n < n_end; ++n) {
+    const float x = __ldcg(acc + n);
+    acc[n] = 0.0f;
+    O[n] = __float2bfloat16_rn(x);
+    if (R) R[n] = __float2bfloat16_rn(x - __bfloat162float(V[n]));
+  }
+}
+
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ KParams kp) {
-  using C = Cfg<BN, NB>;
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmS,
+                   const __grid_constant__ KParams kp) {
+  using C = Cfg<BN, NB, EPI>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* full_bar = bars;                       // [STAGES]
-  uint64_t* empty_bar = bars + C::STAGES;          // [STAGES]
-  uint64_t* tfull_bar = bars + 2 * C::STAGES;      // [2]
-  uint64_t* tempty_bar = bars + 2 * C::STAGES + 2; // [2]
-  uint64_t* drain_bar = bars + 2 * C::STAGES + 4;  // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+  uint8_t* wslots = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wslots + C::W_SLOTS * C::W_SLOT_BYTES);
+  uint64_t* full_bar = bars;                        // [STAGES]
+  uint64_t* empty_bar = bars + C::STAGES;           // [STAGES]
+  uint64_t* tfull_bar = bars + 2 * C::STAGES;       // [2]
+  uint64_t* tempty_bar = bars + 2 * C::STAGES + 2;  // [2]
+  uint64_t* drain_bar = bars + 2 * C::STAGES + 4;   // [1]
+  uint64_t* wfull_bar = bars + 2 * C::STAGES + 5;   // [W_SLOTS]
+  uint64_t* wempty_bar = wfull_bar + C::W_SLOTS;    // [W_SLOTS]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty_bar + C::W_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const GemmProblem& p = kp.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -275,14 +330,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull_bar[i], 1);
-        mbar_init(&tempty_bar[i], 128);
+        mbar_init(&tempty_bar[i], kEpiThreads);
       }
       mbar_init(drain_bar, 1);
+      for (int i = 0; i < C::W_SLOTS; ++i) {
+        mbar_init(&wfull_bar[i], 1);
+        mbar_init(&wempty_bar[i], kEpiThreads);
+      }
       *abort_flag = 0;
+      *last_flag = 0;
       fence_mbarrier_init();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       if constexpr (NB == 2) tma_prefetch_desc(&tmB2);
+      if constexpr (C::W_LOAD) tma_prefetch_desc(&tmS);
     }
     __syncwarp();
     tmem_alloc(tmem_slot, kTmemCols);
@@ -325,12 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (NB == 2) load_operand<B_MN, BN>(sb + C::B_BYTES, &tmB2, &full_bar[st], rb2, nt * BN, k0);
         }
       }
-      // Teardown: make sure every copy this thread issued has landed before the
-      // CTA's shared memory can be released (matters only after an abort).
+      // Teardown: every copy issued here must have landed before the CTA's
+      // shared memory is released (matters only after an abort).
       for (uint32_t st = 0; st < C::STAGES; ++st) {
         if (!(issued_mask & (1u << st))) continue;
-        // The last fill of stage st was fill number f with kc-1 >= st + f*STAGES.
-        const uint32_t f = (kc - 1 - st) / C::STAGES;
+        const uint32_t f = (kc - 1 - st) / C::STAGES;  // last fill of stage st
         mbar_wait_bounded(&full_bar[st], f & 1, abort_flag, 4, &g_device_error);
       }
     }
@@ -339,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole role runs on one thread: tcgen05.mma and tcgen05.commit are
     // issued by a single thread, and a lone waiter cannot diverge from itself.
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, A_MN, B_MN);
+      constexpr uint32_t idesc = make_idesc_bf16(BM, C::N_MMA, A_MN, B_MN);
       uint32_t kc = 0, ls = 0;
       bool ok = true;
       while (ok && iter.next(seg)) {
@@ -360,9 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ksteps = static_cast<int>(min(static_cast<int64_t>(BK / 16), (krem + 15) / 16));
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t accum = (kb > seg.kb0 || ks > 0) ? 1u : 0u;
-            const uint64_t ad = operand_desc<A_MN>(sa, ks);
-            umma_bf16(d_tmem, ad, operand_desc<B_MN>(sb, ks), idesc, accum);
-            if constexpr (NB == 2) umma_bf16(d_tmem + BN, ad, operand_desc<B_MN>(sb + C::B_BYTES, ks), idesc, accum);
+            umma_bf16(d_tmem, operand_desc<A_MN>(sa, ks), operand_desc<B_MN>(sb, ks), idesc, accum);
           }
           umma_commit(&empty_bar[st]);
         }
@@ -375,10 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
     }
     __syncwarp();
-  } else {
+  } else if (warp <= 5) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp % 4;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    uint32_t ls = 0;
+    const int trow = quarter * 32 + lane;  // row of the tile this thread finishes
+    uint32_t ls = 0, wc = 0;
     while (iter.next(seg)) {
       const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
       // Every lane waits (each needs the acquire); the warp leaves together if any gave up,
@@ -389,20 +448,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t mt, nt;
       kp.s.tile_coords(seg.tile, bi, mt, nt);
       const int b1 = bi % p.nb1, b2 = bi / p.nb1;
-      const int64_t m = mt * BM + quarter * 32 + lane;
+      const int64_t m = mt * BM + trow;
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
+      bool ok = true;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32], u[32];
+        float s[32];
+        if constexpr (C::W_LOAD) {
+          const uint32_t slot = wc % C::W_SLOTS, wph = (wc / C::W_SLOTS) & 1;
+          ++wc;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error))) {
+            ok = false;
+            break;
+          }
+          // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
+          const float4* srow = reinterpret_cast<const float4*>(wslots + slot * C::W_SLOT_BYTES + trow * 128);
+          float dep = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = srow[j ^ (trow & 7)];
+            s[4 * j] = x.x;
+            s[4 * j + 1] = x.y;
+            s[4 * j + 2] = x.z;
+            s[4 * j + 3] = x.w;
+            dep += x.x;
+          }
+          // The loader refills this slot with TMA (async proxy) once all 128
+          // threads arrive: every load above must have returned first.
+          fence_proxy_async_shared();
+          mbar_arrive_after(&wempty_bar[slot], dep);
+        }
         tmem_ld_32x32b_x32(tbase + c * 32, r);
-        if constexpr (NB == 2) tmem_ld_32x32b_x32(tbase + BN + c * 32, u);
+        if constexpr (EPI == EPI_GATE) tmem_ld_32x32b_x32(tbase + BN + c * 32, u);
         tmem_wait_ld();
         const int64_t n = nt * BN + c * 32;
-        if (m < p.M && n < p.N) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
+        if (m < p.M && n < p.N) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u, s);
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
+      if (!ok) break;
       ++ls;
+      if constexpr (EPI == EPI_ACCUM) {
+        if (p.fix.counters) {
+          // Publish this CTA's partial sums (each thread's own reductions, then
+          // the whole CTA's through the barrier and a release fence), then count
+          // the CTA in; the last of the tile's contributors finishes the tile
+          // after an acquire fence.
+          __threadfence();
+          epi_barrier();
+          if (trow == 0) {
+            __threadfence();
+            const int prev = atomicAdd(&p.fix.counters[seg.tile], 1);
+            __threadfence();
+            *last_flag = (prev + 1 == kp.s.segments_of(seg.tile)) ? 1 : 0;
+          }
+          epi_barrier();
+          if (*last_flag) {
+            __threadfence();
+            if (m < p.M) fixup_row<BN>(p, b1, b2, m, nt * BN);
+            if (trow == 0) p.fix.counters[seg.tile] = 0;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------- fast-weight loader (update)
+    if constexpr (C::W_LOAD) {
+      if (lane == 0) {
+        uint32_t wc = 0;
+        bool ok = true;
+        while (ok && iter.next(seg)) {
+          int bi;
+          int64_t mt, nt;
+          kp.s.tile_coords(seg.tile, bi, mt, nt);
+          const int b1 = bi % p.nb1, b2 = bi / p.nb1;
+          const int64_t row0 = row_of(p.src, b1, b2) + mt * BM;
+          for (int c = 0; c < BN / 32; ++c, ++wc) {
+            const uint32_t slot = wc % C::W_SLOTS, ph = (wc / C::W_SLOTS) & 1;
+            if (!mbar_wait_bounded(&wempty_bar[slot], ph ^ 1, abort_flag, 5, &g_device_error)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&wfull_bar[slot], C::W_SLOT_BYTES);
+            tma_load_2d(wslots + slot * C::W_SLOT_BYTES, &tmS, &wfull_bar[slot],
+                        static_cast<int>(nt * BN + c * 32), static_cast<int>(row0));
+          }
+        }
+        for (uint32_t slot = 0; slot < C::W_SLOTS && slot < wc; ++slot) {
+          const uint32_t f = (wc - 1 - slot) / C::W_SLOTS;  // last fill of this slot
+          mbar_wait_bounded(&wfull_bar[slot], f & 1, abort_flag, 4, &g_device_error);
+        }
+      }
     }
   }
 
@@ -433,21 +571,25 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-static bool make_map(CUtensorMap* map, const Operand& o, int box_rows) {
+// 2-D tensor map with 128-byte swizzle; the box is 128 bytes wide.
+static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32,
+                     int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(o.cols), static_cast<cuuint64_t>(o.rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(o.ld) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  if (!enc || rows <= 0 || cols <= 0) return false;
+  const int esz = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(o.ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
 static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
-  using C = Cfg<BN, NB>;
+  using C = Cfg<BN, NB, EPI>;
   auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16>;
   static std::mutex mu;
   static uint64_t attr_done = 0;  // bit per device: shared-memory size attribute set
@@ -462,13 +604,18 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
     }
   }
 
-  CUtensorMap mA, mB, mB2;
-  if (!make_map(&mA, p.A, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mB, p.B, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
+  CUtensorMap mA, mB, mB2, mS;
+  if (!make_map(&mA, p.A.ptr, p.A.rows, p.A.cols, p.A.ld, false, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mB, p.B.ptr, p.B.rows, p.B.cols, p.B.ld, false, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
   if (NB == 2) {
-    if (!make_map(&mB2, p.B2, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
+    if (!make_map(&mB2, p.B2.ptr, p.B2.rows, p.B2.cols, p.B2.ld, false, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
   } else {
     mB2 = mB;
+  }
+  if (C::W_LOAD) {
+    if (!make_map(&mS, p.src.ptr, p.src.rows, p.N, p.src.ld, true, BM)) return cudaErrorInvalidValue;
+  } else {
+    mS = mA;
   }
 
   KParams kp;
@@ -485,8 +632,8 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   const int sms = device_sm_count();
   int64_t grid = s.split ? std::min<int64_t>(sms, s.total_iters) : std::min<int64_t>(sms, s.total_tiles);
   if (grid <= 0) return cudaSuccess;
-  count_launch();
-  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM_BYTES, stream>>>(mA, mB, mB2, kp);
+  LaunchMark mark(p.kind, stream);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mA, mB, mB2, mS, kp);
   return cudaGetLastError();
 }
 
@@ -510,6 +657,7 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
   // chunk), the caller guarantees K % 16 == 0.
   const bool a_mn = p.A.mn_major != 0, b_mn = p.B.mn_major != 0;
   if (p.split_k && p.epi != EPI_ACCUM) return cudaErrorInvalidValue;
+  if (p.fix.counters && (!p.split_k || !p.fix.O.ptr || (p.fix.R.ptr && !p.fix.V.ptr))) return cudaErrorInvalidValue;
   switch (p.epi) {
     case EPI_GATE:
       if (!a_mn && b_mn)

@@ -9,8 +9,29 @@
 
 namespace ipttt {
 
-// Launch bookkeeping: every kernel launch of the library calls count_launch().
-void count_launch();
+// Kernel kinds, for launch counting and the optional per-kernel event timing.
+enum KernelKind : int {
+  K_GATE = 0,      // gated up-projection GEMM
+  K_CONV = 1,      // chunk-padded depthwise conv
+  K_PROJ = 2,      // target projection GEMM
+  K_APPLY = 3,     // O_k = Z_k W_k
+  K_RESIDUAL = 4,  // O_k, R_k = O_k - V_k from the apply's fp32 sums
+  K_UPDATE = 5,    // W_{k+1} = W_k + alpha Z_k^T R_k
+  K_GROUP_SUM = 6, // additive scan: per-group Z^T V
+  K_SCAN = 7,      // additive scan: exclusive prefix over groups
+  K_WEIGHT = 8,    // fast-weight copies (bf16 copy of W_o0, W_o0 -> W_final)
+  K_COUNT = 9
+};
+
+// Every kernel launch of the library sits inside one LaunchMark: it counts the
+// launch and, while kernel timing is on, brackets it with CUDA events on `stream`.
+struct LaunchMark {
+  LaunchMark(int kind, cudaStream_t stream);
+  ~LaunchMark();
+  int kind;
+  cudaStream_t stream;
+  int slot;
+};
 int current_device();     // cudaGetDevice, -1 on error
 int device_sm_count();    // SMs of the current device (cached)
 

@@ -163,6 +163,18 @@ ipttt_status ipttt_release(void);
  * library's launches, for profiling).  Host only. */
 int64_t ipttt_last_launch_count(void);
 
+/* Per-kernel timing, a profiling aid that is off by default.  While enabled,
+ * every kernel this library launches is bracketed by two CUDA events on its
+ * stream (no synchronisation is added).  ipttt_kernel_timing(1) clears the
+ * totals and starts recording, (0) stops.  ipttt_kernel_timing_read waits
+ * for the recorded events and returns, for one kernel kind, the launches and
+ * their summed device time in milliseconds since the last start.  Kinds:
+ * 0 gate_up, 1 conv, 2 proj, 3 apply, 4 residual, 5 update, 6 group_sum,
+ * 7 scan, 8 weight_copy (names from ipttt_kernel_name).  Host only. */
+ipttt_status ipttt_kernel_timing(int32_t enable);
+ipttt_status ipttt_kernel_timing_read(int32_t kind, int64_t* launches, double* total_ms);
+const char* ipttt_kernel_name(int32_t kind);
+
 const char* ipttt_status_string(ipttt_status status);
 int ipttt_version(void);
 
