@@ -25,8 +25,9 @@ EXPORTS = (
     "ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
     "ipttt_status_string", "ipttt_version", "ipttt_kernel_timing", "ipttt_kernel_timing_read",
-    "ipttt_kernel_name",
+    "ipttt_kernel_name", "ipttt_make_targets_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
 KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy")
 
 
@@ -55,6 +56,7 @@ def lib() -> ctypes.CDLL:
         dp = ctypes.POINTER(Dims)
         L.ipttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
         L.ipttt_make_targets.argtypes = [vp, vp, vp, vp, i64, i64, dp, vp]
+        L.ipttt_make_targets_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, dp, vp]
         L.ipttt_gate_up.argtypes = [vp, vp, vp, vp, i64, dp, vp]
         L.ipttt_chunk_forward.argtypes = [vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
         L.ipttt_workspace_size.argtypes = [dp, i64, i64, i32, i32, ctypes.POINTER(ctypes.c_size_t)]
@@ -71,7 +73,8 @@ def lib() -> ctypes.CDLL:
         L.ipttt_kernel_timing_read.restype = i32
         L.ipttt_kernel_name.argtypes = [i32]
         L.ipttt_kernel_name.restype = ctypes.c_char_p
-        for name in ("ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
+        for name in ("ipttt_layer_forward", "ipttt_make_targets", "ipttt_make_targets_noalloc", "ipttt_gate_up",
+                     "ipttt_chunk_forward",
                      "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release"):
             getattr(L, name).restype = i32
         _lib = L
@@ -162,6 +165,26 @@ def make_targets(E, conv_w, P, V, L: int, B: int, stream=None) -> None:
     st = lib().ipttt_make_targets(_ptr(E, "E", act), _ptr(conv_w, "conv_w", torch.float32), _ptr(P, "P", act),
                                   _ptr(V, "V", act), int(L), int(B), ctypes.byref(dm), _stream(stream))
     _check(st, "ipttt_make_targets")
+
+
+def make_targets_noalloc(E, conv_w, P, V, L: int, B: int, stream=None) -> None:
+    """ipttt_make_targets_noalloc: the same targets as make_targets, with the
+    conv scratch in the library's fixed device array, so nothing is allocated.
+    For callers that cannot allocate device memory here (memory already handed
+    out by another allocator, or no room for a possibly synchronising
+    cudaMalloc).  batch*L*d act elements must fit in NOALLOC_SCRATCH_BYTES."""
+    torch = _torch()
+    act = E.dtype
+    d = E.shape[1]
+    dm = dims(E.shape[0] // L if L else 0, d, 8, _dtype_code(E))
+    st = lib().ipttt_make_targets_noalloc(_ptr(E, "E", act), _ptr(conv_w, "conv_w", torch.float32),
+                                          _ptr(P, "P", act), _ptr(V, "V", act), int(L), int(B), ctypes.byref(dm),
+                                          _stream(stream))
+    if st == ERR_INVALID_ARG and E.shape[0] * d * E.element_size() > NOALLOC_SCRATCH_BYTES:
+        raise IptttError(st, f"ipttt_make_targets_noalloc: {E.shape[0]} x {d} conv rows need "
+                             f"{E.shape[0] * d * E.element_size()} bytes, more than the fixed "
+                             f"{NOALLOC_SCRATCH_BYTES}-byte scratch")
+    _check(st, "ipttt_make_targets_noalloc")
 
 
 def gate_up(X, W_g, W_u, Z, stream=None) -> None:

@@ -75,6 +75,8 @@ void drain_timing_locked() {
 }
 }  // namespace
 
+void reset_launch_count() { t_launches = 0; }
+
 LaunchMark::LaunchMark(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
   ++t_launches;
   std::lock_guard<std::mutex> g(g_timing_mu);

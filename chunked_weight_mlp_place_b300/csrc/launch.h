@@ -33,6 +33,7 @@ struct LaunchMark {
   int slot;
 };
 int current_device();     // cudaGetDevice, -1 on error
+void reset_launch_count(); // start counting the launches of a new C-ABI call
 int device_sm_count();    // SMs of the current device (cached)
 
 // Read the device error word of the current device (0 = no capped wait ran out) and clear it.

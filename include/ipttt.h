@@ -145,6 +145,35 @@ ipttt_status ipttt_chunk_forward(const void* Z, const void* V, const float* W_o0
                                  int64_t B, float eta, ipttt_rule rule, void* O, float* W_final,
                                  const ipttt_dims* dims, ipttt_stream stream);
 
+/*
+ * Targets without any allocation: the same result as ipttt_make_targets (same
+ * kernels), but the conv output it needs as scratch lives in a fixed array
+ * inside this library rather than in the pool that ipttt_make_targets grows
+ * with cudaMalloc.  The pages have no counterpart of this call; it is for
+ * callers that cannot allocate device memory at this point -- a process whose
+ * GPU memory is already handed out by another allocator (where a new
+ * cudaMalloc can fail or break that allocator's bookkeeping), or a service
+ * that cannot pay for cudaMalloc / cudaFree, which may synchronise the device.
+ *
+ * - Limit: batch*L*d elements of the act type must fit in
+ *   IPTTT_NOALLOC_SCRATCH_BYTES (16 MiB, e.g. 3276 tokens at d = 2560 in
+ *   bf16); larger calls return IPTTT_ERR_INVALID_ARG and do nothing.  Split
+ *   the tokens into chunk-aligned pieces (the conv never reads past a chunk).
+ * - The array takes IPTTT_NOALLOC_SCRATCH_BYTES on every GPU that loads the
+ *   library, until the process exits.
+ * - The first call on a device looks the array's address up on that device
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ * - Every call shares the array: calls that overlap on the GPU (unordered
+ *   streams) race on it.  Nothing in it needs clearing between calls.
+ * - Arguments, layouts and errors otherwise as ipttt_make_targets; no
+ *   cudaMalloc, cudaFree or other allocating call is made.
+ */
+#define IPTTT_NOALLOC_SCRATCH_BYTES (16u << 20)
+ipttt_status ipttt_make_targets_noalloc(const void* E, const float* conv_w, const void* P, void* V,
+                                        int64_t L, int64_t B, const ipttt_dims* dims,
+                                        ipttt_stream stream);
+
 /* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or
  * ipttt_chunk_forward (with_activations = 0) needs for these sizes.  Host only. */
 ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, ipttt_rule rule,

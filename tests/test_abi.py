@@ -130,3 +130,13 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libipttt.so"))
     with pytest.raises(ImportError):
         _lib.lib()
+
+
+def test_noalloc_targets_size_limit_is_checked_on_the_host(L):
+    dm = _dims(batch=1, d=2560)
+    # 4096 tokens x 2560 bf16 = 20 MiB > the 16 MiB fixed scratch: rejected before any device call
+    assert L.ipttt_make_targets_noalloc(FAKE, FAKE, FAKE, FAKE, 4096, 1024, ctypes.byref(dm), None) == \
+        _lib.ERR_INVALID_ARG
+    assert L.ipttt_make_targets_noalloc(FAKE, FAKE, FAKE, FAKE, 100, 64, ctypes.byref(dm), None) == \
+        _lib.ERR_INVALID_ARG
+    assert L.ipttt_make_targets_noalloc(0, 0, 0, 0, 0, 64, ctypes.byref(dm), None) == _lib.OK
