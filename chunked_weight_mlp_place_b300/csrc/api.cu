@@ -6,7 +6,7 @@
 //   Z = SiLU(X W_g) * (X W_u)                          one GEMM, gate epilogue
 //   V = Conv(E) P                                      conv kernel + GEMM
 //   MSE rule, for k = 0 .. K-1 (sequential):
-//     apply     O_acc = Z_k W_k          (bf16 W copy, split over d_ff, fp32 atomics)
+//     apply     O_acc = Z_k W_k          (bf16 W copy, split over d_ff, fp32 reductions)
 //     residual  O_k = O_acc; R_k = O_acc - V_k; O_acc = 0
 //     update    W_{k+1} = W_k - (eta/B) Z_k^T R_k; bf16 copy of W_{k+1}
 //   additive rule, chunk-parallel scan over G groups of g chunks (G*g = K):
@@ -337,14 +337,8 @@ int64_t scan_groups(int64_t K) {
 }
 
 struct EngineLayout {
-  size_t o_acc = 0, r = 0, wb = 0, d = 0, db = 0, counters = 0, total = 0;
-  int64_t n_counters = 0;
+  size_t o_acc = 0, r = 0, wb = 0, d = 0, db = 0, total = 0;
 };
-
-// Output tiles of the apply GEMM (128 x 256), one split-K counter each.
-int64_t apply_tiles(const ipttt_dims* dm, int64_t B, int64_t entries) {
-  return ((B + 127) / 128) * ((dm->d + 255) / 256) * entries;
-}
 
 EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rule rule, size_t base) {
   EngineLayout e;
@@ -357,15 +351,12 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
     e.o_acc = c.take<float>(dm->batch * B * dm->d);
     e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
     if (bf16) e.wb = c.take<uint16_t>(dm->batch * nw);
-    e.n_counters = apply_tiles(dm, B, dm->batch);
   } else {
     const int64_t G = scan_groups(K);
     e.o_acc = c.take<float>(G * dm->batch * B * dm->d);
     e.d = c.take<float>(G * dm->batch * nw);
     if (bf16) e.db = c.take<uint16_t>(G * dm->batch * nw);
-    e.n_counters = apply_tiles(dm, B, G * dm->batch);
   }
-  e.counters = c.take<int>(e.n_counters);
   e.total = c.off;
   return e;
 }
@@ -382,11 +373,9 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
 
   if (rule == IPTTT_RULE_MSE) {
     void* R = ws + lay.r;
-    int* counters = reinterpret_cast<int*>(ws + lay.counters);
     __nv_bfloat16* Wb = bf16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.wb) : nullptr;
     if (bf16) IPTTT_CUDA(launch_to_bf16(W0, w0s, Wb, batch, nw, st));
     IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * B * d, st));
-    if (bf16) IPTTT_CUDA(cudaMemsetAsync(counters, 0, sizeof(int) * lay.n_counters, st));
     const int64_t w0_rows = (dm->w0_per_seq ? batch : 1) * dff;
     for (int64_t k = 0; k < K; ++k) {
       // apply: O_acc[s] = Z_k[s] W_k[s]; on the tensor cores the last split
@@ -405,14 +394,8 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       a.kind = K_APPLY;
       a.D = out(o_acc, d, 0, B);
       a.split_k = 1;
-      if (bf16) {
-        a.fix.counters = counters;
-        a.fix.O = out(O, d, k * B, L);
-        a.fix.V = out(const_cast<void*>(V), d, k * B, L);
-        a.fix.R = out(R, d, 0, B);
-      }
       IPTTT_CUDA(gemm(a, bf16, st));
-      if (!bf16) {
+      {
         // residual: O_k = O_acc, R_k = O_acc - V_k, O_acc = 0
         ResidualArgs ra;
         ra.acc = o_acc;
@@ -468,8 +451,6 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   // exclusive scan over groups -> the fast weight at the start of each group
   IPTTT_CUDA(launch_group_scan(D, Db, W0, w0s, Wf, G, batch, nw, alpha, st));
   IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * G * batch * B * d, st));
-  int* counters = reinterpret_cast<int*>(ws + lay.counters);
-  if (bf16) IPTTT_CUDA(cudaMemsetAsync(counters, 0, sizeof(int) * lay.n_counters, st));
   for (int64_t i = 0; i < g; ++i) {
     GemmProblem a;
     a.M = B;
@@ -483,12 +464,8 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     a.kind = K_APPLY;
     a.D = out(o_acc, d, 0, B, batch * B);
     a.split_k = 1;
-    if (bf16) {
-      a.fix.counters = counters;
-      a.fix.O = out(O, d, i * B, L, g * B);
-    }
     IPTTT_CUDA(gemm(a, bf16, st));
-    if (!bf16) {
+    {
       ResidualArgs ra;
       ra.acc = o_acc;
       ra.O = O;

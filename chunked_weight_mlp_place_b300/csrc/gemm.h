@@ -36,15 +36,6 @@ struct OutRef {
   int64_t rows = 0;                  // rows of the whole matrix (needed where it is read by TMA)
 };
 
-// Split-K fix-up of EPI_ACCUM on the tensor-core path: the CTA that adds the
-// last partial sum of an output tile turns the tile's fp32 sums into the chunk
-// outputs, O = act(acc) and, if V is given, R = act(acc - V), and clears the
-// sums and the tile's counter for the next launch.  No CTA waits for another.
-struct Fixup {
-  int* counters = nullptr;  // one int per output tile, zero between launches; null = no fix-up
-  OutRef O, V, R;           // act-dtype rows, indexed like D
-};
-
 struct GemmProblem {
   int64_t M = 0, N = 0, K = 0;
   int nb1 = 1, nb2 = 1;
@@ -56,7 +47,6 @@ struct GemmProblem {
   OutRef Db;         // AXPY: optional bf16 copy
   float alpha = 1.0f;
   int split_k = 0;   // tensor-core path: 1 = balance (tile, k-block) work over CTAs (needs EPI_ACCUM)
-  Fixup fix;         // tensor-core path, EPI_ACCUM with split_k
   int kind = 0;      // KernelKind label (launch counting / timing)
 };
 

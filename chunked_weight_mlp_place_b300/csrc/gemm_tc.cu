@@ -20,8 +20,8 @@
 // the main loop of the next.  Work is either whole output tiles, strided over
 // the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
 // share of the (tile, k-block) iteration space per CTA; partial sums are added
-// into an fp32 buffer with vector atomics, and the CTA that adds the last
-// partial sum of a tile finishes it (O and the residual R = O - V).
+// into an fp32 buffer with vector reductions (the residual kernel then turns
+// them into O and R = O - V).
 //
 // Every mbarrier wait is capped (common.cuh); a CTA whose wait runs out flags
 // the others, drains its in-flight TMA copies and MMAs, frees its TMEM and
@@ -47,7 +47,6 @@ constexpr int BK = 64;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns between the two accumulator buffers
 constexpr int kEpiThreads = 128;
-constexpr int kEpiBarrier = 1;   // named barrier of the four epilogue warps
 
 template <int BN, int NB, int EPI>
 struct Cfg {
@@ -91,12 +90,7 @@ struct Sched {
     mt = first_m + q % gm;
     nt = q / gm;
   }
-  // Split mode: CTA c owns iterations [floor(c*T/G), floor((c+1)*T/G)); the
-  // owner of iteration i is floor(((i+1)*G - 1) / T).
-  __device__ int64_t owner(int64_t i) const { return ((i + 1) * gridDim.x - 1) / total_iters; }
-  __device__ int segments_of(int64_t t) const {
-    return static_cast<int>(owner((t + 1) * kb_total - 1) - owner(t * kb_total) + 1);
-  }
+  // Split mode: CTA c owns iterations [floor(c*T/G), floor((c+1)*T/G)).
 };
 
 struct SegIter {
@@ -141,10 +135,6 @@ __device__ __forceinline__ int64_t row_of(const Operand& o, int b1, int b2) {
 }
 __device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) {
   return o.y0 + b1 * o.ys1 + b2 * o.ys2;
-}
-
-__device__ __forceinline__ void epi_barrier() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
 }
 
 // Issue the TMA copies of one operand tile (extent EXT along M or N, BK along K).
@@ -224,12 +214,9 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
     float* d = static_cast<float*>(p.D.ptr) + row * p.D.ld + n;
     if (full) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        atomicAdd(reinterpret_cast<float4*>(d) + q,
-                  make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
-                              __uint_as_float(r[4 * q + 3])));
+      for (int q = 0; q < 8; ++q) red_add_v4(d + 4 * q, r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
     } else {
-      for (int i = 0; i < 32 && n + i < p.N; ++i) atomicAdd(d + i, __uint_as_float(r[i]));
+      for (int i = 0; i < 32 && n + i < p.N; ++i) red_add(d + i, __uint_as_float(r[i]));
     }
   } else {  // EPI_AXPY
     const int64_t row = row_of(p.D, b1, b2) + m;
@@ -256,46 +243,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
   }
 }
 
-// Split-K fix-up of one output row: O = bf16(acc), R = bf16(acc - V), acc = 0.
-// The sums were added by other SMs' atomics in L2, so they are read past L1.
-template <int BN>
-__device__ __forceinline__ void fixup_row(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n0) {
-  float* acc = static_cast<float*>(p.D.ptr) + (row_of(p.D, b1, b2) + m) * p.D.ld;
-  __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.fix.O.ptr) + (row_of(p.fix.O, b1, b2) + m) * p.fix.O.ld;
-  const __nv_bfloat16* V =
-      p.fix.V.ptr ? static_cast<const __nv_bfloat16*>(p.fix.V.ptr) + (row_of(p.fix.V, b1, b2) + m) * p.fix.V.ld
-                  : nullptr;
-  __nv_bfloat16* R =
-      p.fix.R.ptr ? static_cast<__nv_bfloat16*>(p.fix.R.ptr) + (row_of(p.fix.R, b1, b2) + m) * p.fix.R.ld : nullptr;
-  const int64_t n_end = min(n0 + BN, p.N);
-  int64_t n = n0;
-  for (; n + 8 <= n_end; n += 8) {
-    float4* a4 = reinterpret_cast<float4*>(acc + n);
-    const float4 x0 = __ldcg(a4), x1 = __ldcg(a4 + 1);
-    a4[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    a4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-    *reinterpret_cast<uint4*>(O + n) = pack8_bf16(v);
-    if (R) {
-      const uint4 vr = *reinterpret_cast<const uint4*>(V + n);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = __bfloat1622float2(h[q]);
-        v[2 * q] -= f.x;
-        v[2 * q + 1] -= f.y;
-      }
-      *reinterpret_cast<uint4*>(R + n) = pack8_bf16(v);
-    }
-  }
-  for (; n < n_end; ++n) {
-    const float x = __ldcg(acc + n);
-    acc[n] = 0.0f;
-    O[n] = __float2bfloat16_rn(x);
-    if (R) R[n] = __float2bfloat16_rn(x - __bfloat162float(V[n]));
-  }
-}
-
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
 __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -317,7 +264,6 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
   uint64_t* wempty_bar = wfull_bar + C::W_SLOTS;    // [W_SLOTS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty_bar + C::W_SLOTS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const GemmProblem& p = kp.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -338,7 +284,6 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
         mbar_init(&wempty_bar[i], kEpiThreads);
       }
       *abort_flag = 0;
-      *last_flag = 0;
       fence_mbarrier_init();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
@@ -490,28 +435,6 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       mbar_arrive(&tempty_bar[acc]);
       if (!ok) break;
       ++ls;
-      if constexpr (EPI == EPI_ACCUM) {
-        if (p.fix.counters) {
-          // Publish this CTA's partial sums (each thread's own reductions, then
-          // the whole CTA's through the barrier and a release fence), then count
-          // the CTA in; the last of the tile's contributors finishes the tile
-          // after an acquire fence.
-          __threadfence();
-          epi_barrier();
-          if (trow == 0) {
-            __threadfence();
-            const int prev = atomicAdd(&p.fix.counters[seg.tile], 1);
-            __threadfence();
-            *last_flag = (prev + 1 == kp.s.segments_of(seg.tile)) ? 1 : 0;
-          }
-          epi_barrier();
-          if (*last_flag) {
-            __threadfence();
-            if (m < p.M) fixup_row<BN>(p, b1, b2, m, nt * BN);
-            if (trow == 0) p.fix.counters[seg.tile] = 0;
-          }
-        }
-      }
     }
   } else {
     // ------------------------------------------- fast-weight loader (update)
@@ -544,6 +467,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
     }
   }
 
+  // Roles that ran on one lane re-converge their warp first: the CTA barrier
+  // below is a warp-aligned instruction, and TMEM may only be freed once every
+  // warp (the epilogue's TMEM loads included) has reached it.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -657,7 +584,6 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
   // chunk), the caller guarantees K % 16 == 0.
   const bool a_mn = p.A.mn_major != 0, b_mn = p.B.mn_major != 0;
   if (p.split_k && p.epi != EPI_ACCUM) return cudaErrorInvalidValue;
-  if (p.fix.counters && (!p.split_k || !p.fix.O.ptr || (p.fix.R.ptr && !p.fix.V.ptr))) return cudaErrorInvalidValue;
   switch (p.epi) {
     case EPI_GATE:
       if (!a_mn && b_mn)
