@@ -386,13 +386,14 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       a.K = dff;
       a.nb1 = bint;
       a.A = mat(Z, batch * L, dff, 0, k * B, L);
-      if (bf16)
+      if (bf16) {
         a.B = mat(Wb, batch * dff, d, 1, 0, dff);
-      else
+      } else {
         a.B = (k == 0) ? mat(W0, w0_rows, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
+      }
       a.epi = EPI_ACCUM;
       a.kind = K_APPLY;
-      a.D = out(o_acc, d, 0, B);
+      a.D = out(o_acc, d, 0, B, 0, batch * B);
       a.split_k = 1;
       IPTTT_CUDA(gemm(a, bf16, st));
       {
@@ -421,7 +422,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.kind = K_UPDATE;
       u.D = out(Wf, d, 0, dff, 0, batch * dff);
       u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r, 0, w0_rows) : out(Wf, d, 0, dff, 0, batch * dff);
-      if (bf16 && k + 1 < K) u.Db = out(Wb, d, 0, dff);
+      if (bf16 && k + 1 < K) u.Db = out(Wb, d, 0, dff, 0, batch * dff);
       u.alpha = -eta / static_cast<float>(B);
       IPTTT_CUDA(gemm(u, bf16, st));
     }
@@ -462,7 +463,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     a.B = bf16 ? mat(Db, G * batch * dff, d, 1, 0, dff, batch * dff) : mat(D, G * batch * dff, d, 1, 0, dff, batch * dff);
     a.epi = EPI_ACCUM;
     a.kind = K_APPLY;
-    a.D = out(o_acc, d, 0, B, batch * B);
+    a.D = out(o_acc, d, 0, B, batch * B, G * batch * B);
     a.split_k = 1;
     IPTTT_CUDA(gemm(a, bf16, st));
     {
@@ -491,7 +492,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.kind = K_UPDATE;
       u.D = out(D, d, 0, dff, batch * dff, G * batch * dff);
       u.src = u.D;
-      if (bf16) u.Db = out(Db, d, 0, dff, batch * dff);
+      if (bf16) u.Db = out(Db, d, 0, dff, batch * dff, G * batch * dff);
       u.alpha = alpha;
       IPTTT_CUDA(gemm(u, bf16, st));
     }

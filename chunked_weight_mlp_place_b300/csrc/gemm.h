@@ -18,7 +18,7 @@ namespace ipttt {
 enum EpiKind : int {
   EPI_STORE = 0,  // D = acc                                  (D in the act dtype)
   EPI_GATE = 1,   // D = SiLU(acc_g) * acc_u, acc_u from B2   (D in the act dtype)
-  EPI_ACCUM = 2,  // D += acc, fp32 atomics                   (D fp32; partial sums)
+  EPI_ACCUM = 2,  // D += acc, fp32 reductions in L2          (D fp32; partial sums)
   EPI_AXPY = 3,   // D = src + alpha * acc (fp32); Db = bf16(D) if Db != nullptr
 };
 
@@ -27,13 +27,15 @@ struct Operand {
   int64_t rows = 0, cols = 0, ld = 0;  // matrix extent and row stride (elements)
   int mn_major = 0;                    // 1: K runs along rows
   int64_t y0 = 0, ys1 = 0, ys2 = 0;    // per-batch row offsets
+  int evict_first = 0;                 // tensor-core path: read with the L2 evict-first policy
 };
 
 struct OutRef {
   void* ptr = nullptr;
   int64_t ld = 0;
   int64_t y0 = 0, ys1 = 0, ys2 = 0;  // row = y0 + b1*ys1 + b2*ys2 + m, column n
-  int64_t rows = 0;                  // rows of the whole matrix (needed where it is read by TMA)
+  int64_t rows = 0;                  // rows of the whole matrix (needed where TMA reads or writes it)
+  int evict_first = 0;               // tensor-core path: TMA traffic with the L2 evict-first policy
 };
 
 struct GemmProblem {

@@ -12,16 +12,25 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16)
 //               into a TMEM accumulator; tcgen05.commit frees each stage;
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output
-//               row) and apply the fused epilogue straight to global memory;
+//               row) and apply the fused epilogue;
 //   warp 6      (update only) fast-weight loader: streams the fp32 W tile the
 //               epilogue will read-modify-write into swizzled shared memory
 //               slots ahead of time, so the epilogue never waits on HBM.
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next.  Work is either whole output tiles, strided over
 // the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
-// share of the (tile, k-block) iteration space per CTA; partial sums are added
-// into an fp32 buffer with vector reductions (the residual kernel then turns
-// them into O and R = O - V).
+// share of the (tile, k-block) iteration space per CTA.
+//
+// Epilogues that move much data go through shared memory and TMA, so global
+// memory sees whole 128-byte lines instead of one row per lane:
+//   apply (split mode)  each warp stages its 32 rows x 32 columns of fp32 partial
+//                       sums and adds them into the fp32 sums in L2 with a TMA
+//                       reduce (the residual kernel then turns the sums into
+//                       O and R = O - V);
+//   update              each warp overwrites its quarter of the fp32 W slot
+//                       with W + alpha*acc in place and stores it with TMA,
+//                       together with a staged bf16 copy; a slot goes back to
+//                       the loader once the store has read it.
 //
 // Every mbarrier wait is capped (common.cuh); a CTA whose wait runs out flags
 // the others, drains its in-flight TMA copies and MMAs, frees its TMEM and
@@ -51,19 +60,28 @@ constexpr int kEpiThreads = 128;
 template <int BN, int NB, int EPI>
 struct Cfg {
   static constexpr bool W_LOAD = (EPI == EPI_AXPY);
+  static constexpr bool RED = (EPI == EPI_ACCUM);
   static constexpr int THREADS = W_LOAD ? 224 : 192;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;  // per B operand
   static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
   static constexpr int N_MMA = BN * NB;        // the B operands sit side by side: one MMA covers them
-  static constexpr int W_SLOT_BYTES = BM * 32 * 4;  // 128 rows x 32 fp32 columns
-  static constexpr int W_SLOTS = W_LOAD ? 4 : 0;
+  // update: the fp32 W tile streams through slots of 128 rows x 16 columns (64-byte rows)
+  static constexpr int WC = 16;
+  static constexpr int W_SLOT_BYTES = BM * WC * 4;
+  static constexpr int W_SLOTS = W_LOAD ? 8 : 0;
+  // per epilogue warp, two staging buffers for TMA stores / reductions:
+  //   apply: 32 rows x 32 fp32 (128-byte rows); update: 32 rows x 16 bf16 (32-byte rows)
+  static constexpr int STG_BYTES = RED ? 32 * 32 * 4 : (W_LOAD ? 32 * WC * 2 : 0);
+  static constexpr int STG_TOTAL = 4 * 2 * STG_BYTES;
   static constexpr int STAGES = W_LOAD ? 3 : 4;
   static constexpr int BAR_BYTES = 512;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + W_SLOTS * W_SLOT_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + W_SLOTS * W_SLOT_BYTES + STG_TOTAL + BAR_BYTES;
   static_assert(N_MMA <= kAccStride && N_MMA % 16 == 0, "accumulator width");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(W_SLOT_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0, "1024-byte aligned swizzle atoms");
 };
 
 struct Seg {
@@ -140,13 +158,22 @@ __device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) {
 // Issue the TMA copies of one operand tile (extent EXT along M or N, BK along K).
 template <bool MN, int EXT>
 __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int64_t row0,
-                                             int64_t i0, int64_t k0) {
+                                             int64_t i0, int64_t k0, int evict_first, uint64_t pol) {
   if constexpr (MN) {
 #pragma unroll
-    for (int j = 0; j < EXT / 64; ++j)
-      tma_load_2d(dst + j * (64 * BK * 2), map, bar, static_cast<int>(i0 + 64 * j), static_cast<int>(row0 + k0));
+    for (int j = 0; j < EXT / 64; ++j) {
+      const int x = static_cast<int>(i0 + 64 * j), y = static_cast<int>(row0 + k0);
+      if (evict_first)
+        tma_load_2d_hint(dst + j * (64 * BK * 2), map, bar, x, y, pol);
+      else
+        tma_load_2d(dst + j * (64 * BK * 2), map, bar, x, y);
+    }
   } else {
-    tma_load_2d(dst, map, bar, static_cast<int>(k0), static_cast<int>(row0 + i0));
+    const int x = static_cast<int>(k0), y = static_cast<int>(row0 + i0);
+    if (evict_first)
+      tma_load_2d_hint(dst, map, bar, x, y, pol);
+    else
+      tma_load_2d(dst, map, bar, x, y);
   }
 }
 
@@ -173,12 +200,11 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   return w;
 }
 
-// Epilogue of 32 consecutive columns n.. of row m.  `s` is the fp32 source row
-// (AXPY only: 32 values already staged in registers).
+// Row-per-lane epilogue of 32 consecutive columns n.. of row m (gate, proj,
+// group sums, and the rows of a split-mode tile that a TMA box cannot cover).
 template <int EPI, bool OUT_BF16>
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
-                                               const uint32_t (&r)[32], const uint32_t (&u)[32],
-                                               const float (&s)[32]) {
+                                               const uint32_t (&r)[32], const uint32_t (&u)[32]) {
   const bool full = (n + 32 <= p.N);
   if constexpr (EPI == EPI_STORE || EPI == EPI_GATE) {
     float v[32];
@@ -218,28 +244,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
     } else {
       for (int i = 0; i < 32 && n + i < p.N; ++i) red_add(d + i, __uint_as_float(r[i]));
     }
-  } else {  // EPI_AXPY
-    const int64_t row = row_of(p.D, b1, b2) + m;
-    float* d = static_cast<float*>(p.D.ptr) + row * p.D.ld + n;
-    __nv_bfloat16* db = nullptr;
-    if (p.Db.ptr) db = static_cast<__nv_bfloat16*>(p.Db.ptr) + (row_of(p.Db, b1, b2) + m) * p.Db.ld + n;
-    float w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = fmaf(p.alpha, __uint_as_float(r[i]), s[i]);
-    if (full) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        reinterpret_cast<float4*>(d)[q] = make_float4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-      if (db) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(db)[q] = pack8_bf16(w + 8 * q);
-      }
-    } else {
-      for (int i = 0; i < 32 && n + i < p.N; ++i) {
-        d[i] = w[i];
-        if (db) db[i] = __float2bfloat16_rn(w[i]);
-      }
-    }
   }
 }
 
@@ -247,6 +251,7 @@ template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
 __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmS,
+                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmDb,
                    const __grid_constant__ KParams kp) {
   using C = Cfg<BN, NB, EPI>;
   extern __shared__ uint8_t smem_raw[];
@@ -254,7 +259,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* stages = smem;
   uint8_t* wslots = smem + C::STAGES * C::STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wslots + C::W_SLOTS * C::W_SLOT_BYTES);
+  uint8_t* stg = wslots + C::W_SLOTS * C::W_SLOT_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + C::STG_TOTAL);
   uint64_t* full_bar = bars;                        // [STAGES]
   uint64_t* empty_bar = bars + C::STAGES;           // [STAGES]
   uint64_t* tfull_bar = bars + 2 * C::STAGES;       // [2]
@@ -281,14 +287,18 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       mbar_init(drain_bar, 1);
       for (int i = 0; i < C::W_SLOTS; ++i) {
         mbar_init(&wfull_bar[i], 1);
-        mbar_init(&wempty_bar[i], kEpiThreads);
+        mbar_init(&wempty_bar[i], 4);  // one arrival per epilogue warp
       }
       *abort_flag = 0;
       fence_mbarrier_init();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       if constexpr (NB == 2) tma_prefetch_desc(&tmB2);
-      if constexpr (C::W_LOAD) tma_prefetch_desc(&tmS);
+      if constexpr (C::W_LOAD) {
+        tma_prefetch_desc(&tmS);
+        tma_prefetch_desc(&tmDb);
+      }
+      if constexpr (C::W_LOAD || C::RED) tma_prefetch_desc(&tmD);
     }
     __syncwarp();
     tmem_alloc(tmem_slot, kTmemCols);
@@ -306,6 +316,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
       uint32_t kc = 0;
       uint32_t issued_mask = 0;
       bool ok = true;
@@ -326,9 +337,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
           mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
           issued_mask |= 1u << st;
           const int64_t k0 = static_cast<int64_t>(kb) * BK;
-          load_operand<A_MN, BM>(sa, &tmA, &full_bar[st], ra, mt * BM, k0);
-          load_operand<B_MN, BN>(sb, &tmB, &full_bar[st], rb, nt * BN, k0);
-          if constexpr (NB == 2) load_operand<B_MN, BN>(sb + C::B_BYTES, &tmB2, &full_bar[st], rb2, nt * BN, k0);
+          load_operand<A_MN, BM>(sa, &tmA, &full_bar[st], ra, mt * BM, k0, p.A.evict_first, pol);
+          load_operand<B_MN, BN>(sb, &tmB, &full_bar[st], rb, nt * BN, k0, p.B.evict_first, pol);
+          if constexpr (NB == 2)
+            load_operand<B_MN, BN>(sb + C::B_BYTES, &tmB2, &full_bar[st], rb2, nt * BN, k0, p.B2.evict_first, pol);
         }
       }
       // Teardown: every copy issued here must have landed before the CTA's
@@ -377,12 +389,14 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       umma_commit(drain_bar);
       mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
     }
-    __syncwarp();
   } else if (warp <= 5) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp % 4;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    const int quarter = warp % 4;          // TMEM lanes 32*quarter .. +31 belong to this warp
     const int trow = quarter * 32 + lane;  // row of the tile this thread finishes
-    uint32_t ls = 0, wc = 0;
+    uint8_t* my_stg = stg + quarter * 2 * C::STG_BYTES;
+    uint64_t pol = 0;
+    if constexpr (C::W_LOAD) pol = l2_policy_evict_first();
+    uint32_t ls = 0, wc = 0, sc = 0;
     while (iter.next(seg)) {
       const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
       // Every lane waits (each needs the acquire); the warp leaves together if any gave up,
@@ -394,52 +408,121 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       kp.s.tile_coords(seg.tile, bi, mt, nt);
       const int b1 = bi % p.nb1, b2 = bi / p.nb1;
       const int64_t m = mt * BM + trow;
+      // this warp's 32 rows can go through one TMA box only if all of them are rows of the problem
+      const bool box_rows = (mt * BM + quarter * 32 + 32 <= p.M);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
       bool ok = true;
+      if constexpr (C::W_LOAD) {
+        // ---- update: W = src + alpha * acc in the slot, TMA stores of W and its bf16 copy
+        const int yD = static_cast<int>(row_of(p.D, b1, b2) + mt * BM + quarter * 32);
+        const int yDb = static_cast<int>(row_of(p.Db, b1, b2) + mt * BM + quarter * 32);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32], u[32];
-        float s[32];
-        if constexpr (C::W_LOAD) {
+        for (int c = 0; c < BN / C::WC; ++c, ++wc) {
           const uint32_t slot = wc % C::W_SLOTS, wph = (wc / C::W_SLOTS) & 1;
-          ++wc;
           if (!__all_sync(0xffffffffu,
                           mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error))) {
             ok = false;
             break;
           }
-          // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
-          const float4* srow = reinterpret_cast<const float4*>(wslots + slot * C::W_SLOT_BYTES + trow * 128);
-          float dep = 0.0f;
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tbase + c * C::WC, r);
+          tmem_wait_ld();
+          // 64-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 1) & 3)
+          float4* srow = reinterpret_cast<float4*>(wslots + slot * C::W_SLOT_BYTES + trow * 64);
+          float w[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 x = srow[j ^ (trow & 7)];
-            s[4 * j] = x.x;
-            s[4 * j + 1] = x.y;
-            s[4 * j + 2] = x.z;
-            s[4 * j + 3] = x.w;
-            dep += x.x;
+          for (int j = 0; j < 4; ++j) {
+            const float4 x = srow[j ^ ((trow >> 1) & 3)];
+            w[4 * j] = fmaf(p.alpha, __uint_as_float(r[4 * j]), x.x);
+            w[4 * j + 1] = fmaf(p.alpha, __uint_as_float(r[4 * j + 1]), x.y);
+            w[4 * j + 2] = fmaf(p.alpha, __uint_as_float(r[4 * j + 2]), x.z);
+            w[4 * j + 3] = fmaf(p.alpha, __uint_as_float(r[4 * j + 3]), x.w);
           }
-          // The loader refills this slot with TMA (async proxy) once all 128
-          // threads arrive: every load above must have returned first.
+          const int64_t n = nt * BN + c * C::WC;
+          if (box_rows) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              srow[j ^ ((trow >> 1) & 3)] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            if (p.Db.ptr) {
+              // 32-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 2) & 1)
+              uint4* brow = reinterpret_cast<uint4*>(my_stg + (wc & 1) * C::STG_BYTES + lane * 32);
+              brow[0 ^ ((lane >> 2) & 1)] = pack8_bf16(w);
+              brow[1 ^ ((lane >> 2) & 1)] = pack8_bf16(w + 8);
+            }
+          } else if (m < p.M) {
+            float* d = static_cast<float*>(p.D.ptr) + (row_of(p.D, b1, b2) + m) * p.D.ld + n;
+            __nv_bfloat16* db =
+                p.Db.ptr ? static_cast<__nv_bfloat16*>(p.Db.ptr) + (row_of(p.Db, b1, b2) + m) * p.Db.ld + n : nullptr;
+            for (int i = 0; i < C::WC && n + i < p.N; ++i) {
+              d[i] = w[i];
+              if (db) db[i] = __float2bfloat16_rn(w[i]);
+            }
+          }
+          // Shared-memory writes (and reads of the slot) before the async-proxy copies below.
           fence_proxy_async_shared();
-          mbar_arrive_after(&wempty_bar[slot], dep);
+          __syncwarp();
+          if (lane == 0) {
+            if (box_rows && n < p.N) {
+              tma_store_2d_hint(&tmD, wslots + slot * C::W_SLOT_BYTES + quarter * 32 * 64, static_cast<int>(n), yD,
+                                pol);
+              if (p.Db.ptr) tma_store_2d(&tmDb, my_stg + (wc & 1) * C::STG_BYTES, static_cast<int>(n), yDb);
+            }
+            bulk_commit_group();
+            // The stores of the previous chunk have read their slot and staging buffer:
+            // hand that slot back to the loader.
+            bulk_wait_group_read<1>();
+            if (wc > 0) mbar_arrive(&wempty_bar[(wc - 1) % C::W_SLOTS]);
+          }
+          __syncwarp();
         }
-        tmem_ld_32x32b_x32(tbase + c * 32, r);
-        if constexpr (EPI == EPI_GATE) tmem_ld_32x32b_x32(tbase + BN + c * 32, u);
-        tmem_wait_ld();
-        const int64_t n = nt * BN + c * 32;
-        if (m < p.M && n < p.N) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u, s);
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32], u[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          if constexpr (EPI == EPI_GATE) tmem_ld_32x32b_x32(tbase + BN + c * 32, u);
+          tmem_wait_ld();
+          const int64_t n = nt * BN + c * 32;
+          if (n >= p.N) continue;
+          if constexpr (C::RED) {
+            if (box_rows) {
+              // 128-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ (t % 8)
+              float4* srow = reinterpret_cast<float4*>(my_stg + (sc & 1) * C::STG_BYTES + lane * 128);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                srow[j ^ (lane & 7)] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                tma_reduce_add_2d(&tmD, my_stg + (sc & 1) * C::STG_BYTES, static_cast<int>(n),
+                                  static_cast<int>(row_of(p.D, b1, b2) + mt * BM + quarter * 32));
+                bulk_commit_group();
+                bulk_wait_group_read<1>();  // the other staging buffer is free again
+              }
+              __syncwarp();
+              ++sc;
+              continue;
+            }
+          }
+          if (m < p.M) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
+        }
       }
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
       if (!ok) break;
       ++ls;
     }
+    // Every bulk store / reduction of this warp has completed before the CTA exits.
+    if constexpr (C::W_LOAD || C::RED) {
+      if (lane == 0) bulk_wait_group<0>();
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------- fast-weight loader (update)
     if constexpr (C::W_LOAD) {
       if (lane == 0) {
+        const uint64_t pol = l2_policy_evict_first();
         uint32_t wc = 0;
         bool ok = true;
         while (ok && iter.next(seg)) {
@@ -448,15 +531,15 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
           kp.s.tile_coords(seg.tile, bi, mt, nt);
           const int b1 = bi % p.nb1, b2 = bi / p.nb1;
           const int64_t row0 = row_of(p.src, b1, b2) + mt * BM;
-          for (int c = 0; c < BN / 32; ++c, ++wc) {
+          for (int c = 0; c < BN / C::WC; ++c, ++wc) {
             const uint32_t slot = wc % C::W_SLOTS, ph = (wc / C::W_SLOTS) & 1;
             if (!mbar_wait_bounded(&wempty_bar[slot], ph ^ 1, abort_flag, 5, &g_device_error)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(&wfull_bar[slot], C::W_SLOT_BYTES);
-            tma_load_2d(wslots + slot * C::W_SLOT_BYTES, &tmS, &wfull_bar[slot],
-                        static_cast<int>(nt * BN + c * 32), static_cast<int>(row0));
+            tma_load_2d_hint(wslots + slot * C::W_SLOT_BYTES, &tmS, &wfull_bar[slot],
+                             static_cast<int>(nt * BN + c * C::WC), static_cast<int>(row0), pol);
           }
         }
         for (uint32_t slot = 0; slot < C::W_SLOTS && slot < wc; ++slot) {
@@ -498,20 +581,31 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D tensor map with 128-byte swizzle; the box is 128 bytes wide.
+// 2-D tensor map of a row-major matrix (rows x cols, row stride ld elements);
+// the box is box_cols x box_rows and its rows are box_cols * element size
+// bytes wide, swizzled with the matching pattern (32, 64 or 128 bytes).
 static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32,
-                     int box_rows) {
+                     int box_cols, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
-  if (!enc || rows <= 0 || cols <= 0) return false;
+  if (!enc || !ptr || rows <= 0 || cols <= 0) return false;
   const int esz = fp32 ? 4 : 2;
+  const int row_bytes = box_cols * esz;
+  CUtensorMapSwizzle sw;
+  if (row_bytes == 128)
+    sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  else if (row_bytes == 64)
+    sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  else if (row_bytes == 32)
+    sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  else
+    return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
@@ -531,19 +625,22 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
     }
   }
 
-  CUtensorMap mA, mB, mB2, mS;
-  if (!make_map(&mA, p.A.ptr, p.A.rows, p.A.cols, p.A.ld, false, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mB, p.B.ptr, p.B.rows, p.B.cols, p.B.ld, false, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
-  if (NB == 2) {
-    if (!make_map(&mB2, p.B2.ptr, p.B2.rows, p.B2.cols, p.B2.ld, false, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
-  } else {
-    mB2 = mB;
-  }
+  // Operand boxes: 64 K-elements (128 bytes) wide; K-major boxes span the
+  // tile's rows, MN-major boxes are 64 K-rows of 64 columns.
+  CUtensorMap mA, mB, mB2, mS, mD, mDb;
+  if (!make_map(&mA, p.A.ptr, p.A.rows, p.A.cols, p.A.ld, false, 64, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mB, p.B.ptr, p.B.rows, p.B.cols, p.B.ld, false, 64, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
+  mB2 = mB;
+  if (NB == 2 && !make_map(&mB2, p.B2.ptr, p.B2.rows, p.B2.cols, p.B2.ld, false, 64, B_MN ? 64 : BN))
+    return cudaErrorInvalidValue;
+  mS = mD = mDb = mA;
   if (C::W_LOAD) {
-    if (!make_map(&mS, p.src.ptr, p.src.rows, p.N, p.src.ld, true, BM)) return cudaErrorInvalidValue;
-  } else {
-    mS = mA;
+    if (!make_map(&mS, p.src.ptr, p.src.rows, p.N, p.src.ld, true, C::WC, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, C::WC, 32)) return cudaErrorInvalidValue;
+    if (p.Db.ptr && !make_map(&mDb, p.Db.ptr, p.Db.rows, p.N, p.Db.ld, false, C::WC, 32))
+      return cudaErrorInvalidValue;
   }
+  if (C::RED && !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, 32, 32)) return cudaErrorInvalidValue;
 
   KParams kp;
   kp.p = p;
@@ -560,7 +657,7 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   int64_t grid = s.split ? std::min<int64_t>(sms, s.total_iters) : std::min<int64_t>(sms, s.total_tiles);
   if (grid <= 0) return cudaSuccess;
   LaunchMark mark(p.kind, stream);
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mA, mB, mB2, mS, kp);
+  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mA, mB, mB2, mS, mD, mDb, kp);
   return cudaGetLastError();
 }
 
