@@ -133,38 +133,54 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const ResidualArgs a
   }
 }
 
-// Vectorised bf16 variant (d % 8 == 0): 8 columns per thread.
-__global__ void __launch_bounds__(kThreads) residual_kernel_bf16x8(const ResidualArgs a) {
-  const int64_t dv = a.d / 8;
-  const int64_t per_entry = a.B * dv;
-  const int64_t total = per_entry * a.nb1 * a.nb2;
-  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t e = idx / per_entry, rem = idx % per_entry;
-    const int64_t i = rem / dv, c = (rem % dv) * 8;
+// Vectorised bf16 variant (d % 8 == 0).  Thread (x, y): 8 columns c = 8*(128*y + x % 128)
+// of kResRows consecutive rows starting at kResRows*(x / 128); all loads are
+// issued before any store, so a thread keeps kResRows round trips in flight.
+constexpr int kResRows = 4;
+__global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs a) {
+  const int64_t rows = a.B * a.nb1 * a.nb2;
+  const int64_t c = (static_cast<int64_t>(blockIdx.y) * 128 + threadIdx.x) * 8;
+  if (c >= a.d) return;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kResRows;
+  float4 x[kResRows][2];
+  uint4 vr[kResRows];
+  int64_t orow[kResRows];
+#pragma unroll
+  for (int j = 0; j < kResRows; ++j) {
+    const int64_t r = r0 + j;
+    if (r >= rows) break;
+    const int64_t e = r / a.B, i = r % a.B;
     const int b1 = static_cast<int>(e % a.nb1), b2 = static_cast<int>(e / a.nb1);
-    const int64_t orow = a.o_y0 + b1 * a.o_ys1 + b2 * a.o_ys2 + i;
-    float4* accp = reinterpret_cast<float4*>(a.acc + (e * a.B + i) * a.d + c);
-    const float4 x0 = accp[0], x1 = accp[1];
+    orow[j] = a.o_y0 + b1 * a.o_ys1 + b2 * a.o_ys2 + i;
+    const float4* accp = reinterpret_cast<const float4*>(a.acc + r * a.d + c);
+    x[j][0] = accp[0];
+    x[j][1] = accp[1];
+    if (a.R) vr[j] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.V) + orow[j] * a.d + c);
+  }
+#pragma unroll
+  for (int j = 0; j < kResRows; ++j) {
+    const int64_t r = r0 + j;
+    if (r >= rows) break;
+    float4* accp = reinterpret_cast<float4*>(a.acc + r * a.d + c);
     accp[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     accp[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 x0 = x[j][0], x1 = x[j][1];
     uint4 o;
     o.x = pack_bf16x2(x0.x, x0.y);
     o.y = pack_bf16x2(x0.z, x0.w);
     o.z = pack_bf16x2(x1.x, x1.y);
     o.w = pack_bf16x2(x1.z, x1.w);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + orow * a.d + c) = o;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + orow[j] * a.d + c) = o;
     if (a.R) {
-      const uint4 vr = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.V) + orow * a.d + c);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr[j]);
       const float2 v0 = __bfloat1622float2(h[0]), v1 = __bfloat1622float2(h[1]), v2 = __bfloat1622float2(h[2]),
                    v3 = __bfloat1622float2(h[3]);
-      uint4 r;
-      r.x = pack_bf16x2(x0.x - v0.x, x0.y - v0.y);
-      r.y = pack_bf16x2(x0.z - v1.x, x0.w - v1.y);
-      r.z = pack_bf16x2(x1.x - v2.x, x1.y - v2.y);
-      r.w = pack_bf16x2(x1.z - v3.x, x1.w - v3.y);
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.R) + (e * a.B + i) * a.d + c) = r;
+      uint4 rr;
+      rr.x = pack_bf16x2(x0.x - v0.x, x0.y - v0.y);
+      rr.y = pack_bf16x2(x0.z - v1.x, x0.w - v1.y);
+      rr.z = pack_bf16x2(x1.x - v2.x, x1.y - v2.y);
+      rr.w = pack_bf16x2(x1.z - v3.x, x1.w - v3.y);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.R) + r * a.d + c) = rr;
     }
   }
 }
@@ -240,8 +256,12 @@ cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t strea
   const int64_t total = a.B * a.d * a.nb1 * a.nb2;
   if (total <= 0) return cudaSuccess;
   LaunchMark mark(K_RESIDUAL, stream);
-  if (bf16 && a.d % 8 == 0)
-    residual_kernel_bf16x8<<<grid_for(total / 8), kThreads, 0, stream>>>(a);
+  if (bf16 && a.d % 8 == 0) {
+    const int64_t rows = a.B * a.nb1 * a.nb2;
+    const dim3 grid(static_cast<unsigned>((rows + kResRows - 1) / kResRows),
+                    static_cast<unsigned>((a.d / 8 + 127) / 128));
+    residual_kernel_bf16x8<<<grid, 128, 0, stream>>>(a);
+  }
   else if (bf16)
     residual_kernel<__nv_bfloat16><<<grid_for(total), kThreads, 0, stream>>>(a);
   else

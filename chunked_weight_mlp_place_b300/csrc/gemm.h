@@ -27,7 +27,6 @@ struct Operand {
   int64_t rows = 0, cols = 0, ld = 0;  // matrix extent and row stride (elements)
   int mn_major = 0;                    // 1: K runs along rows
   int64_t y0 = 0, ys1 = 0, ys2 = 0;    // per-batch row offsets
-  int evict_first = 0;                 // tensor-core path: read with the L2 evict-first policy
 };
 
 struct OutRef {
@@ -35,7 +34,6 @@ struct OutRef {
   int64_t ld = 0;
   int64_t y0 = 0, ys1 = 0, ys2 = 0;  // row = y0 + b1*ys1 + b2*ys2 + m, column n
   int64_t rows = 0;                  // rows of the whole matrix (needed where TMA reads or writes it)
-  int evict_first = 0;               // tensor-core path: TMA traffic with the L2 evict-first policy
 };
 
 struct GemmProblem {

@@ -6,6 +6,11 @@
 //   apply  O_k = Z_k W_k  (split over K)    A = Z_k (K-major)  B = W_k bf16    (MN-major)
 //   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k         (MN-major)
 //
+// Problems with more than one 128-row tile run on CTA pairs (clusters of 2,
+// tcgen05 cta_group::2): one 256 x N MMA per pair, each CTA holding 128 rows
+// of A and half of B's columns in its shared memory, so each SM streams half
+// the B operand it would alone.
+//
 // Each CTA (one per SM) runs these warps:
 //   warp 0      TMA producer: 128x64 A tiles and 64-wide B tiles into a ring of
 //               shared-memory stages (128-byte swizzle), completion on mbarriers;
@@ -55,17 +60,17 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns between the two accumulator buffers
-constexpr int kEpiThreads = 128;
 
-template <int BN, int NB, int EPI>
+template <int BN, int NB, int EPI, bool PAIR>
 struct Cfg {
   static constexpr bool W_LOAD = (EPI == EPI_AXPY);
   static constexpr bool RED = (EPI == EPI_ACCUM);
   static constexpr int THREADS = W_LOAD ? 224 : 192;
+  static constexpr int N_MMA = BN * NB;          // the B operands sit side by side: one MMA covers them
+  static constexpr int M_MMA = PAIR ? 2 * BM : BM;
+  static constexpr int B_COLS = PAIR ? N_MMA / 2 : N_MMA;  // B columns held by one CTA per stage
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;  // per B operand
-  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
-  static constexpr int N_MMA = BN * NB;        // the B operands sit side by side: one MMA covers them
+  static constexpr int STAGE_BYTES = A_BYTES + B_COLS * BK * 2;
   // update: the fp32 W tile streams through slots of 128 rows x 16 columns (64-byte rows)
   static constexpr int WC = 16;
   static constexpr int W_SLOT_BYTES = BM * WC * 4;
@@ -74,14 +79,17 @@ struct Cfg {
   //   apply: 32 rows x 32 fp32 (128-byte rows); update: 32 rows x 16 bf16 (32-byte rows)
   static constexpr int STG_BYTES = RED ? 32 * 32 * 4 : (W_LOAD ? 32 * WC * 2 : 0);
   static constexpr int STG_TOTAL = 4 * 2 * STG_BYTES;
-  static constexpr int STAGES = W_LOAD ? 3 : 4;
+  static constexpr int STAGES = PAIR ? (W_LOAD ? 4 : 6) : (W_LOAD ? 3 : 4);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES =
       1024 + STAGES * STAGE_BYTES + W_SLOTS * W_SLOT_BYTES + STG_TOTAL + BAR_BYTES;
   static_assert(N_MMA <= kAccStride && N_MMA % 16 == 0, "accumulator width");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(B_COLS % 64 == 0, "B columns per CTA: whole 64-column swizzle atoms");
+  static_assert(!PAIR || NB == 1 || BN == B_COLS, "pair: a second B operand is the peer's half");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert(W_SLOT_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0, "1024-byte aligned swizzle atoms");
+  static_assert(STAGE_BYTES % 1024 == 0 && W_SLOT_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0,
+                "1024-byte aligned swizzle atoms");
 };
 
 struct Seg {
@@ -90,11 +98,15 @@ struct Seg {
 };
 
 // Work decomposition shared by all roles (each walks it independently).
+// With CTA pairs, a tile is a pair tile (2*BM rows): n_mt counts pair rows and
+// the CTA of rank r in the pair owns rows 2*mt + r; the two CTAs of a cluster
+// walk the same tiles and k-blocks.
 struct Sched {
   int64_t n_mt, n_nt, tiles_per_batch, total_tiles;
   int kb_total;
   int group_m;
   int split;
+  int pair;
   int64_t total_iters;
 
   __device__ void tile_coords(int64_t t, int& bi, int64_t& mt, int64_t& nt) const {
@@ -108,7 +120,9 @@ struct Sched {
     mt = first_m + q % gm;
     nt = q / gm;
   }
-  // Split mode: CTA c owns iterations [floor(c*T/G), floor((c+1)*T/G)).
+  // Split mode: worker c (a CTA, or a CTA pair) owns iterations [floor(c*T/G), floor((c+1)*T/G)).
+  __device__ int64_t worker() const { return pair ? (blockIdx.x >> 1) : blockIdx.x; }
+  __device__ int64_t workers() const { return pair ? (gridDim.x >> 1) : gridDim.x; }
 };
 
 struct SegIter {
@@ -117,11 +131,11 @@ struct SegIter {
   __device__ void init(const Sched* sc) {
     s = sc;
     if (s->split) {
-      const int64_t G = gridDim.x;
-      it = s->total_iters * blockIdx.x / G;
-      it_end = s->total_iters * (blockIdx.x + 1) / G;
+      const int64_t G = s->workers(), c = s->worker();
+      it = s->total_iters * c / G;
+      it_end = s->total_iters * (c + 1) / G;
     } else {
-      t = blockIdx.x;
+      t = s->worker();
     }
   }
   __device__ bool next(Seg& g) {
@@ -138,7 +152,7 @@ struct SegIter {
     g.tile = t;
     g.kb0 = 0;
     g.kb1 = s->kb_total;
-    t += gridDim.x;
+    t += s->workers();
     return true;
   }
 };
@@ -155,25 +169,24 @@ __device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) {
   return o.y0 + b1 * o.ys1 + b2 * o.ys2;
 }
 
-// Issue the TMA copies of one operand tile (extent EXT along M or N, BK along K).
-template <bool MN, int EXT>
-__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int64_t row0,
-                                             int64_t i0, int64_t k0, int evict_first, uint64_t pol) {
+// Issue the TMA copies of one operand tile (extent EXT along M or N, BK along
+// K).  With CTA pairs the completion is counted on the even CTA's barrier
+// (cluster address bar_cl).
+template <bool MN, int EXT, bool PAIR>
+__device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, uint32_t bar_cl,
+                                             int64_t row0, int64_t i0, int64_t k0) {
+  auto copy = [&](uint8_t* d, int x, int y) {
+    if constexpr (PAIR)
+      tma_load_2d_pair(d, map, bar_cl, x, y);
+    else
+      tma_load_2d(d, map, bar, x, y);
+  };
   if constexpr (MN) {
 #pragma unroll
-    for (int j = 0; j < EXT / 64; ++j) {
-      const int x = static_cast<int>(i0 + 64 * j), y = static_cast<int>(row0 + k0);
-      if (evict_first)
-        tma_load_2d_hint(dst + j * (64 * BK * 2), map, bar, x, y, pol);
-      else
-        tma_load_2d(dst + j * (64 * BK * 2), map, bar, x, y);
-    }
+    for (int j = 0; j < EXT / 64; ++j)
+      copy(dst + j * (64 * BK * 2), static_cast<int>(i0 + 64 * j), static_cast<int>(row0 + k0));
   } else {
-    const int x = static_cast<int>(k0), y = static_cast<int>(row0 + i0);
-    if (evict_first)
-      tma_load_2d_hint(dst, map, bar, x, y, pol);
-    else
-      tma_load_2d(dst, map, bar, x, y);
+    copy(dst, static_cast<int>(k0), static_cast<int>(row0 + i0));
   }
 }
 
@@ -247,13 +260,14 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
   }
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
-__global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR>
+__global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmS,
                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmDb,
                    const __grid_constant__ KParams kp) {
-  using C = Cfg<BN, NB, EPI>;
+  using C = Cfg<BN, NB, EPI, PAIR>;
+  static_assert(!PAIR || B_MN, "pairs split an MN-major B operand by columns");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -273,6 +287,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
 
   const GemmProblem& p = kp.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // CTA pairs: rank 0 issues the pair's MMAs; both CTAs load their own A rows
+  // and their half of B, and run their own epilogue on their 128 TMEM lanes.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const bool mma_cta = (rank == 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -282,7 +300,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull_bar[i], 1);
-        mbar_init(&tempty_bar[i], kEpiThreads);
+        mbar_init(&tempty_bar[i], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
       }
       mbar_init(drain_bar, 1);
       for (int i = 0; i < C::W_SLOTS; ++i) {
@@ -301,11 +319,18 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       if constexpr (C::W_LOAD || C::RED) tma_prefetch_desc(&tmD);
     }
     __syncwarp();
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // The peer signals this CTA's barriers: both CTAs' barriers exist before anyone proceeds.
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -316,7 +341,6 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
       uint32_t kc = 0;
       uint32_t issued_mask = 0;
       bool ok = true;
@@ -324,6 +348,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
         int bi;
         int64_t mt, nt;
         kp.s.tile_coords(seg.tile, bi, mt, nt);
+        if constexpr (PAIR) mt = 2 * mt + rank;
         const int b1 = bi % p.nb1, b2 = bi / p.nb1;
         const int64_t ra = row_of(p.A, b1, b2), rb = row_of(p.B, b1, b2), rb2 = row_of(p.B2, b1, b2);
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++kc) {
@@ -334,29 +359,46 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
           }
           uint8_t* sa = stages + st * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
+          // with pairs, the MMA CTA's full barrier counts both CTAs' bytes
+          const uint32_t bar_cl = PAIR ? mapa_shared(smem_u32(&full_bar[st]), 0) : 0u;
+          if (mma_cta) mbar_arrive_expect_tx(&full_bar[st], (PAIR ? 2 : 1) * C::STAGE_BYTES);
           issued_mask |= 1u << st;
           const int64_t k0 = static_cast<int64_t>(kb) * BK;
-          load_operand<A_MN, BM>(sa, &tmA, &full_bar[st], ra, mt * BM, k0, p.A.evict_first, pol);
-          load_operand<B_MN, BN>(sb, &tmB, &full_bar[st], rb, nt * BN, k0, p.B.evict_first, pol);
-          if constexpr (NB == 2)
-            load_operand<B_MN, BN>(sb + C::B_BYTES, &tmB2, &full_bar[st], rb2, nt * BN, k0, p.B2.evict_first, pol);
+          load_operand<A_MN, BM, PAIR>(sa, &tmA, &full_bar[st], bar_cl, ra, mt * BM, k0);
+          if constexpr (PAIR && NB == 2) {
+            // the even CTA holds the first B operand, its peer the second
+            if (rank == 0)
+              load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN, k0);
+            else
+              load_operand<B_MN, BN, PAIR>(sb, &tmB2, &full_bar[st], bar_cl, rb2, nt * BN, k0);
+          } else if constexpr (PAIR) {
+            load_operand<B_MN, C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN + rank * C::B_COLS, k0);
+          } else {
+            load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], 0u, rb, nt * BN, k0);
+            if constexpr (NB == 2)
+              load_operand<B_MN, BN, PAIR>(sb + BN * BK * 2, &tmB2, &full_bar[st], 0u, rb2, nt * BN, k0);
+          }
         }
       }
       // Teardown: every copy issued here must have landed before the CTA's
-      // shared memory is released (matters only after an abort).
+      // shared memory is released (matters only after an abort).  With pairs
+      // the copies complete on the MMA CTA's barrier; this CTA learns that its
+      // stages were consumed from its empty barriers.
       for (uint32_t st = 0; st < C::STAGES; ++st) {
         if (!(issued_mask & (1u << st))) continue;
         const uint32_t f = (kc - 1 - st) / C::STAGES;  // last fill of stage st
-        mbar_wait_bounded(&full_bar[st], f & 1, abort_flag, 4, &g_device_error);
+        if (PAIR && !mma_cta)
+          mbar_wait_bounded(&empty_bar[st], f & 1, abort_flag, 4, &g_device_error);
+        else
+          mbar_wait_bounded(&full_bar[st], f & 1, abort_flag, 4, &g_device_error);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     // The whole role runs on one thread: tcgen05.mma and tcgen05.commit are
     // issued by a single thread, and a lone waiter cannot diverge from itself.
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(BM, C::N_MMA, A_MN, B_MN);
+    if (lane == 0 && mma_cta) {
+      constexpr uint32_t idesc = make_idesc_bf16(C::M_MMA, C::N_MMA, A_MN, B_MN);
       uint32_t kc = 0, ls = 0;
       bool ok = true;
       while (ok && iter.next(seg)) {
@@ -377,16 +419,28 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
           const int ksteps = static_cast<int>(min(static_cast<int64_t>(BK / 16), (krem + 15) / 16));
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t accum = (kb > seg.kb0 || ks > 0) ? 1u : 0u;
-            umma_bf16(d_tmem, operand_desc<A_MN>(sa, ks), operand_desc<B_MN>(sb, ks), idesc, accum);
+            if constexpr (PAIR)
+              umma_bf16_pair(d_tmem, operand_desc<A_MN>(sa, ks), operand_desc<B_MN>(sb, ks), idesc, accum);
+            else
+              umma_bf16(d_tmem, operand_desc<A_MN>(sa, ks), operand_desc<B_MN>(sb, ks), idesc, accum);
           }
-          umma_commit(&empty_bar[st]);
+          if constexpr (PAIR)
+            umma_commit_pair_both(&empty_bar[st]);
+          else
+            umma_commit(&empty_bar[st]);
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair_both(&tfull_bar[acc]);
+        else
+          umma_commit(&tfull_bar[acc]);
         ++ls;
       }
       // Teardown: wait for every MMA issued here before TMEM is freed.
-      umma_commit(drain_bar);
+      if constexpr (PAIR)
+        umma_commit_pair_both(drain_bar);
+      else
+        umma_commit(drain_bar);
       mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
     }
   } else if (warp <= 5) {
@@ -406,6 +460,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
       int bi;
       int64_t mt, nt;
       kp.s.tile_coords(seg.tile, bi, mt, nt);
+      if constexpr (PAIR) mt = 2 * mt + rank;
       const int b1 = bi % p.nb1, b2 = bi / p.nb1;
       const int64_t m = mt * BM + trow;
       // this warp's 32 rows can go through one TMA box only if all of them are rows of the problem
@@ -508,8 +563,15 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
           if (m < p.M) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
         }
       }
+      // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
       tc_fence_before();
-      mbar_arrive(&tempty_bar[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        else
+          mbar_arrive(&tempty_bar[acc]);
+      }
       if (!ok) break;
       ++ls;
     }
@@ -529,6 +591,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
           int bi;
           int64_t mt, nt;
           kp.s.tile_coords(seg.tile, bi, mt, nt);
+          if constexpr (PAIR) mt = 2 * mt + rank;
           const int b1 = bi % p.nb1, b2 = bi / p.nb1;
           const int64_t row0 = row_of(p.src, b1, b2) + mt * BM;
           for (int c = 0; c < BN / C::WC; ++c, ++wc) {
@@ -552,13 +615,21 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI>::THREADS, 1)
 
   // Roles that ran on one lane re-converge their warp first: the CTA barrier
   // below is a warp-aligned instruction, and TMEM may only be freed once every
-  // warp (the epilogue's TMEM loads included) has reached it.
+  // warp (the epilogue's TMEM loads included) has reached it.  With pairs, the
+  // barrier spans the cluster: the peer's last arrivals on this CTA's barriers
+  // and the even CTA's last MMAs into the peer's TMEM are done before either frees.
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -608,19 +679,40 @@ static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR>
 static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
-  using C = Cfg<BN, NB, EPI>;
-  auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16>;
+  using C = Cfg<BN, NB, EPI, PAIR>;
+  auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16, PAIR>;
   static std::mutex mu;
   static uint64_t attr_done = 0;  // bit per device: shared-memory size attribute set
+  static int max_workers[64] = {0};  // co-resident CTAs (or CTA pairs) per device
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   {
-    const int dev = current_device();
     std::lock_guard<std::mutex> g(mu);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!(attr_done & (1ull << dev))) {
-      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
       if (e != cudaSuccess) return e;
+      int n = device_sm_count();
+      if (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (n / 2));
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        n = clusters;
+      }
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_workers[dev] = n;
       attr_done |= 1ull << dev;
     }
   }
@@ -645,7 +737,9 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   KParams kp;
   kp.p = p;
   Sched& s = kp.s;
-  s.n_mt = (p.M + BM - 1) / BM;
+  const int64_t m_tiles = (p.M + BM - 1) / BM;
+  s.pair = PAIR ? 1 : 0;
+  s.n_mt = PAIR ? (m_tiles + 1) / 2 : m_tiles;
   s.n_nt = (p.N + BN - 1) / BN;
   s.tiles_per_batch = s.n_mt * s.n_nt;
   s.total_tiles = s.tiles_per_batch * p.nb1 * p.nb2;
@@ -653,12 +747,35 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   s.group_m = static_cast<int>(s.n_mt < 16 ? s.n_mt : 16);
   s.split = p.split_k ? 1 : 0;
   s.total_iters = s.total_tiles * s.kb_total;
-  const int sms = device_sm_count();
-  int64_t grid = s.split ? std::min<int64_t>(sms, s.total_iters) : std::min<int64_t>(sms, s.total_tiles);
-  if (grid <= 0) return cudaSuccess;
+  const int64_t workers =
+      std::min<int64_t>(max_workers[dev], s.split ? s.total_iters : s.total_tiles);
+  if (workers <= 0) return cudaSuccess;
   LaunchMark mark(p.kind, stream);
-  kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mA, mB, mB2, mS, mD, mDb, kp);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * workers));
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mA, mB, mB2, mS, mD, mDb, kp);
+  } else {
+    kern<<<static_cast<unsigned>(workers), C::THREADS, C::SMEM_BYTES, stream>>>(mA, mB, mB2, mS, mD, mDb, kp);
+    return cudaGetLastError();
+  }
+}
+
+// Pairs of CTAs once the problem has at least two 128-row tiles.
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
+static cudaError_t run_any(const GemmProblem& p, cudaStream_t stream) {
+  if (p.M > BM) return run<BN, NB, A_MN, B_MN, EPI, OUT_BF16, true>(p, stream);
+  return run<BN, NB, A_MN, B_MN, EPI, OUT_BF16, false>(p, stream);
 }
 
 }  // namespace tc
@@ -684,20 +801,20 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
   switch (p.epi) {
     case EPI_GATE:
       if (!a_mn && b_mn)
-        return p.out_bf16 ? run<128, 2, false, true, EPI_GATE, true>(p, stream)
-                          : run<128, 2, false, true, EPI_GATE, false>(p, stream);
+        return p.out_bf16 ? run_any<128, 2, false, true, EPI_GATE, true>(p, stream)
+                          : run_any<128, 2, false, true, EPI_GATE, false>(p, stream);
       break;
     case EPI_STORE:
       if (!a_mn && b_mn)
-        return p.out_bf16 ? run<256, 1, false, true, EPI_STORE, true>(p, stream)
-                          : run<256, 1, false, true, EPI_STORE, false>(p, stream);
-      if (a_mn && b_mn && !p.out_bf16) return run<256, 1, true, true, EPI_STORE, false>(p, stream);
+        return p.out_bf16 ? run_any<256, 1, false, true, EPI_STORE, true>(p, stream)
+                          : run_any<256, 1, false, true, EPI_STORE, false>(p, stream);
+      if (a_mn && b_mn && !p.out_bf16) return run_any<256, 1, true, true, EPI_STORE, false>(p, stream);
       break;
     case EPI_ACCUM:
-      if (!a_mn && b_mn) return run<256, 1, false, true, EPI_ACCUM, false>(p, stream);
+      if (!a_mn && b_mn) return run_any<256, 1, false, true, EPI_ACCUM, false>(p, stream);
       break;
     case EPI_AXPY:
-      if (a_mn && b_mn) return run<256, 1, true, true, EPI_AXPY, false>(p, stream);
+      if (a_mn && b_mn) return run_any<256, 1, true, true, EPI_AXPY, false>(p, stream);
       break;
   }
   return cudaErrorNotSupported;
