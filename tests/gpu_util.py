@@ -19,8 +19,8 @@ def up(a, dtype, dev="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(dtype).contiguous()
 
 
-def down(t):
-    return t.detach().to(torch.float64).cpu().numpy()
+def down(t, dtype=torch.float64):
+    return t.detach().to(dtype).cpu().numpy()
 
 
 def rel(a, b):
@@ -28,8 +28,9 @@ def rel(a, b):
     return float(np.linalg.norm(np.asarray(a, np.float64) - b) / (den if den > 0 else 1.0))
 
 
-def run_layer(w, a, rule, L=None, W0=None, stream=None):
-    """Run ipttt_layer_forward on arrays ``a`` (from inputs.generate) for workload w."""
+def run_layer(w, a, rule, L=None, W0=None, stream=None, out_dtype=torch.float64):
+    """Run ipttt_layer_forward on arrays ``a`` (from inputs.generate) for workload w;
+    O and W_final come back as numpy arrays of ``out_dtype``."""
     dt = tdtype(w)
     L = w.L if L is None else L
     X, E = up(a["X"], dt), up(a["E"], dt)
@@ -40,4 +41,4 @@ def run_layer(w, a, rule, L=None, W0=None, stream=None):
     ip.layer_forward(X, E, up(a["W_g"], dt), up(a["W_u"], dt), W0t, up(a["conv_w"], torch.float32),
                      up(a["P"], dt), L, w.B, w.eta, rule, O, Wf, stream=stream)
     assert ip.sync_status() == 0
-    return down(O), down(Wf)
+    return down(O, out_dtype), down(Wf, out_dtype)
