@@ -138,6 +138,8 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const ResidualArgs a
 // issued before any store, so a thread keeps kResRows round trips in flight.
 constexpr int kResRows = 4;
 __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t rows = a.B * a.nb1 * a.nb2;
   const int64_t c = (static_cast<int64_t>(blockIdx.y) * 128 + threadIdx.x) * 8;
   if (c >= a.d) return;
@@ -260,7 +262,7 @@ cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t strea
     const int64_t rows = a.B * a.nb1 * a.nb2;
     const dim3 grid(static_cast<unsigned>((rows + kResRows - 1) / kResRows),
                     static_cast<unsigned>((a.d / 8 + 127) / 128));
-    residual_kernel_bf16x8<<<grid, 128, 0, stream>>>(a);
+    return launch_overlapped(residual_kernel_bf16x8, grid, dim3(128), 0, stream, 1, a);
   }
   else if (bf16)
     residual_kernel<__nv_bfloat16><<<grid_for(total), kThreads, 0, stream>>>(a);

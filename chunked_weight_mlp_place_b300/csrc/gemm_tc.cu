@@ -75,10 +75,11 @@ struct Cfg {
   static constexpr int WC = 16;
   static constexpr int W_SLOT_BYTES = BM * WC * 4;
   static constexpr int W_SLOTS = W_LOAD ? 8 : 0;
-  // per epilogue warp, two staging buffers for TMA stores / reductions:
-  //   apply: 32 rows x 32 fp32 (128-byte rows); update: 32 rows x 16 bf16 (32-byte rows)
+  // per epilogue warp, staging buffers for TMA stores / reductions:
+  //   apply: 2 of 32 rows x 32 fp32 (128-byte rows); update: 3 of 32 rows x 16 bf16 (32-byte rows)
   static constexpr int STG_BYTES = RED ? 32 * 32 * 4 : (W_LOAD ? 32 * WC * 2 : 0);
-  static constexpr int STG_TOTAL = 4 * 2 * STG_BYTES;
+  static constexpr int STG_BUFS = W_LOAD ? 3 : 2;
+  static constexpr int STG_TOTAL = 4 * STG_BUFS * STG_BYTES;
   static constexpr int STAGES = PAIR ? (W_LOAD ? 4 : 6) : (W_LOAD ? 3 : 4);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES =
@@ -333,6 +334,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touched only this CTA's shared memory and TMEM: it overlaps
+  // the previous kernel's tail.  Global memory from here on.
+  pdl_wait();
+  pdl_trigger();
 
   SegIter iter;
   iter.init(&kp.s);
@@ -447,7 +452,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp % 4;          // TMEM lanes 32*quarter .. +31 belong to this warp
     const int trow = quarter * 32 + lane;  // row of the tile this thread finishes
-    uint8_t* my_stg = stg + quarter * 2 * C::STG_BYTES;
+    uint8_t* my_stg = stg + quarter * C::STG_BUFS * C::STG_BYTES;
     uint64_t pol = 0;
     if constexpr (C::W_LOAD) pol = l2_policy_evict_first();
     uint32_t ls = 0, wc = 0, sc = 0;
@@ -471,19 +476,16 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         // ---- update: W = src + alpha * acc in the slot, TMA stores of W and its bf16 copy
         const int yD = static_cast<int>(row_of(p.D, b1, b2) + mt * BM + quarter * 32);
         const int yDb = static_cast<int>(row_of(p.Db, b1, b2) + mt * BM + quarter * 32);
-#pragma unroll 1
-        for (int c = 0; c < BN / C::WC; ++c, ++wc) {
+        // One chunk of WC columns: W(slot) + alpha * acc(regs) -> slot (fp32) and staging (bf16),
+        // then this warp's TMA stores.  Stores stay in flight for two chunks: the slot
+        // and staging buffer of chunk wc-2 are released once they have been read.
+        auto chunk = [&](int c, const uint32_t(&r)[C::WC]) -> bool {
           const uint32_t slot = wc % C::W_SLOTS, wph = (wc / C::W_SLOTS) & 1;
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error))) {
-            ok = false;
-            break;
-          }
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(tbase + c * C::WC, r);
-          tmem_wait_ld();
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error)))
+            return false;
           // 64-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 1) & 3)
           float4* srow = reinterpret_cast<float4*>(wslots + slot * C::W_SLOT_BYTES + trow * 64);
+          uint8_t* sbuf = my_stg + (wc % C::STG_BUFS) * C::STG_BYTES;
           float w[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -500,7 +502,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               srow[j ^ ((trow >> 1) & 3)] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
             if (p.Db.ptr) {
               // 32-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 2) & 1)
-              uint4* brow = reinterpret_cast<uint4*>(my_stg + (wc & 1) * C::STG_BYTES + lane * 32);
+              uint4* brow = reinterpret_cast<uint4*>(sbuf + lane * 32);
               brow[0 ^ ((lane >> 2) & 1)] = pack8_bf16(w);
               brow[1 ^ ((lane >> 2) & 1)] = pack8_bf16(w + 8);
             }
@@ -520,16 +522,32 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
             if (box_rows && n < p.N) {
               tma_store_2d_hint(&tmD, wslots + slot * C::W_SLOT_BYTES + quarter * 32 * 64, static_cast<int>(n), yD,
                                 pol);
-              if (p.Db.ptr) tma_store_2d(&tmDb, my_stg + (wc & 1) * C::STG_BYTES, static_cast<int>(n), yDb);
+              if (p.Db.ptr) tma_store_2d(&tmDb, sbuf, static_cast<int>(n), yDb);
             }
             bulk_commit_group();
-            // The stores of the previous chunk have read their slot and staging buffer:
-            // hand that slot back to the loader.
-            bulk_wait_group_read<1>();
-            if (wc > 0) mbar_arrive(&wempty_bar[(wc - 1) % C::W_SLOTS]);
+            bulk_wait_group_read<2>();
+            if (wc >= 2) mbar_arrive(&wempty_bar[(wc - 2) % C::W_SLOTS]);
           }
           __syncwarp();
+          ++wc;
+          return true;
+        };
+        // The accumulator columns of the next chunk load from TMEM while this one is finished.
+        constexpr int NCH = BN / C::WC;
+        static_assert(NCH % 2 == 0, "chunks come in pairs");
+        uint32_t ra[C::WC], rb[C::WC];
+        tmem_ld_32x32b_x16(tbase, ra);
+#pragma unroll 1
+        for (int c = 0; c < NCH && ok; c += 2) {
+          tmem_wait_ld(ra);
+          tmem_ld_32x32b_x16(tbase + (c + 1) * C::WC, rb);
+          ok = chunk(c, ra);
+          tmem_wait_ld(rb);
+          if (!ok) break;
+          if (c + 2 < NCH) tmem_ld_32x32b_x16(tbase + (c + 2) * C::WC, ra);
+          ok = chunk(c + 1, rb);
         }
+        tmem_wait_ld();
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -751,24 +769,8 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
       std::min<int64_t>(max_workers[dev], s.split ? s.total_iters : s.total_tiles);
   if (workers <= 0) return cudaSuccess;
   LaunchMark mark(p.kind, stream);
-  if constexpr (PAIR) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * workers));
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, mA, mB, mB2, mS, mD, mDb, kp);
-  } else {
-    kern<<<static_cast<unsigned>(workers), C::THREADS, C::SMEM_BYTES, stream>>>(mA, mB, mB2, mS, mD, mDb, kp);
-    return cudaGetLastError();
-  }
+  return launch_overlapped(kern, dim3(static_cast<unsigned>((PAIR ? 2 : 1) * workers)), dim3(C::THREADS),
+                           C::SMEM_BYTES, stream, PAIR ? 2 : 1, mA, mB, mB2, mS, mD, mDb, kp);
 }
 
 // Pairs of CTAs once the problem has at least two 128-row tiles.

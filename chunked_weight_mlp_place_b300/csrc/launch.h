@@ -32,6 +32,35 @@ struct LaunchMark {
   cudaStream_t stream;
   int slot;
 };
+// Launch `kern` so that it may start while the previous kernel of `stream` is
+// still finishing (programmatic dependent launch; the kernel calls pdl_wait()
+// before its first global-memory access).  cluster > 1: clusters of that many
+// CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 int current_device();     // cudaGetDevice, -1 on error
 void reset_launch_count(); // start counting the launches of a new C-ABI call
 int device_sm_count();    // SMs of the current device (cached)
