@@ -337,9 +337,12 @@ int64_t scan_groups(int64_t K) {
 }
 
 struct EngineLayout {
-  size_t o_acc = 0, r = 0, wb = 0, d = 0, db = 0, total = 0;
+  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, total = 0;
 };
 
+// Scratch of the chunk engine.  On the tensor cores the fp32 fast weight lives
+// as split hi/lo planes (bf16 hi = the apply's operand, 16-bit lo = the rest of
+// the fp32 bit pattern), so one update reads and writes 8 bytes per element.
 EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rule rule, size_t base) {
   EngineLayout e;
   Carve c;
@@ -350,12 +353,18 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
   if (rule == IPTTT_RULE_MSE) {
     e.o_acc = c.take<float>(dm->batch * B * dm->d);
     e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
-    if (bf16) e.wb = c.take<uint16_t>(dm->batch * nw);
+    if (bf16) {
+      e.hi = c.take<uint16_t>(dm->batch * nw);
+      e.lo = c.take<uint16_t>(dm->batch * nw);
+    }
   } else {
     const int64_t G = scan_groups(K);
     e.o_acc = c.take<float>(G * dm->batch * B * dm->d);
     e.d = c.take<float>(G * dm->batch * nw);
-    if (bf16) e.db = c.take<uint16_t>(G * dm->batch * nw);
+    if (bf16) {
+      e.hi = c.take<uint16_t>(G * dm->batch * nw);
+      e.lo = c.take<uint16_t>(G * dm->batch * nw);
+    }
   }
   e.total = c.off;
   return e;
@@ -370,46 +379,43 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   const int64_t w0r = dm->w0_per_seq ? dff : 0;  // same, in rows
   const int bint = static_cast<int>(batch);
   float* o_acc = reinterpret_cast<float*>(ws + lay.o_acc);
+  uint16_t* hi = bf16 ? reinterpret_cast<uint16_t*>(ws + lay.hi) : nullptr;
+  uint16_t* lo = bf16 ? reinterpret_cast<uint16_t*>(ws + lay.lo) : nullptr;
 
   if (rule == IPTTT_RULE_MSE) {
     void* R = ws + lay.r;
-    __nv_bfloat16* Wb = bf16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.wb) : nullptr;
-    if (bf16) IPTTT_CUDA(launch_to_bf16(W0, w0s, Wb, batch, nw, st));
+    if (bf16) IPTTT_CUDA(launch_split_w(W0, w0s, hi, lo, batch, nw, st));
     IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * B * d, st));
     const int64_t w0_rows = (dm->w0_per_seq ? batch : 1) * dff;
     for (int64_t k = 0; k < K; ++k) {
-      // apply: O_acc[s] = Z_k[s] W_k[s]; on the tensor cores the last split
-      // contributor of each tile also writes O_k and R_k = O_k - V_k
+      // apply: O_acc[s] = Z_k[s] W_k[s], split over d_ff
       GemmProblem a;
       a.M = B;
       a.N = d;
       a.K = dff;
       a.nb1 = bint;
       a.A = mat(Z, batch * L, dff, 0, k * B, L);
-      if (bf16) {
-        a.B = mat(Wb, batch * dff, d, 1, 0, dff);
-      } else {
+      if (bf16)
+        a.B = mat(hi, batch * dff, d, 1, 0, dff);
+      else
         a.B = (k == 0) ? mat(W0, w0_rows, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
-      }
       a.epi = EPI_ACCUM;
       a.kind = K_APPLY;
       a.D = out(o_acc, d, 0, B, 0, batch * B);
       a.split_k = 1;
       IPTTT_CUDA(gemm(a, bf16, st));
-      {
-        // residual: O_k = O_acc, R_k = O_acc - V_k, O_acc = 0
-        ResidualArgs ra;
-        ra.acc = o_acc;
-        ra.V = V;
-        ra.O = O;
-        ra.R = R;
-        ra.B = B;
-        ra.d = d;
-        ra.nb1 = bint;
-        ra.o_y0 = k * B;
-        ra.o_ys1 = L;
-        IPTTT_CUDA(launch_residual(ra, bf16, st));
-      }
+      // residual: O_k = O_acc, R_k = O_acc - V_k, O_acc = 0
+      ResidualArgs ra;
+      ra.acc = o_acc;
+      ra.V = V;
+      ra.O = O;
+      ra.R = R;
+      ra.B = B;
+      ra.d = d;
+      ra.nb1 = bint;
+      ra.o_y0 = k * B;
+      ra.o_ys1 = L;
+      IPTTT_CUDA(launch_residual(ra, bf16, st));
       // update: W_{k+1} = W_k - (eta/B) Z_k^T R_k
       GemmProblem u;
       u.M = dff;
@@ -420,12 +426,17 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.B = mat(R, batch * B, d, 1, 0, B);
       u.epi = EPI_AXPY;
       u.kind = K_UPDATE;
-      u.D = out(Wf, d, 0, dff, 0, batch * dff);
-      u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r, 0, w0_rows) : out(Wf, d, 0, dff, 0, batch * dff);
-      if (bf16 && k + 1 < K) u.Db = out(Wb, d, 0, dff, 0, batch * dff);
+      if (bf16) {
+        u.D = u.src = out(hi, d, 0, dff, 0, batch * dff);
+        u.D_lo = u.src_lo = out(lo, d, 0, dff, 0, batch * dff);
+      } else {
+        u.D = out(Wf, d, 0, dff, 0, batch * dff);
+        u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r, 0, w0_rows) : out(Wf, d, 0, dff, 0, batch * dff);
+      }
       u.alpha = -eta / static_cast<float>(B);
       IPTTT_CUDA(gemm(u, bf16, st));
     }
+    if (bf16) IPTTT_CUDA(launch_merge_w(hi, lo, Wf, batch * nw, st));
     return IPTTT_OK;
   }
 
@@ -433,7 +444,6 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   const int64_t G = scan_groups(K), g = K / G;
   const int gint = static_cast<int>(G);
   float* D = reinterpret_cast<float*>(ws + lay.d);
-  __nv_bfloat16* Db = bf16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.db) : nullptr;
   const float alpha = eta / static_cast<float>(B);
   // group sums, all groups of all sequences at once
   GemmProblem s;
@@ -450,7 +460,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   s.D = out(D, d, 0, dff, batch * dff);
   IPTTT_CUDA(gemm(s, bf16, st));
   // exclusive scan over groups -> the fast weight at the start of each group
-  IPTTT_CUDA(launch_group_scan(D, Db, W0, w0s, Wf, G, batch, nw, alpha, st));
+  IPTTT_CUDA(launch_group_scan(D, hi, lo, W0, w0s, Wf, G, batch, nw, alpha, st));
   IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * G * batch * B * d, st));
   for (int64_t i = 0; i < g; ++i) {
     GemmProblem a;
@@ -460,7 +470,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     a.nb1 = bint;
     a.nb2 = gint;
     a.A = mat(Z, batch * L, dff, 0, i * B, L, g * B);
-    a.B = bf16 ? mat(Db, G * batch * dff, d, 1, 0, dff, batch * dff) : mat(D, G * batch * dff, d, 1, 0, dff, batch * dff);
+    a.B = bf16 ? mat(hi, G * batch * dff, d, 1, 0, dff, batch * dff) : mat(D, G * batch * dff, d, 1, 0, dff, batch * dff);
     a.epi = EPI_ACCUM;
     a.kind = K_APPLY;
     a.D = out(o_acc, d, 0, B, batch * B, G * batch * B);
@@ -490,9 +500,12 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.B = mat(V, batch * L, d, 1, i * B, L, g * B);
       u.epi = EPI_AXPY;
       u.kind = K_UPDATE;
-      u.D = out(D, d, 0, dff, batch * dff, G * batch * dff);
-      u.src = u.D;
-      if (bf16) u.Db = out(Db, d, 0, dff, batch * dff, G * batch * dff);
+      if (bf16) {
+        u.D = u.src = out(hi, d, 0, dff, batch * dff, G * batch * dff);
+        u.D_lo = u.src_lo = out(lo, d, 0, dff, batch * dff, G * batch * dff);
+      } else {
+        u.D = u.src = out(D, d, 0, dff, batch * dff, G * batch * dff);
+      }
       u.alpha = alpha;
       IPTTT_CUDA(gemm(u, bf16, st));
     }

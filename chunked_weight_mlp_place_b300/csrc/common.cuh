@@ -340,6 +340,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// The fp32 fast weight is kept as two 16-bit planes.  hi is the bf16 nearest to
+// w (ties away from zero) -- the tensor-core operand as it stands -- and lo is
+// the signed remainder of w's bit pattern, so bits(w) = (hi << 16) + lo exactly:
+// the pair holds the fp32 value bit for bit.
+__device__ __forceinline__ void split_w(float w, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b = __float_as_uint(w);
+  const uint32_t h = (b + 0x8000u) >> 16;
+  hi = h & 0xFFFFu;
+  lo = (b - (h << 16)) & 0xFFFFu;
+}
+__device__ __forceinline__ float join_w(uint32_t hi, uint32_t lo) {
+  return __uint_as_float((hi << 16) + static_cast<uint32_t>(static_cast<int32_t>(static_cast<int16_t>(lo))));
+}
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 
 template <typename T>

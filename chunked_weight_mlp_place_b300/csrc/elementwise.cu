@@ -188,19 +188,36 @@ __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs
 }
 
 // -------------------------------------------------------------- fast weight
-__global__ void __launch_bounds__(kThreads) to_bf16_kernel(const float* __restrict__ W0, int64_t w0_stride,
-                                                           __nv_bfloat16* __restrict__ Wb, int64_t batch,
-                                                           int64_t n) {
+// W0[s or 0] (fp32) -> its split planes hi[s], lo[s] (split_w) for s < batch.
+__global__ void __launch_bounds__(kThreads) split_w_kernel(const float* __restrict__ W0, int64_t w0_stride,
+                                                           uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                                                           int64_t batch, int64_t n) {
   const int64_t nq = n / 4;
   const int64_t total = nq * batch;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t s = idx / nq, q = idx % nq;
     const float4 x = reinterpret_cast<const float4*>(W0 + s * w0_stride)[q];
-    uint2 o;
-    o.x = pack_bf16x2(x.x, x.y);
-    o.y = pack_bf16x2(x.z, x.w);
-    reinterpret_cast<uint2*>(Wb + s * n)[q] = o;
+    uint32_t h[4], l[4];
+    split_w(x.x, h[0], l[0]);
+    split_w(x.y, h[1], l[1]);
+    split_w(x.z, h[2], l[2]);
+    split_w(x.w, h[3], l[3]);
+    reinterpret_cast<uint2*>(hi + s * n)[q] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    reinterpret_cast<uint2*>(lo + s * n)[q] = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+  }
+}
+
+// W = join_w(hi, lo), element-wise over `total` (a multiple of 4) elements.
+__global__ void __launch_bounds__(kThreads) merge_w_kernel(const uint16_t* __restrict__ hi,
+                                                           const uint16_t* __restrict__ lo, float* __restrict__ W,
+                                                           int64_t total) {
+  const int64_t nq = total / 4;
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < nq;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint2 h = reinterpret_cast<const uint2*>(hi)[q], l = reinterpret_cast<const uint2*>(lo)[q];
+    reinterpret_cast<float4*>(W)[q] = make_float4(join_w(h.x & 0xFFFFu, l.x & 0xFFFFu), join_w(h.x >> 16, l.x >> 16),
+                                                  join_w(h.y & 0xFFFFu, l.y & 0xFFFFu), join_w(h.y >> 16, l.y >> 16));
   }
 }
 
@@ -215,11 +232,12 @@ __global__ void __launch_bounds__(kThreads) copy_w_kernel(const float* __restric
 }
 
 // Exclusive prefix over the G group sums of the additive rule, turning each
-// sum into the fast weight at the start of its group.
-__global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict__ D, __nv_bfloat16* __restrict__ Db,
-                                                              const float* __restrict__ W0, int64_t w0_stride,
-                                                              float* __restrict__ Wf, int64_t G, int64_t batch,
-                                                              int64_t n, float alpha) {
+// sum into the fast weight at the start of its group: in place in fp32, or
+// (hi != nullptr) into the split planes hi[g], lo[g].
+__global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict__ D, uint16_t* __restrict__ hi,
+                                                              uint16_t* __restrict__ lo, const float* __restrict__ W0,
+                                                              int64_t w0_stride, float* __restrict__ Wf, int64_t G,
+                                                              int64_t batch, int64_t n, float alpha) {
   const int64_t total = n * batch;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -228,8 +246,14 @@ __global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict_
     for (int64_t g = 0; g < G; ++g) {
       const int64_t at = g * total + idx;
       const float t = D[at];
-      D[at] = S;
-      if (Db) Db[at] = __float2bfloat16_rn(S);
+      if (hi) {
+        uint32_t h, l;
+        split_w(S, h, l);
+        hi[at] = static_cast<uint16_t>(h);
+        lo[at] = static_cast<uint16_t>(l);
+      } else {
+        D[at] = S;
+      }
       S = fmaf(alpha, t, S);
     }
     Wf[idx] = S;
@@ -271,11 +295,18 @@ cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t strea
   return cudaGetLastError();
 }
 
-cudaError_t launch_to_bf16(const float* W0, int64_t w0_stride, __nv_bfloat16* Wb, int64_t batch, int64_t n,
+cudaError_t launch_split_w(const float* W0, int64_t w0_stride, uint16_t* hi, uint16_t* lo, int64_t batch, int64_t n,
                            cudaStream_t stream) {
   if (n % 4) return cudaErrorInvalidValue;
   LaunchMark mark(K_WEIGHT, stream);
-  to_bf16_kernel<<<grid_for(n / 4 * batch), kThreads, 0, stream>>>(W0, w0_stride, Wb, batch, n);
+  split_w_kernel<<<grid_for(n / 4 * batch), kThreads, 0, stream>>>(W0, w0_stride, hi, lo, batch, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_w(const uint16_t* hi, const uint16_t* lo, float* W, int64_t total, cudaStream_t stream) {
+  if (total % 4) return cudaErrorInvalidValue;
+  LaunchMark mark(K_WEIGHT, stream);
+  merge_w_kernel<<<grid_for(total / 4), kThreads, 0, stream>>>(hi, lo, W, total);
   return cudaGetLastError();
 }
 
@@ -286,10 +317,10 @@ cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_group_scan(float* D, __nv_bfloat16* Db, const float* W0, int64_t w0_stride, float* W_final,
-                              int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream) {
+cudaError_t launch_group_scan(float* D, uint16_t* hi, uint16_t* lo, const float* W0, int64_t w0_stride,
+                              float* W_final, int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream) {
   LaunchMark mark(K_SCAN, stream);
-  group_scan_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(D, Db, W0, w0_stride, W_final, G, batch, n,
+  group_scan_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(D, hi, lo, W0, w0_stride, W_final, G, batch, n,
                                                                   alpha);
   return cudaGetLastError();
 }

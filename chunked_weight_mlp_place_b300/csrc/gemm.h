@@ -19,7 +19,7 @@ enum EpiKind : int {
   EPI_STORE = 0,  // D = acc                                  (D in the act dtype)
   EPI_GATE = 1,   // D = SiLU(acc_g) * acc_u, acc_u from B2   (D in the act dtype)
   EPI_ACCUM = 2,  // D += acc, fp32 reductions in L2          (D fp32; partial sums)
-  EPI_AXPY = 3,   // D = src + alpha * acc (fp32); Db = bf16(D) if Db != nullptr
+  EPI_AXPY = 3,   // D = src + alpha * acc, fp32 (CUDA cores) or split hi/lo planes (tensor cores)
 };
 
 struct Operand {
@@ -42,9 +42,10 @@ struct GemmProblem {
   Operand A, B, B2;
   int epi = EPI_STORE;
   int out_bf16 = 0;  // element type of D for STORE / GATE
-  OutRef D;          // primary output
-  OutRef src;        // AXPY: fp32 source (may equal D)
-  OutRef Db;         // AXPY: optional bf16 copy
+  OutRef D;          // primary output (AXPY on the tensor cores: the hi plane)
+  OutRef src;        // AXPY: source (may equal D); fp32, or the hi plane on the tensor cores
+  OutRef D_lo;       // AXPY on the tensor cores: lo planes of D and src (16-bit, same layout
+  OutRef src_lo;     //   as the hi planes; see split_w in common.cuh)
   float alpha = 1.0f;
   int split_k = 0;   // tensor-core path: 1 = balance (tile, k-block) work over CTAs (needs EPI_ACCUM)
   int kind = 0;      // KernelKind label (launch counting / timing)

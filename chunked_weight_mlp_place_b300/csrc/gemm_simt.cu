@@ -97,10 +97,6 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmProblem p
           const int64_t srow = p.src.y0 + b1 * p.src.ys1 + b2 * p.src.ys2 + m;
           const float w = static_cast<const float*>(p.src.ptr)[srow * p.src.ld + n] + p.alpha * v;
           *d = w;
-          if (p.Db.ptr) {
-            const int64_t brow = p.Db.y0 + b1 * p.Db.ys1 + b2 * p.Db.ys2 + m;
-            static_cast<__nv_bfloat16*>(p.Db.ptr)[brow * p.Db.ld + n] = __float2bfloat16_rn(w);
-          }
           break;
         }
       }

@@ -71,16 +71,18 @@ struct Cfg {
   static constexpr int B_COLS = PAIR ? N_MMA / 2 : N_MMA;  // B columns held by one CTA per stage
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_COLS * BK * 2;
-  // update: the fp32 W tile streams through slots of 128 rows x 16 columns (64-byte rows)
+  // update: the fast weight's hi and lo planes stream through slots of 128 rows x
+  // 16 columns each (two 32-byte-row tiles, 4 KB apart)
   static constexpr int WC = 16;
-  static constexpr int W_SLOT_BYTES = BM * WC * 4;
+  static constexpr int W_SLOT_BYTES = 2 * BM * WC * 2;
   static constexpr int W_SLOTS = W_LOAD ? 8 : 0;
-  // per epilogue warp, staging buffers for TMA stores / reductions:
-  //   apply: 2 of 32 rows x 32 fp32 (128-byte rows); update: 3 of 32 rows x 16 bf16 (32-byte rows)
-  static constexpr int STG_BYTES = RED ? 32 * 32 * 4 : (W_LOAD ? 32 * WC * 2 : 0);
+  // staging buffers of the whole tile (128 rows) for TMA stores / reductions:
+  //   apply: 2 of 128 rows x 32 fp32 (128-byte rows);
+  //   update: 3 of [hi plane | lo plane], 128 rows x 16 x 16-bit each (32-byte rows)
+  static constexpr int STG_BYTES = RED ? BM * 32 * 4 : (W_LOAD ? 2 * BM * WC * 2 : 0);
   static constexpr int STG_BUFS = W_LOAD ? 3 : 2;
-  static constexpr int STG_TOTAL = 4 * STG_BUFS * STG_BYTES;
-  static constexpr int STAGES = PAIR ? (W_LOAD ? 4 : 6) : (W_LOAD ? 3 : 4);
+  static constexpr int STG_TOTAL = STG_BUFS * STG_BYTES;
+  static constexpr int STAGES = PAIR ? (W_LOAD ? 4 : 6) : (W_LOAD ? 2 : 4);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES =
       1024 + STAGES * STAGE_BYTES + W_SLOTS * W_SLOT_BYTES + STG_TOTAL + BAR_BYTES;
@@ -162,6 +164,12 @@ struct KParams {
   GemmProblem p;
   Sched s;
 };
+
+// Named barrier of the four epilogue warps (128 threads); each warp re-converges first.
+__device__ __forceinline__ void epi_barrier() {
+  __syncwarp();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 __device__ __forceinline__ int64_t row_of(const Operand& o, int b1, int b2) {
   return o.y0 + b1 * o.ys1 + b2 * o.ys2;
@@ -265,7 +273,8 @@ template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAI
 __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmS,
-                   const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmDb,
+                   const __grid_constant__ CUtensorMap tmSl, const __grid_constant__ CUtensorMap tmD,
+                   const __grid_constant__ CUtensorMap tmDl,
                    const __grid_constant__ KParams kp) {
   using C = Cfg<BN, NB, EPI, PAIR>;
   static_assert(!PAIR || B_MN, "pairs split an MN-major B operand by columns");
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       mbar_init(drain_bar, 1);
       for (int i = 0; i < C::W_SLOTS; ++i) {
         mbar_init(&wfull_bar[i], 1);
-        mbar_init(&wempty_bar[i], 4);  // one arrival per epilogue warp
+        mbar_init(&wempty_bar[i], 1);  // the epilogue's store issuer, after all four warps read the slot
       }
       *abort_flag = 0;
       fence_mbarrier_init();
@@ -315,7 +324,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       if constexpr (NB == 2) tma_prefetch_desc(&tmB2);
       if constexpr (C::W_LOAD) {
         tma_prefetch_desc(&tmS);
-        tma_prefetch_desc(&tmDb);
+        tma_prefetch_desc(&tmSl);
+        tma_prefetch_desc(&tmDl);
       }
       if constexpr (C::W_LOAD || C::RED) tma_prefetch_desc(&tmD);
     }
@@ -452,15 +462,19 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp % 4;          // TMEM lanes 32*quarter .. +31 belong to this warp
     const int trow = quarter * 32 + lane;  // row of the tile this thread finishes
-    uint8_t* my_stg = stg + quarter * C::STG_BUFS * C::STG_BYTES;
+    const bool issuer = (trow == 0);       // issues the tile-wide TMA stores / reductions
     uint64_t pol = 0;
     if constexpr (C::W_LOAD) pol = l2_policy_evict_first();
     uint32_t ls = 0, wc = 0, sc = 0;
+    // The four warps meet at a named barrier once per stored chunk, so none may leave the
+    // loops early: a warp whose wait ran out (failed) skips the waits and the work from then
+    // on but still walks every tile and chunk, and the CTA ends with the others.
+    bool failed = false;
     while (iter.next(seg)) {
       const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
-      // Every lane waits (each needs the acquire); the warp leaves together if any gave up,
-      // because the TMEM loads below are warp-collective.
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error))) break;
+      // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
+      if (!failed)
+        failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error));
       tc_fence_after();
       int bi;
       int64_t mt, nt;
@@ -468,69 +482,68 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       if constexpr (PAIR) mt = 2 * mt + rank;
       const int b1 = bi % p.nb1, b2 = bi / p.nb1;
       const int64_t m = mt * BM + trow;
-      // this warp's 32 rows can go through one TMA box only if all of them are rows of the problem
-      const bool box_rows = (mt * BM + quarter * 32 + 32 <= p.M);
+      // the tile goes through tile-wide TMA boxes only if all its 128 rows are rows of the problem
+      const bool box_rows = (mt * BM + BM <= p.M);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
-      bool ok = true;
       if constexpr (C::W_LOAD) {
-        // ---- update: W = src + alpha * acc in the slot, TMA stores of W and its bf16 copy
-        const int yD = static_cast<int>(row_of(p.D, b1, b2) + mt * BM + quarter * 32);
-        const int yDb = static_cast<int>(row_of(p.Db, b1, b2) + mt * BM + quarter * 32);
-        // One chunk of WC columns: W(slot) + alpha * acc(regs) -> slot (fp32) and staging (bf16),
-        // then this warp's TMA stores.  Stores stay in flight for two chunks: the slot
-        // and staging buffer of chunk wc-2 are released once they have been read.
-        auto chunk = [&](int c, const uint32_t(&r)[C::WC]) -> bool {
+        // ---- update: W = src + alpha * acc on the split planes (split_w): the slot holds this
+        // tile's hi and lo planes; the result goes through a staging buffer and two TMA stores.
+        const int yD = static_cast<int>(row_of(p.D, b1, b2) + mt * BM);
+        // One chunk of WC columns.  The slot goes back to the loader once all four warps have
+        // read it; the tile-wide stores stay in flight for two chunks, so a staging buffer is
+        // rewritten only after the stores issued from it two chunks earlier have read it.
+        auto chunk = [&](int c, const uint32_t(&r)[C::WC]) {
           const uint32_t slot = wc % C::W_SLOTS, wph = (wc / C::W_SLOTS) & 1;
-          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error)))
-            return false;
-          // 64-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 1) & 3)
-          float4* srow = reinterpret_cast<float4*>(wslots + slot * C::W_SLOT_BYTES + trow * 64);
-          uint8_t* sbuf = my_stg + (wc % C::STG_BUFS) * C::STG_BYTES;
-          float w[16];
+          if (!failed)
+            failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error));
+          // 32-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 2) & 1)
+          const int sw = (trow >> 2) & 1;
+          const uint4* hrow = reinterpret_cast<const uint4*>(wslots + slot * C::W_SLOT_BYTES + trow * 32);
+          const uint4* lrow = reinterpret_cast<const uint4*>(wslots + slot * C::W_SLOT_BYTES + BM * 32 + trow * 32);
+          const uint4 h0 = hrow[0 ^ sw], h1 = hrow[1 ^ sw], l0 = lrow[0 ^ sw], l1 = lrow[1 ^ sw];
+          const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+          const uint32_t lw[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+          uint32_t ho[8], lo[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 x = srow[j ^ ((trow >> 1) & 3)];
-            w[4 * j] = fmaf(p.alpha, __uint_as_float(r[4 * j]), x.x);
-            w[4 * j + 1] = fmaf(p.alpha, __uint_as_float(r[4 * j + 1]), x.y);
-            w[4 * j + 2] = fmaf(p.alpha, __uint_as_float(r[4 * j + 2]), x.z);
-            w[4 * j + 3] = fmaf(p.alpha, __uint_as_float(r[4 * j + 3]), x.w);
+          for (int q = 0; q < 8; ++q) {
+            uint32_t a0, a1, b0, b1;
+            split_w(fmaf(p.alpha, __uint_as_float(r[2 * q]), join_w(hw[q] & 0xFFFFu, lw[q] & 0xFFFFu)), a0, b0);
+            split_w(fmaf(p.alpha, __uint_as_float(r[2 * q + 1]), join_w(hw[q] >> 16, lw[q] >> 16)), a1, b1);
+            ho[q] = a0 | (a1 << 16);
+            lo[q] = b0 | (b1 << 16);
           }
           const int64_t n = nt * BN + c * C::WC;
-          if (box_rows) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              srow[j ^ ((trow >> 1) & 3)] = make_float4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-            if (p.Db.ptr) {
-              // 32-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 2) & 1)
-              uint4* brow = reinterpret_cast<uint4*>(sbuf + lane * 32);
-              brow[0 ^ ((lane >> 2) & 1)] = pack8_bf16(w);
-              brow[1 ^ ((lane >> 2) & 1)] = pack8_bf16(w + 8);
-            }
+          uint8_t* sbuf = stg + (wc % C::STG_BUFS) * C::STG_BYTES;
+          if (failed) {
+            // nothing to store
+          } else if (box_rows) {
+            uint4* hs = reinterpret_cast<uint4*>(sbuf + trow * 32);
+            uint4* lsb = reinterpret_cast<uint4*>(sbuf + BM * 32 + trow * 32);
+            hs[0 ^ sw] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+            hs[1 ^ sw] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
+            lsb[0 ^ sw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            lsb[1 ^ sw] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
           } else if (m < p.M) {
-            float* d = static_cast<float*>(p.D.ptr) + (row_of(p.D, b1, b2) + m) * p.D.ld + n;
-            __nv_bfloat16* db =
-                p.Db.ptr ? static_cast<__nv_bfloat16*>(p.Db.ptr) + (row_of(p.Db, b1, b2) + m) * p.Db.ld + n : nullptr;
+            uint16_t* dh = static_cast<uint16_t*>(p.D.ptr) + (row_of(p.D, b1, b2) + m) * p.D.ld + n;
+            uint16_t* dl = static_cast<uint16_t*>(p.D_lo.ptr) + (row_of(p.D_lo, b1, b2) + m) * p.D_lo.ld + n;
             for (int i = 0; i < C::WC && n + i < p.N; ++i) {
-              d[i] = w[i];
-              if (db) db[i] = __float2bfloat16_rn(w[i]);
+              dh[i] = static_cast<uint16_t>(ho[i / 2] >> (16 * (i % 2)));
+              dl[i] = static_cast<uint16_t>(lo[i / 2] >> (16 * (i % 2)));
             }
           }
-          // Shared-memory writes (and reads of the slot) before the async-proxy copies below.
+          // The slot's reads and the staging writes before the async-proxy copies below.
           fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
+          if (issuer) bulk_wait_group_read<C::STG_BUFS - 2>();  // the next chunk's buffer is free
+          epi_barrier();
+          if (issuer && !failed) {
+            mbar_arrive(&wempty_bar[slot]);
             if (box_rows && n < p.N) {
-              tma_store_2d_hint(&tmD, wslots + slot * C::W_SLOT_BYTES + quarter * 32 * 64, static_cast<int>(n), yD,
-                                pol);
-              if (p.Db.ptr) tma_store_2d(&tmDb, sbuf, static_cast<int>(n), yDb);
+              tma_store_2d(&tmD, sbuf, static_cast<int>(n), yD);
+              tma_store_2d_hint(&tmDl, sbuf + BM * 32, static_cast<int>(n), yD, pol);
             }
             bulk_commit_group();
-            bulk_wait_group_read<2>();
-            if (wc >= 2) mbar_arrive(&wempty_bar[(wc - 2) % C::W_SLOTS]);
           }
-          __syncwarp();
           ++wc;
-          return true;
         };
         // The accumulator columns of the next chunk load from TMEM while this one is finished.
         constexpr int NCH = BN / C::WC;
@@ -538,14 +551,13 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         uint32_t ra[C::WC], rb[C::WC];
         tmem_ld_32x32b_x16(tbase, ra);
 #pragma unroll 1
-        for (int c = 0; c < NCH && ok; c += 2) {
+        for (int c = 0; c < NCH; c += 2) {
           tmem_wait_ld(ra);
           tmem_ld_32x32b_x16(tbase + (c + 1) * C::WC, rb);
-          ok = chunk(c, ra);
+          chunk(c, ra);
           tmem_wait_ld(rb);
-          if (!ok) break;
           if (c + 2 < NCH) tmem_ld_32x32b_x16(tbase + (c + 2) * C::WC, ra);
-          ok = chunk(c + 1, rb);
+          chunk(c + 1, rb);
         }
         tmem_wait_ld();
       } else {
@@ -560,25 +572,26 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           if constexpr (C::RED) {
             if (box_rows) {
               // 128-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ (t % 8)
-              float4* srow = reinterpret_cast<float4*>(my_stg + (sc & 1) * C::STG_BYTES + lane * 128);
+              uint8_t* sbuf = stg + (sc & 1) * C::STG_BYTES;
+              float4* srow = reinterpret_cast<float4*>(sbuf + trow * 128);
+              if (!failed) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                srow[j ^ (lane & 7)] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-              fence_proxy_async_shared();
-              __syncwarp();
-              if (lane == 0) {
-                tma_reduce_add_2d(&tmD, my_stg + (sc & 1) * C::STG_BYTES, static_cast<int>(n),
-                                  static_cast<int>(row_of(p.D, b1, b2) + mt * BM + quarter * 32));
-                bulk_commit_group();
-                bulk_wait_group_read<1>();  // the other staging buffer is free again
+                for (int j = 0; j < 8; ++j)
+                  srow[j ^ (trow & 7)] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
               }
-              __syncwarp();
+              fence_proxy_async_shared();
+              if (issuer) bulk_wait_group_read<0>();  // the other buffer, written next chunk, is free
+              epi_barrier();
+              if (issuer && !failed) {
+                tma_reduce_add_2d(&tmD, sbuf, static_cast<int>(n), static_cast<int>(row_of(p.D, b1, b2) + mt * BM));
+                bulk_commit_group();
+              }
               ++sc;
               continue;
             }
           }
-          if (m < p.M) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
+          if (m < p.M && !failed) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
         }
       }
       // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
@@ -590,12 +603,11 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         else
           mbar_arrive(&tempty_bar[acc]);
       }
-      if (!ok) break;
       ++ls;
     }
-    // Every bulk store / reduction of this warp has completed before the CTA exits.
+    // Every bulk store / reduction has completed before the CTA exits.
     if constexpr (C::W_LOAD || C::RED) {
-      if (lane == 0) bulk_wait_group<0>();
+      if (issuer) bulk_wait_group<0>();
       __syncwarp();
     }
   } else {
@@ -619,8 +631,9 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               break;
             }
             mbar_arrive_expect_tx(&wfull_bar[slot], C::W_SLOT_BYTES);
-            tma_load_2d_hint(wslots + slot * C::W_SLOT_BYTES, &tmS, &wfull_bar[slot],
-                             static_cast<int>(nt * BN + c * C::WC), static_cast<int>(row0), pol);
+            const int x = static_cast<int>(nt * BN + c * C::WC), y = static_cast<int>(row0);
+            tma_load_2d_hint(wslots + slot * C::W_SLOT_BYTES, &tmS, &wfull_bar[slot], x, y, pol);
+            tma_load_2d_hint(wslots + slot * C::W_SLOT_BYTES + BM * 32, &tmSl, &wfull_bar[slot], x, y, pol);
           }
         }
         for (uint32_t slot = 0; slot < C::W_SLOTS && slot < wc; ++slot) {
@@ -737,20 +750,22 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
 
   // Operand boxes: 64 K-elements (128 bytes) wide; K-major boxes span the
   // tile's rows, MN-major boxes are 64 K-rows of 64 columns.
-  CUtensorMap mA, mB, mB2, mS, mD, mDb;
+  CUtensorMap mA, mB, mB2, mS, mSl, mD, mDl;
   if (!make_map(&mA, p.A.ptr, p.A.rows, p.A.cols, p.A.ld, false, 64, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
   if (!make_map(&mB, p.B.ptr, p.B.rows, p.B.cols, p.B.ld, false, 64, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
   mB2 = mB;
   if (NB == 2 && !make_map(&mB2, p.B2.ptr, p.B2.rows, p.B2.cols, p.B2.ld, false, 64, B_MN ? 64 : BN))
     return cudaErrorInvalidValue;
-  mS = mD = mDb = mA;
+  mS = mSl = mD = mDl = mA;
   if (C::W_LOAD) {
-    if (!make_map(&mS, p.src.ptr, p.src.rows, p.N, p.src.ld, true, C::WC, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, C::WC, 32)) return cudaErrorInvalidValue;
-    if (p.Db.ptr && !make_map(&mDb, p.Db.ptr, p.Db.rows, p.N, p.Db.ld, false, C::WC, 32))
+    // hi and lo planes: 16-bit elements, 16-column (32-byte) boxes
+    if (!make_map(&mS, p.src.ptr, p.src.rows, p.N, p.src.ld, false, C::WC, BM) ||
+        !make_map(&mSl, p.src_lo.ptr, p.src_lo.rows, p.N, p.src_lo.ld, false, C::WC, BM) ||
+        !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, false, C::WC, BM) ||
+        !make_map(&mDl, p.D_lo.ptr, p.D_lo.rows, p.N, p.D_lo.ld, false, C::WC, BM))
       return cudaErrorInvalidValue;
   }
-  if (C::RED && !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, 32, 32)) return cudaErrorInvalidValue;
+  if (C::RED && !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, 32, BM)) return cudaErrorInvalidValue;
 
   KParams kp;
   kp.p = p;
@@ -770,7 +785,7 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   if (workers <= 0) return cudaSuccess;
   LaunchMark mark(p.kind, stream);
   return launch_overlapped(kern, dim3(static_cast<unsigned>((PAIR ? 2 : 1) * workers)), dim3(C::THREADS),
-                           C::SMEM_BYTES, stream, PAIR ? 2 : 1, mA, mB, mB2, mS, mD, mDb, kp);
+                           C::SMEM_BYTES, stream, PAIR ? 2 : 1, mA, mB, mB2, mS, mSl, mD, mDl, kp);
 }
 
 // Pairs of CTAs once the problem has at least two 128-row tiles.

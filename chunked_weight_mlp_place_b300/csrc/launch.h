@@ -19,7 +19,7 @@ enum KernelKind : int {
   K_UPDATE = 5,    // W_{k+1} = W_k + alpha Z_k^T R_k
   K_GROUP_SUM = 6, // additive scan: per-group Z^T V
   K_SCAN = 7,      // additive scan: exclusive prefix over groups
-  K_WEIGHT = 8,    // fast-weight copies (bf16 copy of W_o0, W_o0 -> W_final)
+  K_WEIGHT = 8,    // fast-weight conversions (W_o0 -> split planes -> W_final, W_o0 -> W_final)
   K_COUNT = 9
 };
 
@@ -89,16 +89,20 @@ struct ResidualArgs {
 };
 cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t stream);
 
-// Wb[s] = bf16(W0[s or 0]) for s < batch; n = d_ff*d.
-cudaError_t launch_to_bf16(const float* W0, int64_t w0_stride, __nv_bfloat16* Wb, int64_t batch, int64_t n,
+// The fp32 fast weight as split hi/lo planes (split_w / join_w in common.cuh):
+//   split: hi[s], lo[s] = split(W0[s or 0]) for s < batch, n = d_ff*d (a multiple of 4);
+//   merge: W = join(hi, lo) over `total` elements (a multiple of 4).
+cudaError_t launch_split_w(const float* W0, int64_t w0_stride, uint16_t* hi, uint16_t* lo, int64_t batch, int64_t n,
                            cudaStream_t stream);
+cudaError_t launch_merge_w(const uint16_t* hi, const uint16_t* lo, float* W, int64_t total, cudaStream_t stream);
 // W[s] = W0[s or 0] (fp32 copy) for s < batch.
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream);
 
-// Exclusive scan over G group sums, element-wise over batch*n:
-//   S = W0; for g: t = D[g]; D[g] = S; Db[g] = bf16(S) (if Db); S += alpha*t;  W_final = S
-cudaError_t launch_group_scan(float* D, __nv_bfloat16* Db, const float* W0, int64_t w0_stride, float* W_final,
-                              int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream);
+// Exclusive scan over G fp32 group sums D[g], element-wise over batch*n:
+//   S = W0; for g: t = D[g]; state[g] = S; S += alpha*t;  W_final = S
+// where state[g] is D[g] itself (hi == nullptr) or the split planes hi[g], lo[g].
+cudaError_t launch_group_scan(float* D, uint16_t* hi, uint16_t* lo, const float* W0, int64_t w0_stride,
+                              float* W_final, int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream);
 
 }  // namespace ipttt

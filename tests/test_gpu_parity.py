@@ -201,8 +201,8 @@ def test_launch_count_and_no_host_fallback():
     w = inputs.workload("500m", batch=1, L=256, B=64, d=128, d_ff=256)
     a = inputs.generate(w, seed=4)
     run_layer(w, a, "mse")
-    # gate + conv + proj + bf16 copy of W_o0 + K * (apply + residual + update)
-    assert ip.last_launch_count() == 3 + 1 + 3 * (w.L // w.B)
+    # gate + conv + proj + split of W_o0 + K * (apply + residual + update) + merge into W_final
+    assert ip.last_launch_count() == 3 + 1 + 3 * (w.L // w.B) + 1
 
 
 @pytest.mark.parametrize("rule", ["mse", "add"])
