@@ -340,18 +340,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-// The fp32 fast weight is kept as two 16-bit planes.  hi is the bf16 nearest to
-// w (ties away from zero) -- the tensor-core operand as it stands -- and lo is
-// the signed remainder of w's bit pattern, so bits(w) = (hi << 16) + lo exactly:
-// the pair holds the fp32 value bit for bit.
+// The fp32 fast weight is kept as two 16-bit planes.  With b the bit pattern of
+// w: hi = (b + 0x8000) >> 16 is the bf16 nearest to w (ties away from zero) --
+// the tensor-core operand as it stands -- and lo = (b + 0x8000) & 0xFFFF is the
+// remainder, offset by 0x8000 so that it is never negative.  Since
+// b = (hi << 16) + lo - 0x8000, the pair holds the fp32 value bit for bit.
 __device__ __forceinline__ void split_w(float w, uint32_t& hi, uint32_t& lo) {
-  const uint32_t b = __float_as_uint(w);
-  const uint32_t h = (b + 0x8000u) >> 16;
-  hi = h & 0xFFFFu;
-  lo = (b - (h << 16)) & 0xFFFFu;
+  const uint32_t b = __float_as_uint(w) + 0x8000u;
+  hi = b >> 16;
+  lo = b & 0xFFFFu;
 }
 __device__ __forceinline__ float join_w(uint32_t hi, uint32_t lo) {
-  return __uint_as_float((hi << 16) + static_cast<uint32_t>(static_cast<int32_t>(static_cast<int16_t>(lo))));
+  return __uint_as_float(((hi << 16) | lo) - 0x8000u);
+}
+// The same on two elements whose halves are packed in 32-bit words (element 0
+// in the low half): hi2/lo2 hold the hi/lo halves of w0 and w1.
+__device__ __forceinline__ void split_w2(float w0, float w1, uint32_t& hi2, uint32_t& lo2) {
+  const uint32_t b0 = __float_as_uint(w0) + 0x8000u, b1 = __float_as_uint(w1) + 0x8000u;
+  hi2 = __byte_perm(b0, b1, 0x7632);
+  lo2 = __byte_perm(b0, b1, 0x5410);
+}
+__device__ __forceinline__ void join_w2(uint32_t hi2, uint32_t lo2, float& w0, float& w1) {
+  w0 = __uint_as_float(__byte_perm(lo2, hi2, 0x5410) - 0x8000u);
+  w1 = __uint_as_float(__byte_perm(lo2, hi2, 0x7632) - 0x8000u);
 }
 __device__ __forceinline__ float silu_f(float a) { return a / (1.0f + __expf(-a)); }
 

@@ -65,7 +65,9 @@ template <int BN, int NB, int EPI, bool PAIR>
 struct Cfg {
   static constexpr bool W_LOAD = (EPI == EPI_AXPY);
   static constexpr bool RED = (EPI == EPI_ACCUM);
-  static constexpr int THREADS = W_LOAD ? 224 : 192;
+  // update: two groups of four epilogue warps take alternate 16-column chunks
+  static constexpr int EPI_WARPS = W_LOAD ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS + (W_LOAD ? 32 : 0);
   static constexpr int N_MMA = BN * NB;          // the B operands sit side by side: one MMA covers them
   static constexpr int M_MMA = PAIR ? 2 * BM : BM;
   static constexpr int B_COLS = PAIR ? N_MMA / 2 : N_MMA;  // B columns held by one CTA per stage
@@ -76,12 +78,12 @@ struct Cfg {
   static constexpr int WC = 16;
   static constexpr int W_SLOT_BYTES = 2 * BM * WC * 2;
   static constexpr int W_SLOTS = W_LOAD ? 8 : 0;
-  // staging buffers of the whole tile (128 rows) for TMA stores / reductions:
+  // staging buffers of the whole tile (128 rows) for TMA stores / reductions, per group:
   //   apply: 2 of 128 rows x 32 fp32 (128-byte rows);
-  //   update: 3 of [hi plane | lo plane], 128 rows x 16 x 16-bit each (32-byte rows)
+  //   update: 2 of [hi plane | lo plane], 128 rows x 16 x 16-bit each (32-byte rows)
   static constexpr int STG_BYTES = RED ? BM * 32 * 4 : (W_LOAD ? 2 * BM * WC * 2 : 0);
-  static constexpr int STG_BUFS = W_LOAD ? 3 : 2;
-  static constexpr int STG_TOTAL = STG_BUFS * STG_BYTES;
+  static constexpr int STG_BUFS = 2;
+  static constexpr int STG_TOTAL = (EPI_WARPS / 4) * STG_BUFS * STG_BYTES;
   static constexpr int STAGES = PAIR ? (W_LOAD ? 4 : 6) : (W_LOAD ? 2 : 4);
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM_BYTES =
@@ -165,10 +167,11 @@ struct KParams {
   Sched s;
 };
 
-// Named barrier of the four epilogue warps (128 threads); each warp re-converges first.
-__device__ __forceinline__ void epi_barrier() {
+// Named barrier of a group of four epilogue warps (128 threads; group g uses
+// barrier 1 + g); each warp re-converges first.
+__device__ __forceinline__ void epi_barrier(int group) {
   __syncwarp();
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + group) : "memory");
 }
 
 __device__ __forceinline__ int64_t row_of(const Operand& o, int b1, int b2) {
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull_bar[i], 1);
-        mbar_init(&tempty_bar[i], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
+        mbar_init(&tempty_bar[i], (PAIR ? 2 : 1) * C::EPI_WARPS);  // one per epilogue warp (of both CTAs)
       }
       mbar_init(drain_bar, 1);
       for (int i = 0; i < C::W_SLOTS; ++i) {
@@ -458,14 +461,15 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         umma_commit(drain_bar);
       mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
     }
-  } else if (warp <= 5) {
+  } else if (warp < 2 + C::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp % 4;          // TMEM lanes 32*quarter .. +31 belong to this warp
+    const int group = (warp - 2) / 4;      // update: chunks c with c % 2 == group
     const int trow = quarter * 32 + lane;  // row of the tile this thread finishes
-    const bool issuer = (trow == 0);       // issues the tile-wide TMA stores / reductions
+    const bool issuer = (trow == 0);       // issues the group's tile-wide TMA stores / reductions
     uint64_t pol = 0;
     if constexpr (C::W_LOAD) pol = l2_policy_evict_first();
-    uint32_t ls = 0, wc = 0, sc = 0;
+    uint32_t ls = 0, sc = 0;
     // The four warps meet at a named barrier once per stored chunk, so none may leave the
     // loops early: a warp whose wait ran out (failed) skips the waits and the work from then
     // on but still walks every tile and chunk, and the CTA ends with the others.
@@ -487,13 +491,18 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
       if constexpr (C::W_LOAD) {
         // ---- update: W = src + alpha * acc on the split planes (split_w): the slot holds this
-        // tile's hi and lo planes; the result goes through a staging buffer and two TMA stores.
+        // chunk's hi and lo planes; the result goes through the group's staging buffer and two
+        // tile-wide TMA stores.
         const int yD = static_cast<int>(row_of(p.D, b1, b2) + mt * BM);
-        // One chunk of WC columns.  The slot goes back to the loader once all four warps have
-        // read it; the tile-wide stores stay in flight for two chunks, so a staging buffer is
-        // rewritten only after the stores issued from it two chunks earlier have read it.
+        constexpr int NCH = BN / C::WC;
+        static_assert(NCH % 4 == 0, "each group takes pairs of chunks");
+        const uint32_t chunk0 = ls * NCH;  // this CTA's running index of the tile's first chunk
+        // One chunk of WC columns.  The slot goes back to the loader once the group's four warps
+        // have read it; the group's stores stay in flight for one more chunk of the group, so
+        // a staging buffer is rewritten only after the stores issued from it have read it.
         auto chunk = [&](int c, const uint32_t(&r)[C::WC]) {
-          const uint32_t slot = wc % C::W_SLOTS, wph = (wc / C::W_SLOTS) & 1;
+          const uint32_t gch = chunk0 + c;
+          const uint32_t slot = gch % C::W_SLOTS, wph = (gch / C::W_SLOTS) & 1;
           if (!failed)
             failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error));
           // 32-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 2) & 1)
@@ -506,14 +515,14 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           uint32_t ho[8], lo[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            uint32_t a0, a1, b0, b1;
-            split_w(fmaf(p.alpha, __uint_as_float(r[2 * q]), join_w(hw[q] & 0xFFFFu, lw[q] & 0xFFFFu)), a0, b0);
-            split_w(fmaf(p.alpha, __uint_as_float(r[2 * q + 1]), join_w(hw[q] >> 16, lw[q] >> 16)), a1, b1);
-            ho[q] = a0 | (a1 << 16);
-            lo[q] = b0 | (b1 << 16);
+            float w0, w1;
+            join_w2(hw[q], lw[q], w0, w1);
+            split_w2(fmaf(p.alpha, __uint_as_float(r[2 * q]), w0), fmaf(p.alpha, __uint_as_float(r[2 * q + 1]), w1),
+                     ho[q], lo[q]);
           }
           const int64_t n = nt * BN + c * C::WC;
-          uint8_t* sbuf = stg + (wc % C::STG_BUFS) * C::STG_BYTES;
+          const uint32_t lc = ls * (NCH / 2) + c / 2;  // the group's running chunk count
+          uint8_t* sbuf = stg + (group * C::STG_BUFS + lc % C::STG_BUFS) * C::STG_BYTES;
           if (failed) {
             // nothing to store
           } else if (box_rows) {
@@ -533,8 +542,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           }
           // The slot's reads and the staging writes before the async-proxy copies below.
           fence_proxy_async_shared();
-          if (issuer) bulk_wait_group_read<C::STG_BUFS - 2>();  // the next chunk's buffer is free
-          epi_barrier();
+          if (issuer) bulk_wait_group_read<C::STG_BUFS - 2>();  // the group's next buffer is free
+          epi_barrier(group);
           if (issuer && !failed) {
             mbar_arrive(&wempty_bar[slot]);
             if (box_rows && n < p.N) {
@@ -543,21 +552,19 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
             }
             bulk_commit_group();
           }
-          ++wc;
         };
-        // The accumulator columns of the next chunk load from TMEM while this one is finished.
-        constexpr int NCH = BN / C::WC;
-        static_assert(NCH % 2 == 0, "chunks come in pairs");
+        // The group's chunks are c = group, group + 2, ...; the accumulator columns of its next
+        // chunk load from TMEM while this one is finished.
         uint32_t ra[C::WC], rb[C::WC];
-        tmem_ld_32x32b_x16(tbase, ra);
+        tmem_ld_32x32b_x16(tbase + group * C::WC, ra);
 #pragma unroll 1
-        for (int c = 0; c < NCH; c += 2) {
+        for (int c = group; c < NCH; c += 4) {
           tmem_wait_ld(ra);
-          tmem_ld_32x32b_x16(tbase + (c + 1) * C::WC, rb);
+          tmem_ld_32x32b_x16(tbase + (c + 2) * C::WC, rb);
           chunk(c, ra);
           tmem_wait_ld(rb);
-          if (c + 2 < NCH) tmem_ld_32x32b_x16(tbase + (c + 2) * C::WC, ra);
-          chunk(c + 1, rb);
+          if (c + 4 < NCH) tmem_ld_32x32b_x16(tbase + (c + 4) * C::WC, ra);
+          chunk(c + 2, rb);
         }
         tmem_wait_ld();
       } else {
@@ -582,7 +589,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               }
               fence_proxy_async_shared();
               if (issuer) bulk_wait_group_read<0>();  // the other buffer, written next chunk, is free
-              epi_barrier();
+              epi_barrier(0);
               if (issuer && !failed) {
                 tma_reduce_add_2d(&tmD, sbuf, static_cast<int>(n), static_cast<int>(row_of(p.D, b1, b2) + mt * BM));
                 bulk_commit_group();
