@@ -6,9 +6,9 @@
 //   Z = SiLU(X W_g) * (X W_u)                          one GEMM, gate epilogue
 //   V = Conv(E) P                                      conv kernel + GEMM
 //   MSE rule, for k = 0 .. K-1 (sequential):
-//     apply     O_acc = Z_k W_k          (bf16 W copy, split over d_ff, fp32 reductions)
+//     apply     O_acc = Z_k W_k          (bf16 hi plane of W, split over d_ff, fp32 reductions)
 //     residual  O_k = O_acc; R_k = O_acc - V_k; O_acc = 0
-//     update    W_{k+1} = W_k - (eta/B) Z_k^T R_k; bf16 copy of W_{k+1}
+//     update    W_{k+1} = W_k - (eta/B) Z_k^T R_k   (on the hi/lo planes of W)
 //   additive rule, chunk-parallel scan over G groups of g chunks (G*g = K):
 //     group sums   S_j = Z_{group j}^T V_{group j}           (all groups at once)
 //     scan         W^(j) = W_0 + (eta/B) sum_{i<j} S_i; W_final = W^(G)

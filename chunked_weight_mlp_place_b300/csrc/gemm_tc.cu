@@ -3,8 +3,10 @@
 // One persistent kernel template serves the four contractions of the layer:
 //   gate   Z = SiLU(X W_g) * (X W_u)       A = X   (K-major)  B = [W_g | W_u] (MN-major)
 //   proj   V = C P                          A = C   (K-major)  B = P           (MN-major)
-//   apply  O_k = Z_k W_k  (split over K)    A = Z_k (K-major)  B = W_k bf16    (MN-major)
+//   apply  O_k = Z_k W_k  (split over K)    A = Z_k (K-major)  B = hi plane    (MN-major)
 //   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k         (MN-major)
+// (the fast weight W is kept as split hi/lo 16-bit planes, common.cuh::split_w;
+// its hi plane is the bf16 operand of the apply).
 //
 // Problems with more than one 128-row tile run on CTA pairs (clusters of 2,
 // tcgen05 cta_group::2): one 256 x N MMA per pair, each CTA holding 128 rows
@@ -14,13 +16,14 @@
 // Each CTA (one per SM) runs these warps:
 //   warp 0      TMA producer: 128x64 A tiles and 64-wide B tiles into a ring of
 //               shared-memory stages (128-byte swizzle), completion on mbarriers;
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256, K=16)
-//               into a TMEM accumulator; tcgen05.commit frees each stage;
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (one TMEM lane per output
-//               row) and apply the fused epilogue;
-//   warp 6      (update only) fast-weight loader: streams the fp32 W tile the
-//               epilogue will read-modify-write into swizzled shared memory
-//               slots ahead of time, so the epilogue never waits on HBM.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128 or 256 per pair,
+//               N=256, K=16) into a TMEM accumulator; tcgen05.commit frees each stage;
+//   warps 2..   epilogue (4 warps; 8 for the update, two groups taking alternate
+//               16-column chunks): tcgen05.ld the accumulator (one TMEM lane per
+//               output row) and apply the fused epilogue;
+//   last warp   (update only) fast-weight loader: streams the hi and lo planes of
+//               the tile the epilogue read-modify-writes into swizzled shared-
+//               memory slots ahead of time.
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next.  Work is either whole output tiles, strided over
 // the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
@@ -28,14 +31,14 @@
 //
 // Epilogues that move much data go through shared memory and TMA, so global
 // memory sees whole 128-byte lines instead of one row per lane:
-//   apply (split mode)  each warp stages its 32 rows x 32 columns of fp32 partial
-//                       sums and adds them into the fp32 sums in L2 with a TMA
-//                       reduce (the residual kernel then turns the sums into
-//                       O and R = O - V);
-//   update              each warp overwrites its quarter of the fp32 W slot
-//                       with W + alpha*acc in place and stores it with TMA,
-//                       together with a staged bf16 copy; a slot goes back to
-//                       the loader once the store has read it.
+//   apply (split mode)  the epilogue stages the tile's 128 rows x 32 columns of
+//                       fp32 partial sums and adds them into the fp32 sums in L2
+//                       with one TMA reduce (the residual kernel then turns the
+//                       sums into O and R = O - V);
+//   update              a group computes W + alpha*acc on the planes of one
+//                       16-column chunk from its slot, stages the new planes for
+//                       the whole tile and stores them with two TMA stores; the
+//                       slot goes back to the loader once the group has read it.
 //
 // Every mbarrier wait is capped (common.cuh); a CTA whose wait runs out flags
 // the others, drains its in-flight TMA copies and MMAs, frees its TMEM and
