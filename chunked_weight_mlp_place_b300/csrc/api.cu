@@ -340,9 +340,25 @@ struct EngineLayout {
   size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, total = 0;
 };
 
+// Plane geometry of one d_ff x d fast weight (tile-major blocks, see common.cuh).
+int64_t plane_rb(const ipttt_dims* dm) { return (dm->d_ff + kPlaneRows - 1) / kPlaneRows; }
+int64_t plane_cb(const ipttt_dims* dm) { return (dm->d + kPlaneCols - 1) / kPlaneCols; }
+Planes planes_of(const ipttt_dims* dm, uint16_t* hi, uint16_t* lo, int64_t entries, int64_t es1, int64_t es2) {
+  Planes w;
+  w.hi = hi;
+  w.lo = lo;
+  w.rb = plane_rb(dm);
+  w.cb = plane_cb(dm);
+  w.es1 = es1;
+  w.es2 = es2;
+  w.entries = entries;
+  return w;
+}
+
 // Scratch of the chunk engine.  On the tensor cores the fp32 fast weight lives
-// as split hi/lo planes (bf16 hi = the apply's operand, 16-bit lo = the rest of
-// the fp32 bit pattern), so one update reads and writes 8 bytes per element.
+// as tile-major split hi/lo planes (bf16 hi = the apply's operand, 16-bit lo =
+// the rest of the fp32 bit pattern), so one update reads and writes 8 bytes
+// per element.
 EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rule rule, size_t base) {
   EngineLayout e;
   Carve c;
@@ -350,20 +366,21 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
   const bool bf16 = dm->dtype == IPTTT_BF16;
   const int64_t K = L / B;
   const int64_t nw = dm->d_ff * dm->d;
+  const int64_t np = plane_rb(dm) * plane_cb(dm) * kPlaneBlock;  // plane elements per entry
   if (rule == IPTTT_RULE_MSE) {
     e.o_acc = c.take<float>(dm->batch * B * dm->d);
     e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
     if (bf16) {
-      e.hi = c.take<uint16_t>(dm->batch * nw);
-      e.lo = c.take<uint16_t>(dm->batch * nw);
+      e.hi = c.take<uint16_t>(dm->batch * np);
+      e.lo = c.take<uint16_t>(dm->batch * np);
     }
   } else {
     const int64_t G = scan_groups(K);
     e.o_acc = c.take<float>(G * dm->batch * B * dm->d);
     e.d = c.take<float>(G * dm->batch * nw);
     if (bf16) {
-      e.hi = c.take<uint16_t>(G * dm->batch * nw);
-      e.lo = c.take<uint16_t>(G * dm->batch * nw);
+      e.hi = c.take<uint16_t>(G * dm->batch * np);
+      e.lo = c.take<uint16_t>(G * dm->batch * np);
     }
   }
   e.total = c.off;
@@ -384,7 +401,8 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
 
   if (rule == IPTTT_RULE_MSE) {
     void* R = ws + lay.r;
-    if (bf16) IPTTT_CUDA(launch_split_w(W0, w0s, hi, lo, batch, nw, st));
+    const Planes w = planes_of(dm, hi, lo, batch, 1, 0);
+    if (bf16) IPTTT_CUDA(launch_split_planes(W0, w0s, w, dff, d, st));
     IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * B * d, st));
     const int64_t w0_rows = (dm->w0_per_seq ? batch : 1) * dff;
     for (int64_t k = 0; k < K; ++k) {
@@ -395,9 +413,11 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       a.K = dff;
       a.nb1 = bint;
       a.A = mat(Z, batch * L, dff, 0, k * B, L);
-      if (bf16)
+      if (bf16) {
         a.B = mat(hi, batch * dff, d, 1, 0, dff);
-      else
+        a.w = w;
+        a.b_planes = 1;
+      } else
         a.B = (k == 0) ? mat(W0, w0_rows, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
       a.epi = EPI_ACCUM;
       a.kind = K_APPLY;
@@ -427,8 +447,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.epi = EPI_AXPY;
       u.kind = K_UPDATE;
       if (bf16) {
-        u.D = u.src = out(hi, d, 0, dff, 0, batch * dff);
-        u.D_lo = u.src_lo = out(lo, d, 0, dff, 0, batch * dff);
+        u.w = w;
       } else {
         u.D = out(Wf, d, 0, dff, 0, batch * dff);
         u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r, 0, w0_rows) : out(Wf, d, 0, dff, 0, batch * dff);
@@ -436,7 +455,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.alpha = -eta / static_cast<float>(B);
       IPTTT_CUDA(gemm(u, bf16, st));
     }
-    if (bf16) IPTTT_CUDA(launch_merge_w(hi, lo, Wf, batch * nw, st));
+    if (bf16) IPTTT_CUDA(launch_merge_planes(w, Wf, dff, d, st));
     return IPTTT_OK;
   }
 
@@ -460,7 +479,11 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   s.D = out(D, d, 0, dff, batch * dff);
   IPTTT_CUDA(gemm(s, bf16, st));
   // exclusive scan over groups -> the fast weight at the start of each group
-  IPTTT_CUDA(launch_group_scan(D, hi, lo, W0, w0s, Wf, G, batch, nw, alpha, st));
+  const Planes w = planes_of(dm, hi, lo, G * batch, 1, batch);
+  if (bf16)
+    IPTTT_CUDA(launch_group_scan_planes(D, w, W0, w0s, Wf, G, batch, dff, d, alpha, st));
+  else
+    IPTTT_CUDA(launch_group_scan(D, W0, w0s, Wf, G, batch, nw, alpha, st));
   IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * G * batch * B * d, st));
   for (int64_t i = 0; i < g; ++i) {
     GemmProblem a;
@@ -471,6 +494,10 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     a.nb2 = gint;
     a.A = mat(Z, batch * L, dff, 0, i * B, L, g * B);
     a.B = bf16 ? mat(hi, G * batch * dff, d, 1, 0, dff, batch * dff) : mat(D, G * batch * dff, d, 1, 0, dff, batch * dff);
+    if (bf16) {
+      a.w = w;
+      a.b_planes = 1;
+    }
     a.epi = EPI_ACCUM;
     a.kind = K_APPLY;
     a.D = out(o_acc, d, 0, B, batch * B, G * batch * B);
@@ -501,8 +528,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.epi = EPI_AXPY;
       u.kind = K_UPDATE;
       if (bf16) {
-        u.D = u.src = out(hi, d, 0, dff, batch * dff, G * batch * dff);
-        u.D_lo = u.src_lo = out(lo, d, 0, dff, batch * dff, G * batch * dff);
+        u.w = w;
       } else {
         u.D = u.src = out(D, d, 0, dff, batch * dff, G * batch * dff);
       }

@@ -188,36 +188,79 @@ __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs
 }
 
 // -------------------------------------------------------------- fast weight
-// W0[s or 0] (fp32) -> its split planes hi[s], lo[s] (split_w) for s < batch.
-__global__ void __launch_bounds__(kThreads) split_w_kernel(const float* __restrict__ W0, int64_t w0_stride,
-                                                           uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
-                                                           int64_t batch, int64_t n) {
-  const int64_t nq = n / 4;
-  const int64_t total = nq * batch;
+// The fast weight as tile-major split planes (split_w / plane_index in
+// common.cuh).  One work item: 8 consecutive columns of one row of one block
+// (16 bytes of each plane); the planes' padding holds zeros.
+struct PlaneItem {
+  int64_t rbe;  // row block, counted over all entries
+  int64_t e;    // entry
+  int64_t r;    // row of the entry's matrix
+  int64_t c;    // first of 8 columns
+  int64_t cb;   // column block
+  int row;      // row inside the block
+  int half;     // 0: columns 0..7 of the block, 1: 8..15
+};
+__device__ __forceinline__ PlaneItem plane_item(int64_t idx, int64_t RB, int64_t CB) {
+  PlaneItem it;
+  it.half = static_cast<int>(idx & 1);
+  it.row = static_cast<int>((idx >> 1) & (kPlaneRows - 1));
+  const int64_t blk = idx >> 8;
+  it.cb = blk % CB;
+  it.rbe = blk / CB;
+  it.e = it.rbe / RB;
+  it.r = (it.rbe % RB) * kPlaneRows + it.row;
+  it.c = it.cb * kPlaneCols + it.half * 8;
+  return it;
+}
+__device__ __forceinline__ void store_split8(uint16_t* hi, uint16_t* lo, const PlaneItem& it, int64_t CB,
+                                             const float (&w)[8]) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) split_w2(w[2 * q], w[2 * q + 1], h[q], l[q]);
+  const int64_t at = plane_index(it.rbe, it.cb, CB, it.row, it.half * 8);
+  *reinterpret_cast<uint4*>(hi + at) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + at) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// W0[e or 0] (fp32, R x C row-major) -> the planes of `entries` entries.
+__global__ void __launch_bounds__(kThreads) split_planes_kernel(const float* __restrict__ W0, int64_t w0_stride,
+                                                                uint16_t* __restrict__ hi, uint16_t* __restrict__ lo,
+                                                                int64_t entries, int64_t R, int64_t C, int64_t RB,
+                                                                int64_t CB) {
+  const int64_t total = entries * RB * CB * kPlaneRows * 2;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t s = idx / nq, q = idx % nq;
-    const float4 x = reinterpret_cast<const float4*>(W0 + s * w0_stride)[q];
-    uint32_t h[4], l[4];
-    split_w(x.x, h[0], l[0]);
-    split_w(x.y, h[1], l[1]);
-    split_w(x.z, h[2], l[2]);
-    split_w(x.w, h[3], l[3]);
-    reinterpret_cast<uint2*>(hi + s * n)[q] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-    reinterpret_cast<uint2*>(lo + s * n)[q] = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+    const PlaneItem it = plane_item(idx, RB, CB);
+    float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (it.r < R && it.c < C) {
+      const float4* src = reinterpret_cast<const float4*>(W0 + it.e * w0_stride + it.r * C + it.c);
+      const float4 a = src[0], b = src[1];
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+    store_split8(hi, lo, it, CB, w);
   }
 }
 
-// W = join_w(hi, lo), element-wise over `total` (a multiple of 4) elements.
-__global__ void __launch_bounds__(kThreads) merge_w_kernel(const uint16_t* __restrict__ hi,
-                                                           const uint16_t* __restrict__ lo, float* __restrict__ W,
-                                                           int64_t total) {
-  const int64_t nq = total / 4;
-  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < nq;
-       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint2 h = reinterpret_cast<const uint2*>(hi)[q], l = reinterpret_cast<const uint2*>(lo)[q];
-    reinterpret_cast<float4*>(W)[q] = make_float4(join_w(h.x & 0xFFFFu, l.x & 0xFFFFu), join_w(h.x >> 16, l.x >> 16),
-                                                  join_w(h.y & 0xFFFFu, l.y & 0xFFFFu), join_w(h.y >> 16, l.y >> 16));
+// The planes of `entries` entries -> W (fp32, entries x R x C row-major).
+__global__ void __launch_bounds__(kThreads) merge_planes_kernel(const uint16_t* __restrict__ hi,
+                                                                const uint16_t* __restrict__ lo,
+                                                                float* __restrict__ W, int64_t entries, int64_t R,
+                                                                int64_t C, int64_t RB, int64_t CB) {
+  const int64_t total = entries * RB * CB * kPlaneRows * 2;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const PlaneItem it = plane_item(idx, RB, CB);
+    if (it.r >= R || it.c >= C) continue;
+    const int64_t at = plane_index(it.rbe, it.cb, CB, it.row, it.half * 8);
+    const uint4 h = *reinterpret_cast<const uint4*>(hi + at), l = *reinterpret_cast<const uint4*>(lo + at);
+    const uint32_t hv[4] = {h.x, h.y, h.z, h.w}, lv[4] = {l.x, l.y, l.z, l.w};
+    float w[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) join_w2(hv[q], lv[q], w[2 * q], w[2 * q + 1]);
+    float4* dst = reinterpret_cast<float4*>(W + (it.e * R + it.r) * C + it.c);
+    dst[0] = make_float4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_float4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -231,11 +274,9 @@ __global__ void __launch_bounds__(kThreads) copy_w_kernel(const float* __restric
   }
 }
 
-// Exclusive prefix over the G group sums of the additive rule, turning each
-// sum into the fast weight at the start of its group: in place in fp32, or
-// (hi != nullptr) into the split planes hi[g], lo[g].
-__global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict__ D, uint16_t* __restrict__ hi,
-                                                              uint16_t* __restrict__ lo, const float* __restrict__ W0,
+// Exclusive prefix over the G group sums of the additive rule (fp32 mode),
+// turning each sum, in place, into the fast weight at the start of its group.
+__global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict__ D, const float* __restrict__ W0,
                                                               int64_t w0_stride, float* __restrict__ Wf, int64_t G,
                                                               int64_t batch, int64_t n, float alpha) {
   const int64_t total = n * batch;
@@ -246,17 +287,54 @@ __global__ void __launch_bounds__(kThreads) group_scan_kernel(float* __restrict_
     for (int64_t g = 0; g < G; ++g) {
       const int64_t at = g * total + idx;
       const float t = D[at];
-      if (hi) {
-        uint32_t h, l;
-        split_w(S, h, l);
-        hi[at] = static_cast<uint16_t>(h);
-        lo[at] = static_cast<uint16_t>(l);
-      } else {
-        D[at] = S;
-      }
+      D[at] = S;
       S = fmaf(alpha, t, S);
     }
     Wf[idx] = S;
+  }
+}
+
+// The group scan of the additive rule writing the group starting weights as
+// planes: S = W0; for g: state[g*batch + b] = S; S += alpha * D[g]; W_final = S.
+// D is fp32 [G][batch][R][C] row-major; the planes have G*batch entries.
+__global__ void __launch_bounds__(kThreads) group_scan_planes_kernel(const float* __restrict__ D,
+                                                                     uint16_t* __restrict__ hi,
+                                                                     uint16_t* __restrict__ lo,
+                                                                     const float* __restrict__ W0, int64_t w0_stride,
+                                                                     float* __restrict__ Wf, int64_t G, int64_t batch,
+                                                                     int64_t R, int64_t C, int64_t RB, int64_t CB,
+                                                                     float alpha) {
+  const int64_t per_entry = RB * CB * kPlaneRows * 2;
+  const int64_t total = batch * per_entry;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const PlaneItem it = plane_item(idx, RB, CB);  // it.e = sequence b
+    const bool valid = it.r < R && it.c < C;
+    float S[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+      const float4* w0 = reinterpret_cast<const float4*>(W0 + it.e * w0_stride + it.r * C + it.c);
+      const float4 a = w0[0], b = w0[1];
+      S[0] = a.x; S[1] = a.y; S[2] = a.z; S[3] = a.w;
+      S[4] = b.x; S[5] = b.y; S[6] = b.z; S[7] = b.w;
+    }
+    for (int64_t g = 0; g < G; ++g) {
+      PlaneItem ig = it;
+      ig.rbe = (g * batch + it.e) * RB + it.rbe % RB;
+      store_split8(hi, lo, ig, CB, S);
+      if (valid) {
+        const float4* t = reinterpret_cast<const float4*>(D + ((g * batch + it.e) * R + it.r) * C + it.c);
+        const float4 a = t[0], b = t[1];
+        S[0] = fmaf(alpha, a.x, S[0]); S[1] = fmaf(alpha, a.y, S[1]);
+        S[2] = fmaf(alpha, a.z, S[2]); S[3] = fmaf(alpha, a.w, S[3]);
+        S[4] = fmaf(alpha, b.x, S[4]); S[5] = fmaf(alpha, b.y, S[5]);
+        S[6] = fmaf(alpha, b.z, S[6]); S[7] = fmaf(alpha, b.w, S[7]);
+      }
+    }
+    if (valid) {
+      float4* dst = reinterpret_cast<float4*>(Wf + (it.e * R + it.r) * C + it.c);
+      dst[0] = make_float4(S[0], S[1], S[2], S[3]);
+      dst[1] = make_float4(S[4], S[5], S[6], S[7]);
+    }
   }
 }
 
@@ -295,18 +373,20 @@ cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t strea
   return cudaGetLastError();
 }
 
-cudaError_t launch_split_w(const float* W0, int64_t w0_stride, uint16_t* hi, uint16_t* lo, int64_t batch, int64_t n,
-                           cudaStream_t stream) {
-  if (n % 4) return cudaErrorInvalidValue;
+cudaError_t launch_split_planes(const float* W0, int64_t w0_stride, const Planes& w, int64_t R, int64_t C,
+                                cudaStream_t stream) {
+  if (C % 8) return cudaErrorInvalidValue;
   LaunchMark mark(K_WEIGHT, stream);
-  split_w_kernel<<<grid_for(n / 4 * batch), kThreads, 0, stream>>>(W0, w0_stride, hi, lo, batch, n);
+  split_planes_kernel<<<grid_for(w.entries * w.rb * w.cb * kPlaneRows * 2), kThreads, 0, stream>>>(
+      W0, w0_stride, w.hi, w.lo, w.entries, R, C, w.rb, w.cb);
   return cudaGetLastError();
 }
 
-cudaError_t launch_merge_w(const uint16_t* hi, const uint16_t* lo, float* W, int64_t total, cudaStream_t stream) {
-  if (total % 4) return cudaErrorInvalidValue;
+cudaError_t launch_merge_planes(const Planes& w, float* W, int64_t R, int64_t C, cudaStream_t stream) {
+  if (C % 8) return cudaErrorInvalidValue;
   LaunchMark mark(K_WEIGHT, stream);
-  merge_w_kernel<<<grid_for(total / 4), kThreads, 0, stream>>>(hi, lo, W, total);
+  merge_planes_kernel<<<grid_for(w.entries * w.rb * w.cb * kPlaneRows * 2), kThreads, 0, stream>>>(
+      w.hi, w.lo, W, w.entries, R, C, w.rb, w.cb);
   return cudaGetLastError();
 }
 
@@ -317,11 +397,20 @@ cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_group_scan(float* D, uint16_t* hi, uint16_t* lo, const float* W0, int64_t w0_stride,
-                              float* W_final, int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream) {
+cudaError_t launch_group_scan(float* D, const float* W0, int64_t w0_stride, float* W_final, int64_t G,
+                              int64_t batch, int64_t n, float alpha, cudaStream_t stream) {
   LaunchMark mark(K_SCAN, stream);
-  group_scan_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(D, hi, lo, W0, w0_stride, W_final, G, batch, n,
-                                                                  alpha);
+  group_scan_kernel<<<grid_for(n * batch), kThreads, 0, stream>>>(D, W0, w0_stride, W_final, G, batch, n, alpha);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_scan_planes(const float* D, const Planes& w, const float* W0, int64_t w0_stride,
+                                     float* W_final, int64_t G, int64_t batch, int64_t R, int64_t C, float alpha,
+                                     cudaStream_t stream) {
+  if (C % 8) return cudaErrorInvalidValue;
+  LaunchMark mark(K_SCAN, stream);
+  group_scan_planes_kernel<<<grid_for(batch * w.rb * w.cb * kPlaneRows * 2), kThreads, 0, stream>>>(
+      D, w.hi, w.lo, W0, w0_stride, W_final, G, batch, R, C, w.rb, w.cb, alpha);
   return cudaGetLastError();
 }
 

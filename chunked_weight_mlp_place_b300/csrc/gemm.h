@@ -36,16 +36,42 @@ struct OutRef {
   int64_t rows = 0;                  // rows of the whole matrix (needed where TMA reads or writes it)
 };
 
+// The planes are stored tile-major: blocks of kPlaneRows rows x kPlaneCols
+// columns, each block 4 KB contiguous (row r of a block at r * 32 bytes), the
+// blocks of one row of blocks side by side, rows of blocks one after another,
+// sequences (or groups) one after another; the matrix is padded with zeros to
+// whole blocks.  A warp finishing 32 rows of one 16-column chunk then reads
+// and writes 1 KB contiguous, and TMA reads the hi plane as an MN-major
+// operand with the 32-byte swizzle.
+constexpr int kPlaneRows = 128, kPlaneCols = 16, kPlaneBlock = kPlaneRows * kPlaneCols;
+__host__ __device__ __forceinline__ int64_t plane_index(int64_t rb_row, int64_t cb, int64_t nblk_cols, int r, int c) {
+  return (rb_row * nblk_cols + cb) * kPlaneBlock + r * kPlaneCols + c;
+}
+
+// A fast weight (one d_ff x d matrix per entry) as tile-major split planes.
+// Entry e = b1*es1 + b2*es2 owns row blocks e*rb .. e*rb + rb - 1.
+struct Planes {
+  uint16_t* hi = nullptr;
+  uint16_t* lo = nullptr;
+  int64_t rb = 0;   // 128-row blocks per entry
+  int64_t cb = 0;   // 16-column blocks per row of blocks
+  int64_t es1 = 0, es2 = 0;
+  int64_t entries = 0;
+};
+
 struct GemmProblem {
   int64_t M = 0, N = 0, K = 0;
   int nb1 = 1, nb2 = 1;
   Operand A, B, B2;
   int epi = EPI_STORE;
   int out_bf16 = 0;  // element type of D for STORE / GATE
-  OutRef D;          // primary output (AXPY on the tensor cores: the hi plane)
-  OutRef src;        // AXPY: source (may equal D); fp32, or the hi plane on the tensor cores
-  OutRef D_lo;       // AXPY on the tensor cores: lo planes of D and src (16-bit, same layout
-  OutRef src_lo;     //   as the hi planes; see split_w in common.cuh)
+  OutRef D;          // primary output (CUDA-core AXPY: fp32 W)
+  OutRef src;        // CUDA-core AXPY: fp32 source (may equal D)
+  // Tensor-core AXPY: the fast weight's tile-major hi/lo planes (split_w, plane_index in
+  // common.cuh), read and rewritten in place.  Tensor-core ACCUM with b_planes: its B
+  // operand is w.hi.
+  Planes w;
+  int b_planes = 0;
   float alpha = 1.0f;
   int split_k = 0;   // tensor-core path: 1 = balance (tile, k-block) work over CTAs (needs EPI_ACCUM)
   int kind = 0;      // KernelKind label (launch counting / timing)

@@ -5,8 +5,9 @@
 //   proj   V = C P                          A = C   (K-major)  B = P           (MN-major)
 //   apply  O_k = Z_k W_k  (split over K)    A = Z_k (K-major)  B = hi plane    (MN-major)
 //   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k         (MN-major)
-// (the fast weight W is kept as split hi/lo 16-bit planes, common.cuh::split_w;
-// its hi plane is the bf16 operand of the apply).
+// (the fast weight W is kept as split hi/lo 16-bit planes, common.cuh::split_w,
+// stored tile-major in blocks of 128 rows x 16 columns, gemm.h::plane_index;
+// the hi plane is the bf16 operand of the apply, read through a 4-D TMA map).
 //
 // Problems with more than one 128-row tile run on CTA pairs (clusters of 2,
 // tcgen05 cta_group::2): one 256 x N MMA per pair, each CTA holding 128 rows
@@ -15,30 +16,26 @@
 //
 // Each CTA (one per SM) runs these warps:
 //   warp 0      TMA producer: 128x64 A tiles and 64-wide B tiles into a ring of
-//               shared-memory stages (128-byte swizzle), completion on mbarriers;
+//               shared-memory stages (128-byte swizzle; 32-byte for plane
+//               blocks), completion on mbarriers;
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128 or 256 per pair,
 //               N=256, K=16) into a TMEM accumulator; tcgen05.commit frees each stage;
 //   warps 2..   epilogue (4 warps; 8 for the update, two groups taking alternate
 //               16-column chunks): tcgen05.ld the accumulator (one TMEM lane per
-//               output row) and apply the fused epilogue;
-//   last warp   (update only) fast-weight loader: streams the hi and lo planes of
-//               the tile the epilogue read-modify-writes into swizzled shared-
-//               memory slots ahead of time.
+//               output row) and apply the fused epilogue.
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next.  Work is either whole output tiles, strided over
 // the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
 // share of the (tile, k-block) iteration space per CTA.
 //
-// Epilogues that move much data go through shared memory and TMA, so global
-// memory sees whole 128-byte lines instead of one row per lane:
+// The two epilogues that move much data keep global accesses whole lines:
 //   apply (split mode)  the epilogue stages the tile's 128 rows x 32 columns of
 //                       fp32 partial sums and adds them into the fp32 sums in L2
 //                       with one TMA reduce (the residual kernel then turns the
 //                       sums into O and R = O - V);
-//   update              a group computes W + alpha*acc on the planes of one
-//                       16-column chunk from its slot, stages the new planes for
-//                       the whole tile and stores them with two TMA stores; the
-//                       slot goes back to the loader once the group has read it.
+//   update              no staging: a plane block's row is 32 contiguous bytes,
+//                       so each thread reads and writes its row of the hi and lo
+//                       planes directly and a warp moves 1 KB contiguous.
 //
 // Every mbarrier wait is capped (common.cuh); a CTA whose wait runs out flags
 // the others, drains its in-flight TMA copies and MMAs, frees its TMEM and
@@ -53,8 +50,7 @@ namespace ipttt {
 
 // Error word written by kernels whose capped waits ran out (0 = none); read
 // and cleared through read_clear_device_error().  Codes: 1 = TMA-producer
-// wait, 2 = MMA-issuer wait, 3 = epilogue wait, 4 = teardown drain,
-// 5 = fast-weight loader wait.
+// wait, 2 = MMA-issuer wait, 3 = epilogue wait, 4 = teardown drain.
 __device__ int g_device_error = 0;
 
 namespace tc {
@@ -66,38 +62,29 @@ constexpr int kAccStride = 256;  // TMEM columns between the two accumulator buf
 
 template <int BN, int NB, int EPI, bool PAIR>
 struct Cfg {
-  static constexpr bool W_LOAD = (EPI == EPI_AXPY);
+  static constexpr bool W_UPD = (EPI == EPI_AXPY);  // update epilogue on the tile-major planes
   static constexpr bool RED = (EPI == EPI_ACCUM);
   // update: two groups of four epilogue warps take alternate 16-column chunks
-  static constexpr int EPI_WARPS = W_LOAD ? 8 : 4;
-  static constexpr int THREADS = 64 + 32 * EPI_WARPS + (W_LOAD ? 32 : 0);
+  static constexpr int EPI_WARPS = W_UPD ? 8 : 4;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int N_MMA = BN * NB;          // the B operands sit side by side: one MMA covers them
   static constexpr int M_MMA = PAIR ? 2 * BM : BM;
   static constexpr int B_COLS = PAIR ? N_MMA / 2 : N_MMA;  // B columns held by one CTA per stage
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_COLS * BK * 2;
-  // update: the fast weight's hi and lo planes stream through slots of 128 rows x
-  // 16 columns each (two 32-byte-row tiles, 4 KB apart)
-  static constexpr int WC = 16;
-  static constexpr int W_SLOT_BYTES = 2 * BM * WC * 2;
-  static constexpr int W_SLOTS = W_LOAD ? 8 : 0;
-  // staging buffers of the whole tile (128 rows) for TMA stores / reductions, per group:
-  //   apply: 2 of 128 rows x 32 fp32 (128-byte rows);
-  //   update: 2 of [hi plane | lo plane], 128 rows x 16 x 16-bit each (32-byte rows)
-  static constexpr int STG_BYTES = RED ? BM * 32 * 4 : (W_LOAD ? 2 * BM * WC * 2 : 0);
-  static constexpr int STG_BUFS = 2;
-  static constexpr int STG_TOTAL = (EPI_WARPS / 4) * STG_BUFS * STG_BYTES;
-  static constexpr int STAGES = PAIR ? (W_LOAD ? 4 : 6) : (W_LOAD ? 2 : 4);
+  // apply: two staging buffers of the tile's 128 rows x 32 fp32 for the TMA reductions
+  static constexpr int STG_BYTES = RED ? BM * 32 * 4 : 0;
+  static constexpr int STG_TOTAL = 2 * STG_BYTES;
+  static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int BAR_BYTES = 512;
-  static constexpr int SMEM_BYTES =
-      1024 + STAGES * STAGE_BYTES + W_SLOTS * W_SLOT_BYTES + STG_TOTAL + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_TOTAL + BAR_BYTES;
   static_assert(N_MMA <= kAccStride && N_MMA % 16 == 0, "accumulator width");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(B_COLS % 64 == 0, "B columns per CTA: whole 64-column swizzle atoms");
   static_assert(!PAIR || NB == 1 || BN == B_COLS, "pair: a second B operand is the peer's half");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-  static_assert(STAGE_BYTES % 1024 == 0 && W_SLOT_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0,
-                "1024-byte aligned swizzle atoms");
+  static_assert(STAGE_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0, "1024-byte aligned swizzle atoms");
+  static_assert(!W_UPD || BM == kPlaneRows, "an update tile is one row of plane blocks");
 };
 
 struct Seg {
@@ -205,15 +192,34 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
   }
 }
 
+// The B operand read from tile-major hi planes (an MN-major operand, K = rows of
+// the weight): one 4-D box of 16 columns x BK rows x EXT/16 column blocks lands
+// as EXT/16 blocks of BK rows of 32 bytes, the 32-byte-swizzle MN-major layout.
+template <int EXT, bool PAIR>
+__device__ __forceinline__ void load_plane_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                                   uint32_t bar_cl, int64_t rb0, int64_t n0, int64_t k0) {
+  const int c1 = static_cast<int>(k0 % kPlaneRows), c2 = static_cast<int>(n0 / kPlaneCols);
+  const int c3 = static_cast<int>(rb0 + k0 / kPlaneRows);
+  if constexpr (PAIR)
+    tma_load_4d_pair(dst, map, bar_cl, 0, c1, c2, c3);
+  else
+    tma_load_4d(dst, map, bar, 0, c1, c2, c3);
+}
+
 // Shared-memory descriptor of the k-th 16-wide K step of an operand tile.
 //  K-major: rows of 128 bytes (64 K elements), 8-row groups 1024 bytes apart;
 //           the K step advances the start by 32 bytes inside the swizzle atom.
 //  MN-major: 64-element column blocks of 64 K rows (8 KB) side by side; 8-row
 //           K groups 1024 bytes apart (SBO), column blocks 8 KB apart (LBO);
 //           the K step advances the start by 16 rows = 2048 bytes.
-template <bool MN>
+//  plane (MN-major, 32-byte swizzle): 16-element column blocks of 64 K rows
+//           (2 KB) side by side (LBO); 8-row K groups 256 bytes apart (SBO);
+//           the K step advances the start by 16 rows = 512 bytes.
+template <bool MN, bool PLANE = false>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kstep) {
-  if constexpr (MN)
+  if constexpr (PLANE)
+    return make_smem_desc(base + kstep * 512, BK * 32, 256, kLayoutSw32);
+  else if constexpr (MN)
     return make_smem_desc_sw128(base + kstep * 2048, 64 * BK * 2, 1024);
   else
     return make_smem_desc_sw128(base + kstep * 32, 16, 1024);
@@ -275,30 +281,26 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
   }
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR, bool B_PL>
 __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmS,
-                   const __grid_constant__ CUtensorMap tmSl, const __grid_constant__ CUtensorMap tmD,
-                   const __grid_constant__ CUtensorMap tmDl,
+                   const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ KParams kp) {
   using C = Cfg<BN, NB, EPI, PAIR>;
   static_assert(!PAIR || B_MN, "pairs split an MN-major B operand by columns");
+  static_assert(!B_PL || (B_MN && NB == 1), "a plane B operand is MN-major and single");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
   uint8_t* stages = smem;
-  uint8_t* wslots = smem + C::STAGES * C::STAGE_BYTES;
-  uint8_t* stg = wslots + C::W_SLOTS * C::W_SLOT_BYTES;
+  uint8_t* stg = smem + C::STAGES * C::STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + C::STG_TOTAL);
   uint64_t* full_bar = bars;                        // [STAGES]
   uint64_t* empty_bar = bars + C::STAGES;           // [STAGES]
   uint64_t* tfull_bar = bars + 2 * C::STAGES;       // [2]
   uint64_t* tempty_bar = bars + 2 * C::STAGES + 2;  // [2]
   uint64_t* drain_bar = bars + 2 * C::STAGES + 4;   // [1]
-  uint64_t* wfull_bar = bars + 2 * C::STAGES + 5;   // [W_SLOTS]
-  uint64_t* wempty_bar = wfull_bar + C::W_SLOTS;    // [W_SLOTS]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wempty_bar + C::W_SLOTS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const GemmProblem& p = kp.p;
@@ -316,24 +318,15 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&tfull_bar[i], 1);
-        mbar_init(&tempty_bar[i], (PAIR ? 2 : 1) * C::EPI_WARPS);  // one per epilogue warp (of both CTAs)
+        mbar_init(&tempty_bar[i], (PAIR ? 2 : 1) * C::EPI_WARPS);  // one arrival per epilogue warp (of both CTAs)
       }
       mbar_init(drain_bar, 1);
-      for (int i = 0; i < C::W_SLOTS; ++i) {
-        mbar_init(&wfull_bar[i], 1);
-        mbar_init(&wempty_bar[i], 1);  // the epilogue's store issuer, after all four warps read the slot
-      }
       *abort_flag = 0;
       fence_mbarrier_init();
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       if constexpr (NB == 2) tma_prefetch_desc(&tmB2);
-      if constexpr (C::W_LOAD) {
-        tma_prefetch_desc(&tmS);
-        tma_prefetch_desc(&tmSl);
-        tma_prefetch_desc(&tmDl);
-      }
-      if constexpr (C::W_LOAD || C::RED) tma_prefetch_desc(&tmD);
+      if constexpr (C::RED) tma_prefetch_desc(&tmD);
     }
     __syncwarp();
     if constexpr (PAIR) {
@@ -372,6 +365,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         if constexpr (PAIR) mt = 2 * mt + rank;
         const int b1 = bi % p.nb1, b2 = bi / p.nb1;
         const int64_t ra = row_of(p.A, b1, b2), rb = row_of(p.B, b1, b2), rb2 = row_of(p.B2, b1, b2);
+        const int64_t pb0 = (b1 * p.w.es1 + b2 * p.w.es2) * p.w.rb;  // plane B operand: first row block
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++kc) {
           const uint32_t st = kc % C::STAGES, ph = (kc / C::STAGES) & 1;
           if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1, abort_flag, 1, &g_device_error)) {
@@ -386,7 +380,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           issued_mask |= 1u << st;
           const int64_t k0 = static_cast<int64_t>(kb) * BK;
           load_operand<A_MN, BM, PAIR>(sa, &tmA, &full_bar[st], bar_cl, ra, mt * BM, k0);
-          if constexpr (PAIR && NB == 2) {
+          if constexpr (B_PL) {
+            load_plane_operand<C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, pb0,
+                                                nt * BN + rank * C::B_COLS, k0);
+          } else if constexpr (PAIR && NB == 2) {
             // the even CTA holds the first B operand, its peer the second
             if (rank == 0)
               load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN, k0);
@@ -440,10 +437,11 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           const int ksteps = static_cast<int>(min(static_cast<int64_t>(BK / 16), (krem + 15) / 16));
           for (int ks = 0; ks < ksteps; ++ks) {
             const uint32_t accum = (kb > seg.kb0 || ks > 0) ? 1u : 0u;
+            const uint64_t ad = operand_desc<A_MN>(sa, ks), bd = operand_desc<B_MN, B_PL>(sb, ks);
             if constexpr (PAIR)
-              umma_bf16_pair(d_tmem, operand_desc<A_MN>(sa, ks), operand_desc<B_MN>(sb, ks), idesc, accum);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
             else
-              umma_bf16(d_tmem, operand_desc<A_MN>(sa, ks), operand_desc<B_MN>(sb, ks), idesc, accum);
+              umma_bf16(d_tmem, ad, bd, idesc, accum);
           }
           if constexpr (PAIR)
             umma_commit_pair_both(&empty_bar[st]);
@@ -464,113 +462,141 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         umma_commit(drain_bar);
       mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
     }
-  } else if (warp < 2 + C::EPI_WARPS) {
+  } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp % 4;          // TMEM lanes 32*quarter .. +31 belong to this warp
-    const int group = (warp - 2) / 4;      // update: chunks c with c % 2 == group
     const int trow = quarter * 32 + lane;  // row of the tile this thread finishes
-    const bool issuer = (trow == 0);       // issues the group's tile-wide TMA stores / reductions
-    uint64_t pol = 0;
-    if constexpr (C::W_LOAD) pol = l2_policy_evict_first();
-    uint32_t ls = 0, sc = 0;
-    // The four warps meet at a named barrier once per stored chunk, so none may leave the
-    // loops early: a warp whose wait ran out (failed) skips the waits and the work from then
-    // on but still walks every tile and chunk, and the CTA ends with the others.
+    const bool issuer = (trow == 0);       // apply: issues the tile-wide TMA reductions
+    // A warp whose wait ran out (failed) skips the waits and the work from then on but
+    // still walks every tile and chunk, so the apply's named barriers always fill up.
     bool failed = false;
-    while (iter.next(seg)) {
-      const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
-      // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
-      if (!failed)
-        failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error));
-      tc_fence_after();
-      int bi;
-      int64_t mt, nt;
-      kp.s.tile_coords(seg.tile, bi, mt, nt);
-      if constexpr (PAIR) mt = 2 * mt + rank;
-      const int b1 = bi % p.nb1, b2 = bi / p.nb1;
-      const int64_t m = mt * BM + trow;
-      // the tile goes through tile-wide TMA boxes only if all its 128 rows are rows of the problem
-      const bool box_rows = (mt * BM + BM <= p.M);
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
-      if constexpr (C::W_LOAD) {
-        // ---- update: W = src + alpha * acc on the split planes (split_w): the slot holds this
-        // chunk's hi and lo planes; the result goes through the group's staging buffer and two
-        // tile-wide TMA stores.
-        const int yD = static_cast<int>(row_of(p.D, b1, b2) + mt * BM);
-        constexpr int NCH = BN / C::WC;
-        static_assert(NCH % 4 == 0, "each group takes pairs of chunks");
-        const uint32_t chunk0 = ls * NCH;  // this CTA's running index of the tile's first chunk
-        // One chunk of WC columns.  The slot goes back to the loader once the group's four warps
-        // have read it; the group's stores stay in flight for one more chunk of the group, so
-        // a staging buffer is rewritten only after the stores issued from it have read it.
-        auto chunk = [&](int c, const uint32_t(&r)[C::WC]) {
-          const uint32_t gch = chunk0 + c;
-          const uint32_t slot = gch % C::W_SLOTS, wph = (gch / C::W_SLOTS) & 1;
-          if (!failed)
-            failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&wfull_bar[slot], wph, abort_flag, 3, &g_device_error));
-          // 32-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t >> 2) & 1)
-          const int sw = (trow >> 2) & 1;
-          const uint4* hrow = reinterpret_cast<const uint4*>(wslots + slot * C::W_SLOT_BYTES + trow * 32);
-          const uint4* lrow = reinterpret_cast<const uint4*>(wslots + slot * C::W_SLOT_BYTES + BM * 32 + trow * 32);
-          const uint4 h0 = hrow[0 ^ sw], h1 = hrow[1 ^ sw], l0 = lrow[0 ^ sw], l1 = lrow[1 ^ sw];
-          const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-          const uint32_t lw[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-          uint32_t ho[8], lo[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            float w0, w1;
-            join_w2(hw[q], lw[q], w0, w1);
-            split_w2(fmaf(p.alpha, __uint_as_float(r[2 * q]), w0), fmaf(p.alpha, __uint_as_float(r[2 * q + 1]), w1),
-                     ho[q], lo[q]);
-          }
-          const int64_t n = nt * BN + c * C::WC;
-          const uint32_t lc = ls * (NCH / 2) + c / 2;  // the group's running chunk count
-          uint8_t* sbuf = stg + (group * C::STG_BUFS + lc % C::STG_BUFS) * C::STG_BYTES;
-          if (failed) {
-            // nothing to store
-          } else if (box_rows) {
-            uint4* hs = reinterpret_cast<uint4*>(sbuf + trow * 32);
-            uint4* lsb = reinterpret_cast<uint4*>(sbuf + BM * 32 + trow * 32);
-            hs[0 ^ sw] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-            hs[1 ^ sw] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
-            lsb[0 ^ sw] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            lsb[1 ^ sw] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-          } else if (m < p.M) {
-            uint16_t* dh = static_cast<uint16_t*>(p.D.ptr) + (row_of(p.D, b1, b2) + m) * p.D.ld + n;
-            uint16_t* dl = static_cast<uint16_t*>(p.D_lo.ptr) + (row_of(p.D_lo, b1, b2) + m) * p.D_lo.ld + n;
-            for (int i = 0; i < C::WC && n + i < p.N; ++i) {
-              dh[i] = static_cast<uint16_t>(ho[i / 2] >> (16 * (i % 2)));
-              dl[i] = static_cast<uint16_t>(lo[i / 2] >> (16 * (i % 2)));
-            }
-          }
-          // The slot's reads and the staging writes before the async-proxy copies below.
-          fence_proxy_async_shared();
-          if (issuer) bulk_wait_group_read<C::STG_BUFS - 2>();  // the group's next buffer is free
-          epi_barrier(group);
-          if (issuer && !failed) {
-            mbar_arrive(&wempty_bar[slot]);
-            if (box_rows && n < p.N) {
-              tma_store_2d(&tmD, sbuf, static_cast<int>(n), yD);
-              tma_store_2d_hint(&tmDl, sbuf + BM * 32, static_cast<int>(n), yD, pol);
-            }
-            bulk_commit_group();
-          }
-        };
-        // The group's chunks are c = group, group + 2, ...; the accumulator columns of its next
-        // chunk load from TMEM while this one is finished.
-        uint32_t ra[C::WC], rb[C::WC];
-        tmem_ld_32x32b_x16(tbase + group * C::WC, ra);
+    uint32_t ls = 0;
+    if constexpr (C::W_UPD) {
+      // ---- update: W = W + alpha * acc on the tile-major split planes (split_w).  A tile's
+      // 128 rows are one row of plane blocks and its 16-column chunks are blocks, so thread
+      // `trow` owns 32 contiguous bytes of each plane per chunk and a warp reads and writes
+      // 1 KB contiguous.  Two groups of four warps take alternate chunks (group g the chunks
+      // c = g, g + 2, ...).  Each group loads the planes of its next three chunks ahead,
+      // across tile boundaries, and the accumulator columns of its next chunk from TMEM.
+      constexpr int WC = kPlaneCols;
+      constexpr int NCH = BN / WC;
+      constexpr int GCH = NCH / 2;  // chunks per group and tile
+      static_assert(GCH % 4 == 0, "each group's chunks come in fours");
+      const int group = (warp - 2) / 4;
+      struct TileW {
+        uint16_t* hi;  // this thread's row of the tile's first chunk block (nullptr: no rows here)
+        uint16_t* lo;
+        int64_t cb0;   // the tile's first column block
+      };
+      auto tile_w = [&](const Seg& t) {
+        TileW x{nullptr, nullptr, 0};
+        int bi;
+        int64_t mt, nt;
+        kp.s.tile_coords(t.tile, bi, mt, nt);
+        if constexpr (PAIR) mt = 2 * mt + rank;
+        if (mt * BM >= p.M) return x;  // a pair's second tile past the last row block
+        const int b1 = bi % p.nb1, b2 = bi / p.nb1;
+        const int64_t rbk = (b1 * p.w.es1 + b2 * p.w.es2) * p.w.rb + mt;
+        x.cb0 = nt * (BN / WC);
+        const int64_t off = plane_index(rbk, x.cb0, p.w.cb, trow, 0);
+        x.hi = p.w.hi + off;
+        x.lo = p.w.lo + off;
+        return x;
+      };
+      uint4 wh[4][2], wl[4][2];  // planes of the chunks in flight, indexed by chunk % 4
+      auto wload = [&](const TileW& t, int c, uint4 (&h)[2], uint4 (&l)[2]) {
+        if (t.hi == nullptr || t.cb0 + c >= p.w.cb) return;
+        const uint4* hp = reinterpret_cast<const uint4*>(t.hi + static_cast<int64_t>(c) * kPlaneBlock);
+        const uint4* lp = reinterpret_cast<const uint4*>(t.lo + static_cast<int64_t>(c) * kPlaneBlock);
+        h[0] = hp[0];
+        h[1] = hp[1];
+        l[0] = __ldcs(lp);
+        l[1] = __ldcs(lp + 1);
+      };
+      SegIter ahead = iter;
+      Seg cur, nxt;
+      bool have = ahead.next(cur);
+      TileW tw = have ? tile_w(cur) : TileW{nullptr, nullptr, 0};
+      wload(tw, group, wh[0], wl[0]);
+      wload(tw, group + 2, wh[1], wl[1]);
+      wload(tw, group + 4, wh[2], wl[2]);
+      while (have) {
+        const bool have_next = ahead.next(nxt);
+        const TileW tn = have_next ? tile_w(nxt) : TileW{nullptr, nullptr, 0};
+        const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
+        if (!failed)
+          failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error));
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
+        uint32_t ra[WC], rb[WC];
+        tmem_ld_32x32b_x16(tbase + group * WC, ra);
 #pragma unroll 1
-        for (int c = group; c < NCH; c += 4) {
-          tmem_wait_ld(ra);
-          tmem_ld_32x32b_x16(tbase + (c + 2) * C::WC, rb);
-          chunk(c, ra);
-          tmem_wait_ld(rb);
-          if (c + 4 < NCH) tmem_ld_32x32b_x16(tbase + (c + 4) * C::WC, ra);
-          chunk(c + 2, rb);
+        for (int j4 = 0; j4 < GCH; j4 += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j4 + u, c = group + 2 * j;
+            uint32_t(&r)[WC] = (u & 1) ? rb : ra;
+            uint32_t(&rn)[WC] = (u & 1) ? ra : rb;
+            tmem_wait_ld(r);
+            if (j + 1 < GCH) tmem_ld_32x32b_x16(tbase + (c + 2) * WC, rn);
+            const uint32_t hw[8] = {wh[u][0].x, wh[u][0].y, wh[u][0].z, wh[u][0].w,
+                                    wh[u][1].x, wh[u][1].y, wh[u][1].z, wh[u][1].w};
+            const uint32_t lw[8] = {wl[u][0].x, wl[u][0].y, wl[u][0].z, wl[u][0].w,
+                                    wl[u][1].x, wl[u][1].y, wl[u][1].z, wl[u][1].w};
+            // the planes of the group's chunk j + 3 go into the registers its chunk j - 1 used
+            if (j + 3 < GCH)
+              wload(tw, c + 6, wh[(u + 3) & 3], wl[(u + 3) & 3]);
+            else
+              wload(tn, c + 6 - NCH, wh[(u + 3) & 3], wl[(u + 3) & 3]);
+            uint32_t ho[8], lo[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float w0, w1;
+              join_w2(hw[q], lw[q], w0, w1);
+              split_w2(fmaf(p.alpha, __uint_as_float(r[2 * q]), w0), fmaf(p.alpha, __uint_as_float(r[2 * q + 1]), w1),
+                       ho[q], lo[q]);
+            }
+            if (!failed && tw.hi != nullptr && tw.cb0 + c < p.w.cb) {
+              uint4* hp = reinterpret_cast<uint4*>(tw.hi + static_cast<int64_t>(c) * kPlaneBlock);
+              uint4* lp = reinterpret_cast<uint4*>(tw.lo + static_cast<int64_t>(c) * kPlaneBlock);
+              hp[0] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+              hp[1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
+              __stcs(lp, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+              __stcs(lp + 1, make_uint4(lo[4], lo[5], lo[6], lo[7]));
+            }
+          }
         }
         tmem_wait_ld();
-      } else {
+        // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+          else
+            mbar_arrive(&tempty_bar[acc]);
+        }
+        ++ls;
+        have = have_next;
+        tw = tn;
+      }
+    } else {
+      uint32_t sc = 0;
+      while (iter.next(seg)) {
+        const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
+        // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
+        if (!failed)
+          failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error));
+        tc_fence_after();
+        int bi;
+        int64_t mt, nt;
+        kp.s.tile_coords(seg.tile, bi, mt, nt);
+        if constexpr (PAIR) mt = 2 * mt + rank;
+        const int b1 = bi % p.nb1, b2 = bi / p.nb1;
+        const int64_t m = mt * BM + trow;
+        // the tile goes through tile-wide TMA boxes only if all its 128 rows are rows of the problem
+        const bool box_rows = (mt * BM + BM <= p.M);
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32], u[32];
@@ -603,53 +629,21 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           }
           if (m < p.M && !failed) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
         }
-      }
-      // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR)
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
-        else
-          mbar_arrive(&tempty_bar[acc]);
-      }
-      ++ls;
-    }
-    // Every bulk store / reduction has completed before the CTA exits.
-    if constexpr (C::W_LOAD || C::RED) {
-      if (issuer) bulk_wait_group<0>();
-      __syncwarp();
-    }
-  } else {
-    // ------------------------------------------- fast-weight loader (update)
-    if constexpr (C::W_LOAD) {
-      if (lane == 0) {
-        const uint64_t pol = l2_policy_evict_first();
-        uint32_t wc = 0;
-        bool ok = true;
-        while (ok && iter.next(seg)) {
-          int bi;
-          int64_t mt, nt;
-          kp.s.tile_coords(seg.tile, bi, mt, nt);
-          if constexpr (PAIR) mt = 2 * mt + rank;
-          const int b1 = bi % p.nb1, b2 = bi / p.nb1;
-          const int64_t row0 = row_of(p.src, b1, b2) + mt * BM;
-          for (int c = 0; c < BN / C::WC; ++c, ++wc) {
-            const uint32_t slot = wc % C::W_SLOTS, ph = (wc / C::W_SLOTS) & 1;
-            if (!mbar_wait_bounded(&wempty_bar[slot], ph ^ 1, abort_flag, 5, &g_device_error)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&wfull_bar[slot], C::W_SLOT_BYTES);
-            const int x = static_cast<int>(nt * BN + c * C::WC), y = static_cast<int>(row0);
-            tma_load_2d_hint(wslots + slot * C::W_SLOT_BYTES, &tmS, &wfull_bar[slot], x, y, pol);
-            tma_load_2d_hint(wslots + slot * C::W_SLOT_BYTES + BM * 32, &tmSl, &wfull_bar[slot], x, y, pol);
-          }
+        // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+          else
+            mbar_arrive(&tempty_bar[acc]);
         }
-        for (uint32_t slot = 0; slot < C::W_SLOTS && slot < wc; ++slot) {
-          const uint32_t f = (wc - 1 - slot) / C::W_SLOTS;  // last fill of this slot
-          mbar_wait_bounded(&wfull_bar[slot], f & 1, abort_flag, 4, &g_device_error);
-        }
+        ++ls;
+      }
+      // Every bulk reduction has completed before the CTA exits.
+      if constexpr (C::RED) {
+        if (issuer) bulk_wait_group<0>();
+        __syncwarp();
       }
     }
   }
@@ -720,10 +714,28 @@ static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR>
+// 4-D map of tile-major hi planes read as an MN-major operand: dims (16
+// columns, 128 rows, column blocks, row blocks of all entries); a box is
+// 16 columns x BK rows x box_cols/16 column blocks, 32-byte swizzle.
+static bool make_plane_map(CUtensorMap* map, const Planes& w, int box_cols) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || !w.hi || w.rb <= 0 || w.cb <= 0 || w.entries <= 0) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kPlaneCols), static_cast<cuuint64_t>(kPlaneRows),
+                        static_cast<cuuint64_t>(w.cb), static_cast<cuuint64_t>(w.rb * w.entries)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kPlaneCols) * 2, static_cast<cuuint64_t>(kPlaneBlock) * 2,
+                           static_cast<cuuint64_t>(kPlaneBlock) * 2 * w.cb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kPlaneCols), static_cast<cuuint32_t>(BK),
+                       static_cast<cuuint32_t>(box_cols / kPlaneCols), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w.hi, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR, bool B_PL>
 static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   using C = Cfg<BN, NB, EPI, PAIR>;
-  auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16, PAIR>;
+  auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16, PAIR, B_PL>;
   static std::mutex mu;
   static uint64_t attr_done = 0;  // bit per device: shared-memory size attribute set
   static int max_workers[64] = {0};  // co-resident CTAs (or CTA pairs) per device
@@ -760,22 +772,18 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
 
   // Operand boxes: 64 K-elements (128 bytes) wide; K-major boxes span the
   // tile's rows, MN-major boxes are 64 K-rows of 64 columns.
-  CUtensorMap mA, mB, mB2, mS, mSl, mD, mDl;
+  CUtensorMap mA, mB, mB2, mD;
   if (!make_map(&mA, p.A.ptr, p.A.rows, p.A.cols, p.A.ld, false, 64, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mB, p.B.ptr, p.B.rows, p.B.cols, p.B.ld, false, 64, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
-  mB2 = mB;
+  if (B_PL) {
+    if (!make_plane_map(&mB, p.w, C::B_COLS)) return cudaErrorInvalidValue;
+  } else if (!make_map(&mB, p.B.ptr, p.B.rows, p.B.cols, p.B.ld, false, 64, B_MN ? 64 : BN)) {
+    return cudaErrorInvalidValue;
+  }
+  mB2 = mD = mB;
   if (NB == 2 && !make_map(&mB2, p.B2.ptr, p.B2.rows, p.B2.cols, p.B2.ld, false, 64, B_MN ? 64 : BN))
     return cudaErrorInvalidValue;
-  mS = mSl = mD = mDl = mA;
-  if (C::W_LOAD) {
-    // hi and lo planes: 16-bit elements, 16-column (32-byte) boxes
-    if (!make_map(&mS, p.src.ptr, p.src.rows, p.N, p.src.ld, false, C::WC, BM) ||
-        !make_map(&mSl, p.src_lo.ptr, p.src_lo.rows, p.N, p.src_lo.ld, false, C::WC, BM) ||
-        !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, false, C::WC, BM) ||
-        !make_map(&mDl, p.D_lo.ptr, p.D_lo.rows, p.N, p.D_lo.ld, false, C::WC, BM))
-      return cudaErrorInvalidValue;
-  }
   if (C::RED && !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, 32, BM)) return cudaErrorInvalidValue;
+  if (C::W_UPD && (!p.w.hi || !p.w.lo || p.w.rb <= 0 || p.w.cb <= 0)) return cudaErrorInvalidValue;
 
   KParams kp;
   kp.p = p;
@@ -795,14 +803,14 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   if (workers <= 0) return cudaSuccess;
   LaunchMark mark(p.kind, stream);
   return launch_overlapped(kern, dim3(static_cast<unsigned>((PAIR ? 2 : 1) * workers)), dim3(C::THREADS),
-                           C::SMEM_BYTES, stream, PAIR ? 2 : 1, mA, mB, mB2, mS, mSl, mD, mDl, kp);
+                           C::SMEM_BYTES, stream, PAIR ? 2 : 1, mA, mB, mB2, mD, kp);
 }
 
 // Pairs of CTAs once the problem has at least two 128-row tiles.
-template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16>
+template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool B_PL = false>
 static cudaError_t run_any(const GemmProblem& p, cudaStream_t stream) {
-  if (p.M > BM) return run<BN, NB, A_MN, B_MN, EPI, OUT_BF16, true>(p, stream);
-  return run<BN, NB, A_MN, B_MN, EPI, OUT_BF16, false>(p, stream);
+  if (p.M > BM) return run<BN, NB, A_MN, B_MN, EPI, OUT_BF16, true, B_PL>(p, stream);
+  return run<BN, NB, A_MN, B_MN, EPI, OUT_BF16, false, B_PL>(p, stream);
 }
 
 }  // namespace tc
@@ -838,7 +846,9 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
       if (a_mn && b_mn && !p.out_bf16) return run_any<256, 1, true, true, EPI_STORE, false>(p, stream);
       break;
     case EPI_ACCUM:
-      if (!a_mn && b_mn) return run_any<256, 1, false, true, EPI_ACCUM, false>(p, stream);
+      if (!a_mn && b_mn)
+        return p.b_planes ? run_any<256, 1, false, true, EPI_ACCUM, false, true>(p, stream)
+                          : run_any<256, 1, false, true, EPI_ACCUM, false>(p, stream);
       break;
     case EPI_AXPY:
       if (a_mn && b_mn) return run_any<256, 1, true, true, EPI_AXPY, false>(p, stream);

@@ -89,20 +89,24 @@ struct ResidualArgs {
 };
 cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t stream);
 
-// The fp32 fast weight as split hi/lo planes (split_w / join_w in common.cuh):
-//   split: hi[s], lo[s] = split(W0[s or 0]) for s < batch, n = d_ff*d (a multiple of 4);
-//   merge: W = join(hi, lo) over `total` elements (a multiple of 4).
-cudaError_t launch_split_w(const float* W0, int64_t w0_stride, uint16_t* hi, uint16_t* lo, int64_t batch, int64_t n,
-                           cudaStream_t stream);
-cudaError_t launch_merge_w(const uint16_t* hi, const uint16_t* lo, float* W, int64_t total, cudaStream_t stream);
+// The fp32 fast weight as tile-major split planes (split_w / plane_index in
+// common.cuh; Planes in gemm.h), R x C per entry, C a multiple of 8:
+//   split: the planes of every entry e = split(W0[e or 0]) (w0_stride elements apart, 0 = shared);
+//   merge: W (entries x R x C fp32) = join(planes).
+cudaError_t launch_split_planes(const float* W0, int64_t w0_stride, const Planes& w, int64_t R, int64_t C,
+                                cudaStream_t stream);
+cudaError_t launch_merge_planes(const Planes& w, float* W, int64_t R, int64_t C, cudaStream_t stream);
 // W[s] = W0[s or 0] (fp32 copy) for s < batch.
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream);
 
 // Exclusive scan over G fp32 group sums D[g], element-wise over batch*n:
-//   S = W0; for g: t = D[g]; state[g] = S; S += alpha*t;  W_final = S
-// where state[g] is D[g] itself (hi == nullptr) or the split planes hi[g], lo[g].
-cudaError_t launch_group_scan(float* D, uint16_t* hi, uint16_t* lo, const float* W0, int64_t w0_stride,
-                              float* W_final, int64_t G, int64_t batch, int64_t n, float alpha, cudaStream_t stream);
+//   S = W0; for g: t = D[g]; D[g] = S; S += alpha*t;  W_final = S        (fp32 mode, in place)
+cudaError_t launch_group_scan(float* D, const float* W0, int64_t w0_stride, float* W_final, int64_t G,
+                              int64_t batch, int64_t n, float alpha, cudaStream_t stream);
+// The same scan writing each group's starting weight as the planes of entry g*batch + b.
+cudaError_t launch_group_scan_planes(const float* D, const Planes& w, const float* W0, int64_t w0_stride,
+                                     float* W_final, int64_t G, int64_t batch, int64_t R, int64_t C, float alpha,
+                                     cudaStream_t stream);
 
 }  // namespace ipttt
