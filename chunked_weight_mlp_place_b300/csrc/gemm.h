@@ -40,12 +40,14 @@ struct OutRef {
 // columns, each block 4 KB contiguous (row r of a block at r * 32 bytes), the
 // blocks of one row of blocks side by side, rows of blocks one after another,
 // sequences (or groups) one after another; the matrix is padded with zeros to
-// whole blocks.  A warp finishing 32 rows of one 16-column chunk then reads
-// and writes 1 KB contiguous, and TMA reads the hi plane as an MN-major
-// operand with the 32-byte swizzle.
+// whole blocks.  Inside a row the two 8-column halves trade places where bit 2
+// of r is set: the 32-byte swizzle of a shared-memory operand tile, so any 64
+// rows of a block starting at a multiple of 8 are 2 KB that TMA copies as they
+// are (rows of 512 bytes) into the MN-major 32-byte-swizzle operand layout.  A
+// warp finishing 32 rows of one 16-column chunk reads and writes 1 KB contiguous.
 constexpr int kPlaneRows = 128, kPlaneCols = 16, kPlaneBlock = kPlaneRows * kPlaneCols;
 __host__ __device__ __forceinline__ int64_t plane_index(int64_t rb_row, int64_t cb, int64_t nblk_cols, int r, int c) {
-  return (rb_row * nblk_cols + cb) * kPlaneBlock + r * kPlaneCols + c;
+  return (rb_row * nblk_cols + cb) * kPlaneBlock + r * kPlaneCols + (c ^ (((r >> 2) & 1) << 3));
 }
 
 // A fast weight (one d_ff x d matrix per entry) as tile-major split planes.

@@ -7,7 +7,7 @@
 //   update W += alpha Z_k^T R_k             A = Z_k (MN-major) B = R_k         (MN-major)
 // (the fast weight W is kept as split hi/lo 16-bit planes, common.cuh::split_w,
 // stored tile-major in blocks of 128 rows x 16 columns, gemm.h::plane_index;
-// the hi plane is the bf16 operand of the apply, read through a 4-D TMA map).
+// the hi plane is the bf16 operand of the apply, read through a 3-D TMA map).
 //
 // Problems with more than one 128-row tile run on CTA pairs (clusters of 2,
 // tcgen05 cta_group::2): one 256 x N MMA per pair, each CTA holding 128 rows
@@ -80,7 +80,6 @@ struct Cfg {
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_TOTAL + BAR_BYTES;
   static_assert(N_MMA <= kAccStride && N_MMA % 16 == 0, "accumulator width");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(B_COLS % 64 == 0, "B columns per CTA: whole 64-column swizzle atoms");
   static_assert(!PAIR || NB == 1 || BN == B_COLS, "pair: a second B operand is the peer's half");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
   static_assert(STAGE_BYTES % 1024 == 0 && STG_BYTES % 1024 == 0, "1024-byte aligned swizzle atoms");
@@ -193,17 +192,19 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
 }
 
 // The B operand read from tile-major hi planes (an MN-major operand, K = rows of
-// the weight): one 4-D box of 16 columns x BK rows x EXT/16 column blocks lands
-// as EXT/16 blocks of BK rows of 32 bytes, the 32-byte-swizzle MN-major layout.
+// the weight).  The map views the planes as rows of 512 bytes (16 rows of a
+// block), 8 to a block, blocks in storage order; one box of 4 such rows x EXT/16
+// blocks lands as EXT/16 pieces of BK rows x 32 bytes, 2 KB apart, already in
+// the 32-byte-swizzle layout (gemm.h::plane_index).
 template <int EXT, bool PAIR>
 __device__ __forceinline__ void load_plane_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                                   uint32_t bar_cl, int64_t rb0, int64_t n0, int64_t k0) {
-  const int c1 = static_cast<int>(k0 % kPlaneRows), c2 = static_cast<int>(n0 / kPlaneCols);
-  const int c3 = static_cast<int>(rb0 + k0 / kPlaneRows);
+                                                   uint32_t bar_cl, int64_t rb0, int64_t cb, int64_t n0, int64_t k0) {
+  const int c1 = static_cast<int>((k0 % kPlaneRows) / 16);
+  const int c2 = static_cast<int>((rb0 + k0 / kPlaneRows) * cb + n0 / kPlaneCols);
   if constexpr (PAIR)
-    tma_load_4d_pair(dst, map, bar_cl, 0, c1, c2, c3);
+    tma_load_3d_pair(dst, map, bar_cl, 0, c1, c2);
   else
-    tma_load_4d(dst, map, bar, 0, c1, c2, c3);
+    tma_load_3d(dst, map, bar, 0, c1, c2);
 }
 
 // Shared-memory descriptor of the k-th 16-wide K step of an operand tile.
@@ -289,6 +290,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
   using C = Cfg<BN, NB, EPI, PAIR>;
   static_assert(!PAIR || B_MN, "pairs split an MN-major B operand by columns");
   static_assert(!B_PL || (B_MN && NB == 1), "a plane B operand is MN-major and single");
+  static_assert(B_PL ? C::B_COLS % kPlaneCols == 0 : C::B_COLS % 64 == 0,
+                "B columns per CTA: whole swizzle atoms (64 columns, or 16 for plane blocks)");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           const int64_t k0 = static_cast<int64_t>(kb) * BK;
           load_operand<A_MN, BM, PAIR>(sa, &tmA, &full_bar[st], bar_cl, ra, mt * BM, k0);
           if constexpr (B_PL) {
-            load_plane_operand<C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, pb0,
+            load_plane_operand<C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, pb0, p.w.cb,
                                                 nt * BN + rank * C::B_COLS, k0);
           } else if constexpr (PAIR && NB == 2) {
             // the even CTA holds the first B operand, its peer the second
@@ -498,20 +501,21 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         const int b1 = bi % p.nb1, b2 = bi / p.nb1;
         const int64_t rbk = (b1 * p.w.es1 + b2 * p.w.es2) * p.w.rb + mt;
         x.cb0 = nt * (BN / WC);
-        const int64_t off = plane_index(rbk, x.cb0, p.w.cb, trow, 0);
+        const int64_t off = plane_index(rbk, x.cb0, p.w.cb, 0, 0) + trow * kPlaneCols;
         x.hi = p.w.hi + off;
         x.lo = p.w.lo + off;
         return x;
       };
+      const int sw = (trow >> 2) & 1;  // this row's 16-byte halves trade places (plane_index)
       uint4 wh[4][2], wl[4][2];  // planes of the chunks in flight, indexed by chunk % 4
       auto wload = [&](const TileW& t, int c, uint4 (&h)[2], uint4 (&l)[2]) {
         if (t.hi == nullptr || t.cb0 + c >= p.w.cb) return;
         const uint4* hp = reinterpret_cast<const uint4*>(t.hi + static_cast<int64_t>(c) * kPlaneBlock);
         const uint4* lp = reinterpret_cast<const uint4*>(t.lo + static_cast<int64_t>(c) * kPlaneBlock);
-        h[0] = hp[0];
-        h[1] = hp[1];
-        l[0] = __ldcs(lp);
-        l[1] = __ldcs(lp + 1);
+        h[0] = hp[sw];
+        h[1] = hp[sw ^ 1];
+        l[0] = __ldcs(lp + sw);
+        l[1] = __ldcs(lp + (sw ^ 1));
       };
       SegIter ahead = iter;
       Seg cur, nxt;
@@ -559,10 +563,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
             if (!failed && tw.hi != nullptr && tw.cb0 + c < p.w.cb) {
               uint4* hp = reinterpret_cast<uint4*>(tw.hi + static_cast<int64_t>(c) * kPlaneBlock);
               uint4* lp = reinterpret_cast<uint4*>(tw.lo + static_cast<int64_t>(c) * kPlaneBlock);
-              hp[0] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-              hp[1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
-              __stcs(lp, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-              __stcs(lp + 1, make_uint4(lo[4], lo[5], lo[6], lo[7]));
+              hp[sw] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+              hp[sw ^ 1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
+              __stcs(lp + sw, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+              __stcs(lp + (sw ^ 1), make_uint4(lo[4], lo[5], lo[6], lo[7]));
             }
           }
         }
@@ -714,21 +718,22 @@ static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D map of tile-major hi planes read as an MN-major operand: dims (16
-// columns, 128 rows, column blocks, row blocks of all entries); a box is
-// 16 columns x BK rows x box_cols/16 column blocks, 32-byte swizzle.
+// 3-D map of tile-major hi planes read as an MN-major operand: dims (256
+// elements = 512 bytes, 8 rows of 512 bytes per block, blocks of all entries);
+// a box is BK/16 rows x box_cols/16 blocks, no swizzle (the planes are stored
+// swizzled).
 static bool make_plane_map(CUtensorMap* map, const Planes& w, int box_cols) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc || !w.hi || w.rb <= 0 || w.cb <= 0 || w.entries <= 0) return false;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kPlaneCols), static_cast<cuuint64_t>(kPlaneRows),
-                        static_cast<cuuint64_t>(w.cb), static_cast<cuuint64_t>(w.rb * w.entries)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kPlaneCols) * 2, static_cast<cuuint64_t>(kPlaneBlock) * 2,
-                           static_cast<cuuint64_t>(kPlaneBlock) * 2 * w.cb};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(kPlaneCols), static_cast<cuuint32_t>(BK),
-                       static_cast<cuuint32_t>(box_cols / kPlaneCols), 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w.hi, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  constexpr int kRow = 256;  // elements per 512-byte row
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(kPlaneBlock / kRow),
+                        static_cast<cuuint64_t>(w.cb * w.rb * w.entries)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRow) * 2, static_cast<cuuint64_t>(kPlaneBlock) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kRow), static_cast<cuuint32_t>(BK * kPlaneCols / kRow),
+                       static_cast<cuuint32_t>(box_cols / kPlaneCols)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w.hi, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
