@@ -48,7 +48,7 @@ import numpy as np
 
 __all__ = [
     "silu", "gated_activation", "chunk_conv", "make_targets", "mse_loss",
-    "chunk_step", "chunk_engine", "layer_forward",
+    "chunk_step", "chunk_engine", "layer_forward", "layer_forward_varlen",
 ]
 
 
@@ -172,4 +172,44 @@ def layer_forward(X: np.ndarray, E: np.ndarray, W_g: np.ndarray, W_u: np.ndarray
             V_k = make_targets(E[rows], conv_w, P, B)
             O[s * K * B + k * B: s * K * B + (k + 1) * B], W = chunk_step(Z_k, V_k, W, eta, rule)
         W_fin[s] = W
+    return O, W_fin
+
+
+def layer_forward_varlen(X: np.ndarray, E: np.ndarray, W_g: np.ndarray, W_u: np.ndarray,
+                         W_o0: np.ndarray, conv_w: np.ndarray, P: np.ndarray, cu_seqlens,
+                         B: int, eta: float, rule: str = "mse") -> Tuple[np.ndarray, np.ndarray]:
+    """The layer over packed documents, with the fast weight reset at every
+    document boundary (itsolotime §3.2, "boundary reset": back to the
+    pretrained initial value, so no document sees another's updates).
+
+    Document i holds rows cu_seqlens[i] .. cu_seqlens[i+1]-1 of X and E.
+    Readings where the pages are silent:
+
+    * a document's chunks start at its first token: B tokens each, the last one
+      holding what is left (1 .. B tokens);
+    * that last chunk's step is normalised by its own token count (the chunk
+      loss is the mean over the chunk's tokens, as for full chunks);
+    * the conv reads zeros past the document's end, as past any chunk's end.
+
+    W_o0 is (d_ff, d) shared by all documents, or (n_docs, d_ff, d).  Returns
+    O (T, d) and W_final (n_docs, d_ff, d).
+    """
+    X = np.asarray(X, np.float64)
+    E = np.asarray(E, np.float64)
+    cu = [int(c) for c in cu_seqlens]
+    n_docs = len(cu) - 1
+    if n_docs < 0 or cu[0] != 0 or cu[-1] != X.shape[0] or any(b <= a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must rise strictly from 0 to the number of rows")
+    W0 = np.asarray(W_o0, np.float64)
+    O = np.zeros((X.shape[0], E.shape[1]), np.float64)
+    W_fin = np.zeros((n_docs,) + W0.shape[-2:], np.float64)
+    for i in range(n_docs):
+        W = np.array(W0[i] if W0.ndim == 3 else W0, np.float64, copy=True)
+        for c0 in range(cu[i], cu[i + 1], B):
+            rows = slice(c0, min(c0 + B, cu[i + 1]))
+            n = rows.stop - rows.start
+            Z_k = gated_activation(X[rows], W_g, W_u)
+            V_k = make_targets(E[rows], conv_w, P, n)  # the whole (possibly short) chunk is one conv chunk
+            O[rows], W = chunk_step(Z_k, V_k, W, eta, rule)
+        W_fin[i] = W
     return O, W_fin

@@ -120,14 +120,16 @@ def test_mse_gradient_finite_differences():
 # -------------------------------------------------------------- brute force
 def _brute_force(Z, V, W0, B, eta, rule):
     """Pure-Python per-token loops, accumulating each token's gradient and
-    applying the sum at the end of its chunk (B=1: one update per token)."""
+    applying the sum, over the chunk's token count, at the end of its chunk
+    (B=1: one update per token; a short last chunk averages its own tokens)."""
     Z, V = Z.tolist(), V.tolist()
     W = [list(r) for r in W0.tolist()]
     d_ff, d = len(W), len(W[0])
     O = []
     for c0 in range(0, len(Z), B):
         G = [[0.0] * d for _ in range(d_ff)]
-        for t in range(c0, c0 + B):
+        n = min(B, len(Z) - c0)
+        for t in range(c0, c0 + n):
             o = [sum(Z[t][i] * W[i][j] for i in range(d_ff)) for j in range(d)]
             O.append(o)
             e = [o[j] - V[t][j] for j in range(d)] if rule == "mse" else [-V[t][j] for j in range(d)]
@@ -136,7 +138,7 @@ def _brute_force(Z, V, W0, B, eta, rule):
                     G[i][j] += Z[t][i] * e[j]
         for i in range(d_ff):
             for j in range(d):
-                W[i][j] -= eta / B * G[i][j]
+                W[i][j] -= eta / n * G[i][j]
     return np.array(O), np.array(W)
 
 
@@ -296,3 +298,106 @@ def test_tiny_workload_is_stable_and_finite():
         O, W = orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"],
                                  w.L, w.B, w.eta, rule)
         assert np.all(np.isfinite(O)) and np.all(np.isfinite(W))
+
+
+# ------------------------------------------------- packed documents (varlen)
+def _targets_per_token(E, conv_w, P, starts, ends, B):
+    """v_t = (sum_j conv_w[:, j] * E[t+j]) P over the taps that stay inside t's
+    chunk, chunks of B tokens counted from each document's first token and cut
+    at its last: a per-token loop, independent of the oracle's chunk slicing."""
+    V = np.zeros_like(E)
+    for a, b in zip(starts, ends):
+        for t in range(a, b):
+            end = min(a + ((t - a) // B + 1) * B, b)
+            c = np.zeros(E.shape[1])
+            for j in range(4):
+                if t + j < end:
+                    c += conv_w[:, j] * E[t + j]
+            V[t] = c @ P
+    return V
+
+
+def _docs(lengths, seed=11, d=4, d_ff=6):
+    rng = np.random.default_rng(seed)
+    T = int(sum(lengths))
+    t = dict(X=rng.standard_normal((T, d)), E=rng.standard_normal((T, d)),
+             W_g=rng.standard_normal((d, d_ff)) / np.sqrt(d), W_u=rng.standard_normal((d, d_ff)) / np.sqrt(d),
+             W_o0=rng.standard_normal((d_ff, d)) / np.sqrt(d_ff), conv_w=rng.standard_normal((d, 4)) * np.sqrt(0.5),
+             P=rng.standard_normal((d, d)) / np.sqrt(d))
+    t["cu"] = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return t
+
+
+def _varlen(t, B, eta, rule="mse", W0=None):
+    return orc.layer_forward_varlen(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"] if W0 is None else W0,
+                                    t["conv_w"], t["P"], t["cu"], B, eta, rule)
+
+
+@pytest.mark.parametrize("rule", ["mse", "add"])
+def test_varlen_whole_chunk_documents_equal_the_batched_layer(rule):
+    """Documents of whole chunks, all of one length: the batched layer, each
+    sequence restarting from W_o0 (the reset is the batched layer's own)."""
+    t = _docs([12, 12, 12])
+    O, W = _varlen(t, 4, 0.2, rule)
+    Ob, Wb = orc.layer_forward(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"], t["conv_w"], t["P"], 12, 4, 0.2, rule)
+    np.testing.assert_allclose(O, Ob, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(W, Wb, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("rule", ["mse", "add"])
+def test_varlen_ragged_documents_match_per_token_brute_force(rule):
+    """Ragged last chunks (13 = 4+4+4+1, 6 = 4+2) and a document shorter than B:
+    per-token outputs and gradients, the fast weight reset per document, each
+    chunk's step averaged over its own tokens."""
+    lengths, B, eta = [13, 3, 6], 4, 0.25
+    t = _docs(lengths)
+    O, W = _varlen(t, B, eta, rule)
+    cu = t["cu"]
+    Z = orc.gated_activation(t["X"], t["W_g"], t["W_u"])
+    V = _targets_per_token(t["E"], t["conv_w"], t["P"], cu[:-1], cu[1:], B)
+    for i in range(len(lengths)):
+        r = slice(cu[i], cu[i + 1])
+        Ob, Wb = _brute_force(Z[r], V[r], t["W_o0"], B, eta, rule)
+        np.testing.assert_allclose(O[r], Ob, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(W[i], Wb, rtol=1e-12, atol=1e-12)
+
+
+def test_varlen_short_document_closed_form():
+    """One document of n < B tokens is one chunk: O = MLP(x) with W_o0 (two
+    plain matmuls and the logistic function), and
+    W_final = W_o0 - (eta/n) Z^T (Z W_o0 - V)."""
+    n, B, eta = 5, 8, 0.3
+    t = _docs([n], seed=12)
+    O, W = _varlen(t, B, eta)
+    a = t["X"] @ t["W_g"]
+    Z = a * scipy.special.expit(a) * (t["X"] @ t["W_u"])
+    V = _targets_per_token(t["E"], t["conv_w"], t["P"], [0], [n], B)
+    np.testing.assert_allclose(O, Z @ t["W_o0"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(W[0], t["W_o0"] - (eta / n) * Z.T @ (Z @ t["W_o0"] - V), rtol=1e-12, atol=1e-13)
+
+
+def test_varlen_documents_are_isolated():
+    """Changing one document's tokens changes nothing in the others (the reset
+    at each boundary, and no conv tap reads across one)."""
+    lengths, B = [9, 7, 10], 4
+    t = _docs(lengths)
+    O, W = _varlen(t, B, 0.2)
+    cu = t["cu"]
+    t2 = dict(t)
+    t2["X"] = t["X"].copy()
+    t2["E"] = t["E"].copy()
+    t2["X"][cu[1]:cu[2]] += 1.0
+    t2["E"][cu[1]:cu[2]] -= 0.5
+    O2, W2 = _varlen(t2, B, 0.2)
+    for i in (0, 2):
+        np.testing.assert_array_equal(O2[cu[i]:cu[i + 1]], O[cu[i]:cu[i + 1]])
+        np.testing.assert_array_equal(W2[i], W[i])
+    assert not np.allclose(O2[cu[1]:cu[2]], O[cu[1]:cu[2]])
+    assert not np.allclose(W2[1], W[1])
+
+
+def test_varlen_rejects_bad_boundaries():
+    t = _docs([4, 4])
+    for cu in ([0, 4, 4, 8], [1, 8], [0, 4, 9]):
+        with pytest.raises(ValueError):
+            orc.layer_forward_varlen(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"], t["conv_w"], t["P"], cu, 4, 0.1)
