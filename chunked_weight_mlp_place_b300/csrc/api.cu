@@ -543,6 +543,179 @@ struct LaunchScope {
   LaunchScope() { t_launches = 0; }
 };
 
+// ------------------------------------------------------- packed documents
+// The layer over packed documents, the fast weight reset to W_o0 at every
+// boundary (In-Place TTT, itsolotime §3.2 "boundary reset").  Documents are
+// taken longest first, so the ones still running at chunk step i are a prefix
+// of that order and each step is one batched apply / residual / update over
+// them; a document's rows are found through a table of starts.  A document's
+// last chunk may be short: the residual pass writes zeros past its end (the
+// update's contraction then ignores those rows) and scales R by B/n, so the
+// step is the mean over the chunk's n tokens.
+struct VarlenPlan {
+  int64_t T = 0, n_docs = 0, k_max = 0;
+  std::vector<int64_t> order;   // sorted position -> document
+  std::vector<int64_t> starts;  // sorted position -> first row
+  std::vector<int64_t> lens;    // sorted position -> tokens
+  std::vector<int64_t> active;  // chunk step -> documents still running
+};
+
+ipttt_status plan_varlen(const int64_t* cu, int64_t n_docs, int64_t B, VarlenPlan* pl) {
+  if (!cu || n_docs < 0 || cu[0] != 0) return IPTTT_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n_docs; ++i)
+    if (cu[i + 1] <= cu[i]) return IPTTT_ERR_INVALID_ARG;
+  pl->n_docs = n_docs;
+  pl->T = cu[n_docs];
+  pl->order.resize(n_docs);
+  for (int64_t i = 0; i < n_docs; ++i) pl->order[i] = i;
+  std::stable_sort(pl->order.begin(), pl->order.end(),
+                   [&](int64_t a, int64_t b) { return cu[a + 1] - cu[a] > cu[b + 1] - cu[b]; });
+  pl->starts.resize(n_docs);
+  pl->lens.resize(n_docs);
+  for (int64_t s = 0; s < n_docs; ++s) {
+    pl->starts[s] = cu[pl->order[s]];
+    pl->lens[s] = cu[pl->order[s] + 1] - cu[pl->order[s]];
+  }
+  pl->k_max = n_docs ? (pl->lens[0] + B - 1) / B : 0;
+  pl->active.assign(pl->k_max, 0);
+  for (int64_t s = 0; s < n_docs; ++s)
+    for (int64_t i = 0; i < (pl->lens[s] + B - 1) / B; ++i) ++pl->active[i];
+  return IPTTT_OK;
+}
+
+ipttt_status run_varlen(const void* X, const void* E, const void* W_g, const void* W_u, const float* W0,
+                        const float* conv_w, const void* P, const int64_t* cu, const VarlenPlan& pl, int64_t B,
+                        float eta, ipttt_rule rule, void* O, float* Wf, const ipttt_dims* dm, cudaStream_t st) {
+  const bool bf16 = dm->dtype == IPTTT_BF16;
+  const int64_t n = pl.n_docs, T = pl.T, d = dm->d, dff = dm->d_ff, nw = dff * d;
+  const size_t es = act_size(dm);
+  const int64_t np = plane_rb(dm) * plane_cb(dm) * kPlaneBlock;
+  Carve c;
+  const size_t z_off = c.take<uint8_t>(T * dff * static_cast<int64_t>(es));
+  const size_t v_off = c.take<uint8_t>(T * d * static_cast<int64_t>(es));
+  const size_t c_off = c.take<uint8_t>(T * d * static_cast<int64_t>(es));
+  const size_t acc_off = c.take<float>(n * B * d);
+  const size_t r_off = c.take<uint8_t>(n * B * d * static_cast<int64_t>(es));
+  const size_t hi_off = bf16 ? c.take<uint16_t>(n * np) : 0;
+  const size_t lo_off = bf16 ? c.take<uint16_t>(n * np) : 0;
+  const size_t cu_off = c.take<int64_t>(n + 1);
+  const size_t st_off = c.take<int64_t>(n);
+  const size_t ln_off = c.take<int64_t>(n);
+  const size_t wt_off = c.take<int64_t>(n);
+  void* wsv = nullptr;
+  IPTTT_TRY(pool_reserve(c.off, &wsv));
+  uint8_t* ws = static_cast<uint8_t*>(wsv);
+  int64_t* cu_d = reinterpret_cast<int64_t*>(ws + cu_off);
+  int64_t* starts_d = reinterpret_cast<int64_t*>(ws + st_off);
+  int64_t* lens_d = reinterpret_cast<int64_t*>(ws + ln_off);
+  int64_t* wtab_d = reinterpret_cast<int64_t*>(ws + wt_off);
+  std::vector<int64_t> wtab(n);
+  for (int64_t s = 0; s < n; ++s) wtab[s] = pl.order[s] * dff;
+  // pageable sources: each copy has read its source when the call returns
+  IPTTT_CUDA(cudaMemcpyAsync(cu_d, cu, sizeof(int64_t) * (n + 1), cudaMemcpyHostToDevice, st));
+  IPTTT_CUDA(cudaMemcpyAsync(starts_d, pl.starts.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, st));
+  IPTTT_CUDA(cudaMemcpyAsync(lens_d, pl.lens.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, st));
+  IPTTT_CUDA(cudaMemcpyAsync(wtab_d, wtab.data(), sizeof(int64_t) * n, cudaMemcpyHostToDevice, st));
+
+  void* Z = ws + z_off;
+  void* V = ws + v_off;
+  void* R = ws + r_off;
+  float* o_acc = reinterpret_cast<float*>(ws + acc_off);
+  uint16_t* hi = bf16 ? reinterpret_cast<uint16_t*>(ws + hi_off) : nullptr;
+  uint16_t* lo = bf16 ? reinterpret_cast<uint16_t*>(ws + lo_off) : nullptr;
+  IPTTT_TRY(run_gate(X, W_g, W_u, Z, T, dm, st));
+  IPTTT_CUDA(launch_conv_varlen(E, conv_w, ws + c_off, T, cu_d, n, B, d, bf16, st));
+  {
+    GemmProblem p;
+    p.M = T;
+    p.N = d;
+    p.K = d;
+    p.A = mat(ws + c_off, T, d, 0);
+    p.B = mat(P, d, d, 1);
+    p.epi = EPI_STORE;
+    p.kind = K_PROJ;
+    p.out_bf16 = bf16;
+    p.D = out(V, d);
+    IPTTT_CUDA(gemm(p, bf16, st));
+  }
+  // fast weights: planes in sorted order (bf16), or W_final itself in document order (fp32)
+  const Planes w = planes_of(dm, hi, lo, n, 1, 0);
+  if (bf16) {
+    if (dm->w0_per_seq) {
+      for (int64_t s = 0; s < n; ++s)
+        IPTTT_CUDA(launch_split_planes(W0 + pl.order[s] * nw, 0, planes_of(dm, hi + s * np, lo + s * np, 1, 1, 0),
+                                       dff, d, st));
+    } else {
+      IPTTT_CUDA(launch_split_planes(W0, 0, w, dff, d, st));
+    }
+  } else {
+    IPTTT_CUDA(launch_copy_w(W0, dm->w0_per_seq ? nw : 0, Wf, n, nw, st));
+  }
+  IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * n * B * d, st));
+  const float alpha = (rule == IPTTT_RULE_MSE ? -eta : eta) / static_cast<float>(B);
+  for (int64_t i = 0; i < pl.k_max; ++i) {
+    const int na = static_cast<int>(pl.active[i]);
+    GemmProblem a;
+    a.M = B;
+    a.N = d;
+    a.K = dff;
+    a.nb1 = na;
+    a.A = mat(Z, T, dff, 0, i * B);
+    a.A.ytab = starts_d;
+    if (bf16) {
+      a.B = mat(hi, n * dff, d, 1, 0, dff);
+      a.w = w;
+      a.b_planes = 1;
+    } else {
+      a.B = mat(Wf, n * dff, d, 1);
+      a.B.ytab = wtab_d;
+    }
+    a.epi = EPI_ACCUM;
+    a.kind = K_APPLY;
+    a.D = out(o_acc, d, 0, B, 0, n * B);
+    a.split_k = 1;
+    IPTTT_CUDA(gemm(a, bf16, st));
+    ResidualArgs ra;
+    ra.acc = o_acc;
+    ra.V = V;
+    ra.O = O;
+    ra.R = R;
+    ra.B = B;
+    ra.d = d;
+    ra.nb1 = na;
+    ra.o_y0 = i * B;
+    ra.otab = starts_d;
+    ra.lens = lens_d;
+    ra.r_from_v = rule == IPTTT_RULE_ADD;
+    IPTTT_CUDA(launch_residual(ra, bf16, st));
+    GemmProblem u;
+    u.M = dff;
+    u.N = d;
+    u.K = B;
+    u.nb1 = na;
+    u.A = mat(Z, T, dff, 1, i * B);
+    u.A.ytab = starts_d;
+    u.B = mat(R, n * B, d, 1, 0, B);
+    u.epi = EPI_AXPY;
+    u.kind = K_UPDATE;
+    if (bf16) {
+      u.w = w;
+    } else {
+      u.D = out(Wf, d, 0, 0, 0, n * dff);
+      u.D.ytab = wtab_d;
+      u.src = u.D;
+    }
+    u.alpha = alpha;
+    IPTTT_CUDA(gemm(u, bf16, st));
+  }
+  if (bf16) {
+    for (int64_t s = 0; s < n; ++s)
+      IPTTT_CUDA(launch_merge_planes(planes_of(dm, hi + s * np, lo + s * np, 1, 1, 0), Wf + pl.order[s] * nw, dff, d,
+                                     st));
+  }
+  return IPTTT_OK;
+}
+
 }  // namespace
 }  // namespace ipttt
 
@@ -646,6 +819,28 @@ ipttt_status ipttt_layer_forward(const void* X, const void* E, const void* W_g, 
   IPTTT_TRY(run_gate(X, W_g, W_u, ws + z_off, T, dims, st));
   IPTTT_TRY(run_targets(E, conv_w, P, ws + v_off, ws + c_off, T, L, B, dims, st));
   return run_engine(ws + z_off, ws + v_off, W_o0, L, B, eta, rule, O, W_final, dims, ws, lay, st);
+}
+
+ipttt_status ipttt_layer_forward_varlen(const void* X, const void* E, const void* W_g, const void* W_u,
+                                        const float* W_o0, const float* conv_w, const void* P,
+                                        const int64_t* cu_seqlens, int64_t n_docs, int64_t B, float eta,
+                                        ipttt_rule rule, void* O, float* W_final, const ipttt_dims* dims,
+                                        ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, false));
+  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
+  if (B < 1 || n_docs < 0 || !cu_seqlens) return IPTTT_ERR_INVALID_ARG;
+  if (dims->dtype == IPTTT_BF16 && B % 16) return IPTTT_ERR_INVALID_ARG;
+  VarlenPlan pl;
+  IPTTT_TRY(plan_varlen(cu_seqlens, n_docs, B, &pl));
+  if (n_docs == 0) return IPTTT_OK;
+  // token rows, fast-weight rows and chunk rows of all documents are TMA coordinates (int32)
+  if (pl.T > (int64_t{1} << 31) || dims->d_ff * n_docs > (int64_t{1} << 31) || B * n_docs > (int64_t{1} << 31))
+    return IPTTT_ERR_INVALID_ARG;
+  IPTTT_TRY(check_ptrs({X, E, W_g, W_u, static_cast<const void*>(W_o0), static_cast<const void*>(conv_w), P,
+                        static_cast<const void*>(O), static_cast<const void*>(W_final)}));
+  return run_varlen(X, E, W_g, W_u, W_o0, conv_w, P, cu_seqlens, pl, B, eta, rule, O, W_final, dims,
+                    static_cast<cudaStream_t>(stream));
 }
 
 ipttt_status ipttt_sync_status(ipttt_stream stream) {

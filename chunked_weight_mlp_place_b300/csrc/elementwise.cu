@@ -21,81 +21,155 @@ int grid_for(int64_t work_items) {
 // ---------------------------------------------------------------------- conv
 // C[t, c] = sum_{j<4} w[c, j] * E[t+j, c], with E[t+j] read as zero once t+j
 // leaves the chunk of B tokens holding t (In-Place TTT target, itsolotime §2.3).
-// One thread: VEC channels x TT consecutive tokens, sliding a 4-row window.
-template <typename T, int VEC, int TT>
-__global__ void __launch_bounds__(kThreads) conv_kernel(const T* __restrict__ E, const float* __restrict__ w,
-                                                        T* __restrict__ C, int64_t rows, int64_t L, int64_t B,
-                                                        int64_t d) {
-  const int64_t cgroups = d / VEC;
-  const int64_t tblocks = (rows + TT - 1) / TT;
-  const int64_t total = cgroups * tblocks;
+// Sequences are whole chunks (L % B == 0), so chunks start at the multiples of
+// B in the flattened rows.  One thread: 8 channels (16 bytes) x TT consecutive
+// tokens, sliding a 4-row window; its position inside the chunk is computed
+// once and stepped along the rows.
+constexpr int kConvThreads = 128;  // three blocks per SM at up to 170 registers a thread
+template <int TT>
+__global__ void __launch_bounds__(kConvThreads, 3) conv_bf16x8_kernel(const __nv_bfloat16* __restrict__ E,
+                                                               const float* __restrict__ w,
+                                                               __nv_bfloat16* __restrict__ C, int64_t rows,
+                                                               int64_t B, int64_t d) {
+  const int64_t cgroups = d / 8;
+  const int64_t total = cgroups * ((rows + TT - 1) / TT);
   for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
        item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t cg = item % cgroups, tb = item / cgroups;
-    const int64_t c0 = cg * VEC, r0 = tb * TT;
-    float wt[4][VEC];
+    const int64_t tb = item / cgroups;
+    const int64_t c0 = (item - tb * cgroups) * 8, r0 = tb * TT;
+    // window of rows r0 .. r0+TT+2, all loads in flight before any arithmetic
+    uint4 raw[TT + 3];
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
+    for (int i = 0; i < TT + 3; ++i)
+      raw[i] = (r0 + i < rows) ? *reinterpret_cast<const uint4*>(E + (r0 + i) * d + c0) : make_uint4(0, 0, 0, 0);
+    float wt[4][8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
       const float4 q = *reinterpret_cast<const float4*>(w + (c0 + v) * 4);
       wt[0][v] = q.x;
       wt[1][v] = q.y;
       wt[2][v] = q.z;
       wt[3][v] = q.w;
     }
-    // window of rows r0 .. r0+TT+2 (rows past their chunk end are masked per output)
-    float win[TT + 3][VEC];
-#pragma unroll
-    for (int i = 0; i < TT + 3; ++i) {
-      const int64_t r = r0 + i;
-      if (r < rows) {
-        const T* src = E + r * d + c0;
-        if constexpr (VEC == 8 && sizeof(T) == 2) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(src);
-          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float2 f = __bfloat1622float2(h[v]);
-            win[i][2 * v] = f.x;
-            win[i][2 * v + 1] = f.y;
-          }
-        } else {
-#pragma unroll
-          for (int v = 0; v < VEC; ++v) win[i][v] = to_f32<T>(src[v]);
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) win[i][v] = 0.0f;
-      }
-    }
+    int64_t pos = r0 % B;  // row r0's place in its chunk
 #pragma unroll
     for (int i = 0; i < TT; ++i) {
-      const int64_t r = r0 + i;
-      if (r >= rows) break;
-      const int64_t t = r % L;                      // position in its sequence
-      const int64_t room = (t / B + 1) * B - t;     // rows left in the chunk, counting t
-      float acc[VEC];
+      if (r0 + i >= rows) break;
+      const int64_t room = B - pos;  // rows left in the chunk, counting this one
+      float acc[8];
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) acc[v] = 0.0f;
+      for (int v = 0; v < 8; ++v) acc[v] = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (j < room) {
 #pragma unroll
-          for (int v = 0; v < VEC; ++v) acc[v] = fmaf(wt[j][v], win[i + j][v], acc[v]);
+          for (int v = 0; v < 4; ++v) {
+            const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&raw[i + j])[v]);
+            acc[2 * v] = fmaf(wt[j][2 * v], f.x, acc[2 * v]);
+            acc[2 * v + 1] = fmaf(wt[j][2 * v + 1], f.y, acc[2 * v + 1]);
+          }
         }
       }
-      T* dst = C + r * d + c0;
-      if constexpr (VEC == 8 && sizeof(T) == 2) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        *reinterpret_cast<uint4*>(dst) = o;
-      } else {
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) dst[v] = from_f32<T>(acc[v]);
-      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(C + (r0 + i) * d + c0) = o;
+      if (++pos == B) pos = 0;
     }
+  }
+}
+
+// Packed documents (launch_conv_varlen): the document holding row r, by
+// binary search in cu (cu[0] = 0 <= r < cu[n_docs]).
+__device__ __forceinline__ int64_t doc_of(const int64_t* cu, int64_t n_docs, int64_t r) {
+  int64_t lo = 0, hi = n_docs;  // cu[lo] <= r < cu[hi]
+  while (hi - lo > 1) {
+    const int64_t mid = (lo + hi) / 2;
+    if (cu[mid] <= r) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// conv_bf16x8_kernel over packed documents: chunks are counted from each
+// document's first row, and a document's last row ends its last chunk.
+template <int TT>
+__global__ void __launch_bounds__(kConvThreads, 3) conv_bf16x8_varlen_kernel(
+    const __nv_bfloat16* __restrict__ E, const float* __restrict__ w, __nv_bfloat16* __restrict__ C, int64_t rows,
+    const int64_t* __restrict__ cu, int64_t n_docs, int64_t B, int64_t d) {
+  const int64_t cgroups = d / 8;
+  const int64_t total = cgroups * ((rows + TT - 1) / TT);
+  for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
+       item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tb = item / cgroups;
+    const int64_t c0 = (item - tb * cgroups) * 8, r0 = tb * TT;
+    uint4 raw[TT + 3];
+#pragma unroll
+    for (int i = 0; i < TT + 3; ++i)
+      raw[i] = (r0 + i < rows) ? *reinterpret_cast<const uint4*>(E + (r0 + i) * d + c0) : make_uint4(0, 0, 0, 0);
+    float wt[4][8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 q = *reinterpret_cast<const float4*>(w + (c0 + v) * 4);
+      wt[0][v] = q.x;
+      wt[1][v] = q.y;
+      wt[2][v] = q.z;
+      wt[3][v] = q.w;
+    }
+    int64_t doc = doc_of(cu, n_docs, r0);
+    int64_t end = cu[doc + 1];
+    int64_t pos = (r0 - cu[doc]) % B;  // row r0's place in its chunk
+#pragma unroll
+    for (int i = 0; i < TT; ++i) {
+      const int64_t r = r0 + i;
+      if (r >= rows) break;
+      if (r == end) {  // the next document starts here
+        ++doc;
+        end = cu[doc + 1];
+        pos = 0;
+      }
+      const int64_t room = min(B - pos, end - r);  // rows left in the chunk, counting this one
+      float acc[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) acc[v] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < room) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&raw[i + j])[v]);
+            acc[2 * v] = fmaf(wt[j][2 * v], f.x, acc[2 * v]);
+            acc[2 * v + 1] = fmaf(wt[j][2 * v + 1], f.y, acc[2 * v + 1]);
+          }
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(C + r * d + c0) = o;
+      if (++pos == B) pos = 0;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) conv_scalar_varlen_kernel(const float* __restrict__ E,
+                                                                      const float* __restrict__ w,
+                                                                      float* __restrict__ C, int64_t rows,
+                                                                      const int64_t* __restrict__ cu, int64_t n_docs,
+                                                                      int64_t B, int64_t d) {
+  const int64_t total = rows * d;
+  for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
+       item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t c = item % d, r = item / d;
+    const int64_t doc = doc_of(cu, n_docs, r);
+    const int64_t room = min(B - (r - cu[doc]) % B, cu[doc + 1] - r);
+    float acc = 0.0f;
+    for (int j = 0; j < 4 && j < room; ++j) acc = fmaf(w[c * 4 + j], E[(r + j) * d + c], acc);
+    C[r * d + c] = acc;
   }
 }
 
@@ -116,20 +190,46 @@ __global__ void __launch_bounds__(kThreads) conv_kernel_scalar(const float* __re
 }
 
 // ------------------------------------------------------------------ residual
+// Where row r = e*B + i of the chunk goes, and what it holds (ResidualArgs).
+struct ResRow {
+  int64_t orow;  // row of O and V
+  float scale;   // of R
+  bool valid;    // inside its document
+};
+__device__ __forceinline__ ResRow residual_row(const ResidualArgs& a, int64_t r) {
+  const int64_t e = r / a.B, i = r % a.B;
+  const int b1 = static_cast<int>(e % a.nb1), b2 = static_cast<int>(e / a.nb1);
+  ResRow x;
+  x.orow = a.o_y0 + (a.otab ? a.otab[b1] : b1 * a.o_ys1) + b2 * a.o_ys2 + i;
+  x.valid = true;
+  x.scale = 1.0f;
+  if (a.lens) {
+    const int64_t n = min(a.B, a.lens[b1] - a.o_y0);
+    x.valid = i < n;
+    x.scale = static_cast<float>(a.B) / static_cast<float>(n);
+  }
+  return x;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) residual_kernel(const ResidualArgs a) {
   const int64_t per_entry = a.B * a.d;
   const int64_t total = per_entry * a.nb1 * a.nb2;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t e = idx / per_entry, rem = idx % per_entry;
-    const int64_t i = rem / a.d, c = rem % a.d;
-    const int b1 = static_cast<int>(e % a.nb1), b2 = static_cast<int>(e / a.nb1);
-    const int64_t orow = a.o_y0 + b1 * a.o_ys1 + b2 * a.o_ys2 + i;
+    const int64_t r = idx / a.d, c = idx % a.d;
+    const ResRow x = residual_row(a, r);
     const float v = a.acc[idx];
     a.acc[idx] = 0.0f;
-    static_cast<T*>(a.O)[orow * a.d + c] = from_f32<T>(v);
-    if (a.R) static_cast<T*>(a.R)[idx] = from_f32<T>(v - to_f32<T>(static_cast<const T*>(a.V)[orow * a.d + c]));
+    if (x.valid) static_cast<T*>(a.O)[x.orow * a.d + c] = from_f32<T>(v);
+    if (a.R) {
+      float rv = 0.0f;
+      if (x.valid) {
+        const float t = to_f32<T>(static_cast<const T*>(a.V)[x.orow * a.d + c]);
+        rv = x.scale * (a.r_from_v ? t : v - t);
+      }
+      static_cast<T*>(a.R)[idx] = from_f32<T>(rv);
+    }
   }
 }
 
@@ -146,18 +246,17 @@ __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kResRows;
   float4 x[kResRows][2];
   uint4 vr[kResRows];
-  int64_t orow[kResRows];
+  ResRow rw[kResRows];
 #pragma unroll
   for (int j = 0; j < kResRows; ++j) {
     const int64_t r = r0 + j;
     if (r >= rows) break;
-    const int64_t e = r / a.B, i = r % a.B;
-    const int b1 = static_cast<int>(e % a.nb1), b2 = static_cast<int>(e / a.nb1);
-    orow[j] = a.o_y0 + b1 * a.o_ys1 + b2 * a.o_ys2 + i;
+    rw[j] = residual_row(a, r);
     const float4* accp = reinterpret_cast<const float4*>(a.acc + r * a.d + c);
     x[j][0] = accp[0];
     x[j][1] = accp[1];
-    if (a.R) vr[j] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.V) + orow[j] * a.d + c);
+    if (a.R && rw[j].valid)
+      vr[j] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.V) + rw[j].orow * a.d + c);
   }
 #pragma unroll
   for (int j = 0; j < kResRows; ++j) {
@@ -167,21 +266,31 @@ __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs
     accp[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     accp[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 x0 = x[j][0], x1 = x[j][1];
-    uint4 o;
-    o.x = pack_bf16x2(x0.x, x0.y);
-    o.y = pack_bf16x2(x0.z, x0.w);
-    o.z = pack_bf16x2(x1.x, x1.y);
-    o.w = pack_bf16x2(x1.z, x1.w);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + orow[j] * a.d + c) = o;
+    if (rw[j].valid) {
+      uint4 o;
+      o.x = pack_bf16x2(x0.x, x0.y);
+      o.y = pack_bf16x2(x0.z, x0.w);
+      o.z = pack_bf16x2(x1.x, x1.y);
+      o.w = pack_bf16x2(x1.z, x1.w);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.O) + rw[j].orow * a.d + c) = o;
+    }
     if (a.R) {
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr[j]);
-      const float2 v0 = __bfloat1622float2(h[0]), v1 = __bfloat1622float2(h[1]), v2 = __bfloat1622float2(h[2]),
-                   v3 = __bfloat1622float2(h[3]);
+      float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (rw[j].valid) {
+        const float acc8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&vr[j]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 t = __bfloat1622float2(h[q]);
+          y[2 * q] = rw[j].scale * (a.r_from_v ? t.x : acc8[2 * q] - t.x);
+          y[2 * q + 1] = rw[j].scale * (a.r_from_v ? t.y : acc8[2 * q + 1] - t.y);
+        }
+      }
       uint4 rr;
-      rr.x = pack_bf16x2(x0.x - v0.x, x0.y - v0.y);
-      rr.y = pack_bf16x2(x0.z - v1.x, x0.w - v1.y);
-      rr.z = pack_bf16x2(x1.x - v2.x, x1.y - v2.y);
-      rr.w = pack_bf16x2(x1.z - v3.x, x1.w - v3.y);
+      rr.x = pack_bf16x2(y[0], y[1]);
+      rr.y = pack_bf16x2(y[2], y[3]);
+      rr.z = pack_bf16x2(y[4], y[5]);
+      rr.w = pack_bf16x2(y[6], y[7]);
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.R) + r * a.d + c) = rr;
     }
   }
@@ -345,13 +454,36 @@ cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t row
   if (rows <= 0) return cudaSuccess;
   LaunchMark mark(K_CONV, stream);
   if (bf16) {
+    if (d % 8 || L % B) return cudaErrorInvalidValue;
     constexpr int TT = 8;
     const int64_t items = (d / 8) * ((rows + TT - 1) / TT);
-    conv_kernel<__nv_bfloat16, 8, TT><<<grid_for(items), kThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(E), conv_w, static_cast<__nv_bfloat16*>(C), rows, L, B, d);
+    const int64_t waves = static_cast<int64_t>(device_sm_count()) * 3;
+    const int64_t blocks = std::min<int64_t>((items + kConvThreads - 1) / kConvThreads, waves * 4);
+    conv_bf16x8_kernel<TT><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), kConvThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(E), conv_w, static_cast<__nv_bfloat16*>(C), rows, B, d);
   } else {
     conv_kernel_scalar<<<grid_for(rows * d), kThreads, 0, stream>>>(static_cast<const float*>(E), conv_w,
                                                                      static_cast<float*>(C), rows, L, B, d);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_varlen(const void* E, const float* conv_w, void* C, int64_t rows, const int64_t* cu,
+                               int64_t n_docs, int64_t B, int64_t d, bool bf16, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  if (n_docs < 1 || B < 1 || !cu) return cudaErrorInvalidValue;
+  LaunchMark mark(K_CONV, stream);
+  if (bf16) {
+    if (d % 8) return cudaErrorInvalidValue;
+    constexpr int TT = 8;
+    const int64_t items = (d / 8) * ((rows + TT - 1) / TT);
+    const int64_t waves = static_cast<int64_t>(device_sm_count()) * 3;
+    const int64_t blocks = std::min<int64_t>((items + kConvThreads - 1) / kConvThreads, waves * 4);
+    conv_bf16x8_varlen_kernel<TT><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), kConvThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(E), conv_w, static_cast<__nv_bfloat16*>(C), rows, cu, n_docs, B, d);
+  } else {
+    conv_scalar_varlen_kernel<<<grid_for(rows * d), kThreads, 0, stream>>>(
+        static_cast<const float*>(E), conv_w, static_cast<float*>(C), rows, cu, n_docs, B, d);
   }
   return cudaGetLastError();
 }

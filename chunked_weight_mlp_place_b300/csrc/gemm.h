@@ -6,7 +6,8 @@
 //     epilogue(acc) -> outputs of batch entry b
 //
 // An operand is a window of a row-major matrix in global memory.  Its rows are
-// offset per batch entry: row = y0 + b1*ys1 + b2*ys2 + i.  For a K-major
+// offset per batch entry: row = y0 + b1*ys1 + b2*ys2 + i, or, where a table
+// of entry starts is given (packed documents), row = y0 + ytab[b1] + b2*ys2 + i.  For a K-major
 // operand, i is the M (or N) index and the K index runs along the columns; for
 // an MN-major operand, i is the K index and M (or N) runs along the columns.
 #pragma once
@@ -27,6 +28,7 @@ struct Operand {
   int64_t rows = 0, cols = 0, ld = 0;  // matrix extent and row stride (elements)
   int mn_major = 0;                    // 1: K runs along rows
   int64_t y0 = 0, ys1 = 0, ys2 = 0;    // per-batch row offsets
+  const int64_t* ytab = nullptr;       // device table replacing b1*ys1 (null: none)
 };
 
 struct OutRef {
@@ -34,7 +36,14 @@ struct OutRef {
   int64_t ld = 0;
   int64_t y0 = 0, ys1 = 0, ys2 = 0;  // row = y0 + b1*ys1 + b2*ys2 + m, column n
   int64_t rows = 0;                  // rows of the whole matrix (needed where TMA reads or writes it)
+  const int64_t* ytab = nullptr;     // device table replacing b1*ys1 (null: none)
 };
+
+// First row of batch entry (b1, b2) of an operand or output.
+template <typename R>
+__host__ __device__ __forceinline__ int64_t entry_row(const R& o, int b1, int b2) {
+  return o.y0 + (o.ytab ? o.ytab[b1] : b1 * o.ys1) + b2 * o.ys2;
+}
 
 // The planes are stored tile-major: blocks of kPlaneRows rows x kPlaneCols
 // columns, each block 4 KB contiguous (row r of a block at r * 32 bytes), the

@@ -10,15 +10,12 @@ namespace {
 
 constexpr int kBM = 64, kBN = 64, kBK = 16, kThreads = 256;
 
-__device__ __forceinline__ int64_t op_row(const Operand& o, int b1, int b2) {
-  return o.y0 + b1 * o.ys1 + b2 * o.ys2;
-}
 
 // Load a kBK x 64 slice of operand `o` (rows i0.., K range k0..) into s[k][i].
 __device__ __forceinline__ void load_tile(const Operand& o, int b1, int b2, int64_t i0, int64_t ext_i, int64_t k0,
                                           int64_t K, float (*s)[kBM + 4]) {
   const float* base = static_cast<const float*>(o.ptr);
-  const int64_t r0 = op_row(o, b1, b2);
+  const int64_t r0 = entry_row(o, b1, b2);
 #pragma unroll
   for (int it = 0; it < (kBK * kBM) / kThreads; ++it) {
     const int idx = threadIdx.x + it * kThreads;
@@ -72,7 +69,7 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmProblem p
     }
     __syncthreads();
   }
-  const int64_t drow0 = p.D.y0 + b1 * p.D.ys1 + b2 * p.D.ys2;
+  const int64_t drow0 = entry_row(p.D, b1, b2);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t m = m0 + ty * 4 + i;
@@ -94,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmProblem p
           atomicAdd(d, v);
           break;
         case EPI_AXPY: {
-          const int64_t srow = p.src.y0 + b1 * p.src.ys1 + b2 * p.src.ys2 + m;
+          const int64_t srow = entry_row(p.src, b1, b2) + m;
           const float w = static_cast<const float*>(p.src.ptr)[srow * p.src.ld + n] + p.alpha * v;
           *d = w;
           break;

@@ -163,12 +163,8 @@ __device__ __forceinline__ void epi_barrier(int group) {
   asm volatile("bar.sync %0, 128;" ::"r"(1 + group) : "memory");
 }
 
-__device__ __forceinline__ int64_t row_of(const Operand& o, int b1, int b2) {
-  return o.y0 + b1 * o.ys1 + b2 * o.ys2;
-}
-__device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) {
-  return o.y0 + b1 * o.ys1 + b2 * o.ys2;
-}
+__device__ __forceinline__ int64_t row_of(const Operand& o, int b1, int b2) { return entry_row(o, b1, b2); }
+__device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) { return entry_row(o, b1, b2); }
 
 // Issue the TMA copies of one operand tile (extent EXT along M or N, BK along
 // K).  With CTA pairs the completion is counted on the even CTA's barrier

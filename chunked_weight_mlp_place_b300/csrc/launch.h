@@ -74,10 +74,19 @@ cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream);  // fp3
 // C = chunk-padded depthwise conv of E (width 4, taps t..t+3), rows = batch*L.
 cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t rows, int64_t L, int64_t B, int64_t d,
                         bool bf16, cudaStream_t stream);
+// The same over packed documents: document i holds rows cu[i] .. cu[i+1]-1
+// (cu: n_docs+1 device int64, rising from 0 to rows); chunks of B tokens are
+// counted from each document's first row and the last one ends with it.
+cudaError_t launch_conv_varlen(const void* E, const float* conv_w, void* C, int64_t rows, const int64_t* cu,
+                               int64_t n_docs, int64_t B, int64_t d, bool bf16, cudaStream_t stream);
 
 // Per batch entry e = b1 + nb1*b2 and chunk row i < B:
-//   O[orow] = act(acc[e*B+i]);  R[e*B+i] = act(acc[e*B+i] - V[vrow])  (if R);  acc[e*B+i] = 0
-// with orow = o_y0 + b1*o_ys1 + b2*o_ys2 + i (V rows likewise).
+//   O[orow] = act(acc[e*B+i]);  R[e*B+i] = act(acc[e*B+i] - V[orow])  (if R);  acc[e*B+i] = 0
+// with orow = o_y0 + b1*o_ys1 + b2*o_ys2 + i (otab[b1] in place of b1*o_ys1 where given).
+// Packed documents (lens given): the chunk holds n = min(B, lens[b1] - o_y0)
+// tokens of entry b1's document; rows i >= n lie past its end (O and V are not
+// touched there, R = 0) and R is scaled by B/n, so a step of eta/B is the
+// chunk's mean.  r_from_v: R = V instead of O - V (the additive rule's step).
 struct ResidualArgs {
   float* acc = nullptr;
   const void* V = nullptr;
@@ -86,6 +95,9 @@ struct ResidualArgs {
   int64_t B = 0, d = 0;
   int nb1 = 1, nb2 = 1;
   int64_t o_y0 = 0, o_ys1 = 0, o_ys2 = 0;
+  const int64_t* otab = nullptr;
+  const int64_t* lens = nullptr;
+  int r_from_v = 0;
 };
 cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t stream);
 

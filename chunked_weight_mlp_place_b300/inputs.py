@@ -32,11 +32,11 @@ from typing import Dict, Optional, Sequence
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "generate", "round_to_bf16", "workload"]
+__all__ = ["Workload", "WORKLOADS", "generate", "round_to_bf16", "workload", "doc_boundaries", "DOC_MIXES"]
 
 # Stream indices inside the spawned SeedSequence; fixed so that adding a tensor
-# never changes the values of the others.
-_STREAMS = ("ids", "table", "X", "W_g", "W_u", "W_o0", "conv_w", "P")
+# never changes the values of the others (new streams go at the end).
+_STREAMS = ("ids", "table", "X", "W_g", "W_u", "W_o0", "conv_w", "P", "doc_len")
 
 
 @dataclasses.dataclass(frozen=True)
@@ -147,3 +147,26 @@ def generate(w: Workload, seed: int = 0, n_tokens: Optional[int] = None,
     if "P" in want:
         out["P"] = q(_normal(rng["P"], (w.d, w.d), 1.0 / w.d))
     return out
+
+
+# Packed-document length mixes (min, max tokens), log-uniform between them: a
+# long-tailed spread of document lengths, so that most documents end inside a
+# chunk and a few span many chunks.  "long128k" packs 128k tokens of documents
+# from 256 tokens to 32k (the long-context range of the write-ups' experiments).
+DOC_MIXES: Dict[str, tuple] = {
+    "long128k": (256, 32768),
+    "short": (1, 600),
+}
+
+
+def doc_boundaries(n_tokens: int, seed: int = 0, mix: str = "long128k") -> np.ndarray:
+    """Boundaries cu_seqlens (int64, 0 .. n_tokens, strictly rising) of documents
+    packed back to back: lengths drawn log-uniformly in the mix's range until
+    n_tokens is filled, the last one cut to fit."""
+    lo, hi = DOC_MIXES[mix]
+    rng = _streams(seed)["doc_len"]
+    cu = [0]
+    while cu[-1] < n_tokens:
+        n = int(round(float(np.exp(rng.uniform(np.log(lo), np.log(hi))))))
+        cu.append(min(n_tokens, cu[-1] + max(1, n)))
+    return np.asarray(cu, dtype=np.int64)

@@ -119,6 +119,36 @@ ipttt_status ipttt_layer_forward(const void* X, const void* E, const void* W_g, 
                                  const ipttt_dims* dims, ipttt_stream stream);
 
 /*
+ * Whole layer over packed documents of different lengths, the fast weight
+ * reset to W_o0 at every document boundary (In-Place TTT, itsolotime §3.2,
+ * "boundary reset": no document sees another's updates).
+ *
+ *   cu_seqlens [n_docs+1] int64, HOST array: document i holds rows
+ *                  cu_seqlens[i] .. cu_seqlens[i+1]-1; cu_seqlens[0] == 0 and
+ *                  the values rise strictly (every document has a token).
+ *                  Read during the call only.
+ *   X, E   [T, d]            act   T = cu_seqlens[n_docs], documents back to back
+ *   W_g, W_u, conv_w, P            as in ipttt_layer_forward
+ *   W_o0   [d_ff, d] fp32          shared initial fast weight, or [n_docs, d_ff, d]
+ *                                  if dims->w0_per_seq (document order)
+ *   B                              tokens per chunk (a multiple of 16 in bf16 mode)
+ *   O      [T, d]            act   out: O_k = Z_k W_k, chunk by chunk per document
+ *   W_final[n_docs, d_ff, d] fp32  out: each document's fast weight after its last chunk
+ *
+ * dims->batch is ignored.  Chunks are counted from each document's first
+ * token; a document's last chunk holds the n <= B tokens left, its step is
+ * normalised by n (the chunk mean, as for full chunks), and the conv reads
+ * zeros past the document's end as past any chunk's end.  Both rules run
+ * chunk by chunk here.  Errors: IPTTT_ERR_INVALID_ARG for a bad cu_seqlens, B
+ * or pointer (nothing is queued), else as ipttt_layer_forward.
+ */
+ipttt_status ipttt_layer_forward_varlen(const void* X, const void* E, const void* W_g, const void* W_u,
+                                        const float* W_o0, const float* conv_w, const void* P,
+                                        const int64_t* cu_seqlens, int64_t n_docs, int64_t B, float eta,
+                                        ipttt_rule rule, void* O, float* W_final,
+                                        const ipttt_dims* dims, ipttt_stream stream);
+
+/*
  * Targets only: V = Proj(Conv(E)) with the conv zero-padded at every chunk's
  * end (itsolotime §2.3; the next-token case is conv one-hot at tap 1, P = I).
  *

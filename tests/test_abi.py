@@ -79,6 +79,29 @@ def test_invalid_arguments_are_rejected_on_the_host(L):
     assert L.ipttt_chunk_forward(FAKE, FAKE, FAKE, 256, 48, 0.1, 0, FAKE, FAKE, ctypes.byref(dm), None) == E
 
 
+def _varlen(L, dm, cu, B=64, eta=0.1, rule=0):
+    arr = (ctypes.c_int64 * max(1, len(cu)))(*cu) if cu is not None else None
+    return L.ipttt_layer_forward_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, arr, max(0, len(cu or []) - 1),
+                                        B, eta, rule, FAKE, FAKE, ctypes.byref(dm), None)
+
+
+def test_varlen_arguments_are_checked_on_the_host(L):
+    E = _lib.ERR_INVALID_ARG
+    dm = _dims()
+    assert _varlen(L, dm, None) == E                                   # no boundaries
+    assert _varlen(L, dm, [1, 64]) == E                                # must start at 0
+    assert _varlen(L, dm, [0, 64, 64, 128]) == E                       # empty document
+    assert _varlen(L, dm, [0, 100, 90]) == E                           # falling boundary
+    assert _varlen(L, dm, [0, 64], B=24) == E                          # bf16 needs B % 16 == 0
+    assert _varlen(L, dm, [0, 64], B=0) == E
+    assert _varlen(L, dm, [0, 64], rule=3) == E
+    assert _varlen(L, dm, [0, 64], eta=float("inf")) == E
+    assert _varlen(L, dm, [0]) == _lib.OK                              # no documents: nothing to do
+    # valid boundaries, ragged lengths: the call reaches the device check
+    st = _varlen(L, dm, [0, 70, 75, 300])
+    assert st in (_lib.ERR_UNSUPPORTED, _lib.OK, _lib.ERR_INVALID_ARG)
+
+
 def test_fp32_mode_takes_any_sizes_on_the_host_checks(L):
     # fp32 accepts ragged sizes; with valid arguments the call reaches the device
     # check, which on a machine without a B300 says "unsupported".
