@@ -33,6 +33,7 @@ import numpy as np  # noqa: E402
 from chunked_weight_mlp_place_b300 import inputs  # noqa: E402
 
 METRIC = "fast-weight layer tokens/s and % roofline at d=2560,d_ff=9728,L=128k,B=1024"
+METRIC_DOCS = "packed-document fast-weight layer tokens/s and % roofline at d=2560,d_ff=9728,128k tokens,B=1024"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = {  # source files whose change invalidates a stored ncu traffic figure
     "gate_up": ["gemm_tc.cu", "common.cuh", "gemm.h"],
@@ -54,6 +55,8 @@ def parse_args():
     ap.add_argument("--B", type=int, default=None, help="chunk size override (the 4b_sweep points)")
     ap.add_argument("--L", type=int, default=None, help="sequence length override (small profiling cases)")
     ap.add_argument("--rule", choices=["mse", "add"], default="mse")
+    ap.add_argument("--docs", default=None, choices=sorted(inputs.DOC_MIXES),
+                    help="pack the tokens as documents of this length mix (fast weight reset per document)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle work for the CPU baseline")
@@ -73,31 +76,41 @@ def flops_per_token(w):
     return 8 * w.d * w.d_ff + 2 * w.d * w.d
 
 
-def roofline_tokens_per_s(w, peaks):
+def chunk_counts(w, cu=None):
+    """Chunks of every sequence (or packed document): the fast-weight updates a step makes."""
+    if cu is None:
+        return np.full(w.batch, w.L // w.B, dtype=np.int64)
+    return (np.diff(np.asarray(cu, np.int64)) + w.B - 1) // w.B
+
+
+def roofline_tokens_per_s(w, peaks, cu=None):
     """The layer's roofline: the slower of all GEMM FLOPs at the dense bf16 peak
     and one fp32 read + write of W_o per chunk at the HBM bandwidth."""
     T = w.batch * w.L
     t_flop = flops_per_token(w) * T / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = w.batch * (w.L // w.B) * 2 * w.d_ff * w.d * 4 / (peaks["hbm_gbs"] * 1e9)
+    t_hbm = int(chunk_counts(w, cu).sum()) * 2 * w.d_ff * w.d * 4 / (peaks["hbm_gbs"] * 1e9)
     return T / max(t_flop, t_hbm), ("tensor" if t_flop >= t_hbm else "hbm")
 
 
-def kernel_work(w, name):
-    """Algorithmic FLOPs and bytes of ONE launch of kernel `name` in a step."""
+def kernel_work(w, name, cu=None):
+    """Algorithmic FLOPs and bytes of ONE launch of kernel `name` in a step (with
+    packed documents, the step's total over its launches of that kernel)."""
     T = w.batch * w.L
-    chunk_tokens = w.batch * w.B
+    n_chunks = chunk_counts(w, cu)
+    steps = int(n_chunks.max())  # launches of the chunk kernels per step
+    w_bytes = int(n_chunks.sum()) * 2.0 * w.d_ff * w.d * 4
     if name == "gate_up":
         return 4.0 * w.d * w.d_ff * T, 0.0
     if name == "proj":
         return 2.0 * w.d * w.d * T, 0.0
     if name == "apply":
-        return 2.0 * w.d * w.d_ff * chunk_tokens, 0.0
+        return 2.0 * w.d * w.d_ff * T / steps, 0.0
     if name == "update":
-        return 2.0 * w.d * w.d_ff * chunk_tokens, w.batch * 2.0 * w.d_ff * w.d * 4
+        return 2.0 * w.d * w.d_ff * T / steps, w_bytes / steps
     if name == "conv":
         return 0.0, 2.0 * T * w.d * 2
     if name == "residual":
-        return 0.0, w.batch * w.B * w.d * (4 + 4 + 2 + 2 + 2)
+        return 0.0, T * w.d * (4 + 4 + 2 + 2 + 2) / steps
     return 0.0, 0.0
 
 
@@ -226,6 +239,29 @@ def oracle_sample(w, seconds):
     return n * one.B / tn, desc, blas_threads(), n * one.B
 
 
+def oracle_sample_docs(w, cu, seconds):
+    """Time the float64 oracle on whole documents of the packed workload,
+    shortest first, until about `seconds` of work.  Returns (tokens/s, description, cores)."""
+    from oracle import ipttt_oracle as orc  # test infrastructure: the CPU baseline only
+    lens = np.diff(cu)
+    order = np.argsort(lens, kind="stable")
+    a = inputs.generate(w.replace(batch=1), seed=0)
+    done, tok, el = 0, 0, 0.0
+    for i in order:
+        r = slice(int(cu[i]), int(cu[i + 1]))
+        s = time.perf_counter()
+        orc.layer_forward_varlen(a["X"][r], a["E"][r], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"],
+                                 [0, int(lens[i])], w.B, w.eta, "mse")
+        el += time.perf_counter() - s
+        tok += int(lens[i])
+        done += 1
+        if el >= seconds:
+            break
+    desc = (f"float64 oracle over the {done} shortest of {len(lens)} packed documents ({tok} tokens) of the "
+            f"{w.name} workload (d={w.d}, d_ff={w.d_ff}, B={w.B})")
+    return tok / el, desc, blas_threads()
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, w, rank, world):
     if rank != 0:
@@ -236,8 +272,12 @@ def run_reference(args, w, rank, world):
     rule = args.rule
 
     def step():
-        orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"], one.B, one.B,
-                          one.eta, rule)
+        if args.docs:  # one document of one chunk through the packed-document oracle
+            orc.layer_forward_varlen(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"],
+                                     [0, one.B], one.B, one.eta, rule)
+        else:
+            orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"], one.B, one.B,
+                              one.eta, rule)
 
     for _ in range(args.warmup):
         step()
@@ -249,19 +289,29 @@ def run_reference(args, w, rank, world):
     val = tok / el
     sample = f"one chunk ({one.B} tokens) of the {w.name} workload per step, float64 oracle"
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": metric_of(args), "value": val, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, args, world),
+        "config": config_of(w, args, world,
+                            inputs.doc_boundaries(w.batch * w.L, seed=0, mix=args.docs) if args.docs else None),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
-def config_of(w, args, world):
+def metric_of(args):
+    return METRIC_DOCS if args.docs else METRIC
+
+
+def config_of(w, args, world, cu=None):
+    docs = ""
+    if cu is not None:
+        lens = np.diff(cu)
+        docs = (f" packed as {len(lens)} documents of {int(lens.min())}..{int(lens.max())} tokens "
+                f"({args.docs} mix), fast weight reset per document;")
     return {"workload": f"{w.name}: batch={w.batch} L={w.L} B={w.B} d={w.d} d_ff={w.d_ff} rule={args.rule} "
-                        f"eta={w.eta} bf16 activations, fp32 fast weight",
+                        f"eta={w.eta}{docs} bf16 activations, fp32 fast weight",
             "batch_per_gpu": w.batch, "L": w.L, "B": w.B, "d": w.d, "d_ff": w.d_ff, "rule": args.rule,
             "parallelism": f"sequence-sharded x{world} (no collective)",
             "l2": "inputs (X, E, Z: >=0.6 GB each) exceed the 126 MB L2; no flush"}
@@ -312,9 +362,17 @@ def main():
     Wf = torch.empty(w.batch, w.d_ff, w.d, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    cu = inputs.doc_boundaries(T, seed=rank, mix=args.docs) if args.docs else None
+    if cu is not None:
+        Wf = torch.empty(len(cu) - 1, w.d_ff, w.d, dtype=torch.float32, device=dev)
+
     def step():
-        ip.layer_forward(d["X"], d["E"], d["W_g"], d["W_u"], d["W_o0"], d["conv_w"], d["P"], w.L, w.B, w.eta,
-                         args.rule, O, Wf, stream=stream)
+        if cu is not None:
+            ip.layer_forward_varlen(d["X"], d["E"], d["W_g"], d["W_u"], d["W_o0"], d["conv_w"], d["P"], cu, w.B,
+                                    w.eta, args.rule, O, Wf, stream=stream)
+        else:
+            ip.layer_forward(d["X"], d["E"], d["W_g"], d["W_u"], d["W_o0"], d["conv_w"], d["P"], w.L, w.B, w.eta,
+                             args.rule, O, Wf, stream=stream)
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -397,10 +455,10 @@ def main():
     if dom:
         n_launch, total_ms = kt[dom]
         avg_s = total_ms / n_launch / 1e3
-        fl, by = kernel_work(w, dom)
+        fl, by = kernel_work(w, dom, cu)
         t_f = fl / (peaks["bf16_tflops_sustained"] * 1e12) if fl else 0.0
         t_b = by / (peaks["hbm_gbs"] * 1e9) if by else 0.0
-        wk = f"{w.name}-B{w.B}-{args.rule}"
+        wk = f"{w.name}-B{w.B}-{args.rule}" + (f"-docs-{args.docs}" if args.docs else "")
         if t_f >= t_b:
             roof = {"bound": "tensor", "kernel": dom, "achieved": fl / avg_s / 1e12,
                     "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
@@ -415,17 +473,20 @@ def main():
     kernels = {k: {"launches": n, "total_ms": round(ms, 4), "avg_us": round(ms / n * 1e3, 2),
                    "share": round(ms / max(1e-9, sum(x[1] for x in kt.values())), 4)} for k, (n, ms) in kt.items()}
 
-    roof_tps, layer_bound = roofline_tokens_per_s(w, peaks)
+    roof_tps, layer_bound = roofline_tokens_per_s(w, peaks, cu)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        v, desc, cores, _ = oracle_sample(w, args.cpu_seconds)
+        if cu is not None:
+            v, desc, cores = oracle_sample_docs(w, cu, args.cpu_seconds)
+        else:
+            v, desc, cores, _ = oracle_sample(w, args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
     ms_step = elapsed_ms / args.steps
     out = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric_of(args), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, args, world),
+        "config": config_of(w, args, world, cu),
         "pct_roofline": 100.0 * value / world / roof_tps,
         "layer_roofline": {"tokens_per_s": roof_tps, "bound": layer_bound,
                            "tflops_achieved": flops_per_token(w) * value / 1e12,

@@ -45,3 +45,22 @@ def test_shapes_distributions_and_representability():
     assert not np.array_equal(inputs.round_to_bf16(a["W_o0"]), a["W_o0"])
     # E is the embedding-table gather of the ids
     assert a["ids"].min() >= 0 and a["ids"].max() < w.vocab
+
+
+def test_doc_boundaries_are_seeded_rising_and_cover_the_tokens():
+    for mix, (lo, hi) in inputs.DOC_MIXES.items():
+        cu = inputs.doc_boundaries(50000, seed=3, mix=mix)
+        np.testing.assert_array_equal(cu, inputs.doc_boundaries(50000, seed=3, mix=mix))
+        assert cu[0] == 0 and cu[-1] == 50000 and cu.dtype == np.int64
+        lens = np.diff(cu)
+        assert np.all(lens >= 1)
+        assert np.all(lens[:-1] >= lo) and np.all(lens <= hi + 1)   # the last one is cut to fit
+        assert not np.array_equal(cu, inputs.doc_boundaries(50000, seed=4, mix=mix))
+    # the document stream was appended: X still comes from the third of the
+    # original eight spawned streams
+    w = inputs.workload("tiny")
+    a = inputs.generate(w, seed=0, want=("X",))
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence(0).spawn(8)[2]))
+    X = g.standard_normal(size=(w.L, w.d), dtype=np.float32)
+    X = (X / np.sqrt(np.mean(np.square(X, dtype=np.float64), axis=1, keepdims=True) + 1e-6)).astype(np.float32)
+    np.testing.assert_array_equal(a["X"], X)
