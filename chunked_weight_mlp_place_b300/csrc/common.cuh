@@ -61,6 +61,19 @@ __device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float dep) {
 }
 // Order this thread's earlier generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses to the same memory.
+// 32-byte global load / store of one thread (address 32-byte aligned): a whole
+// sector per lane.
+__device__ __forceinline__ void ld_global_v8(const void* g, uint32_t (&v)[8]) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "l"(g));
+}
+__device__ __forceinline__ void st_global_v8(void* g, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(g), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -503,15 +503,13 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         return x;
       };
       const int sw = (trow >> 2) & 1;  // this row's 16-byte halves trade places (plane_index)
-      uint4 wh[4][2], wl[4][2];  // planes of the chunks in flight, indexed by chunk % 4
-      auto wload = [&](const TileW& t, int c, uint4 (&h)[2], uint4 (&l)[2]) {
+      // planes of the chunks in flight, indexed by chunk % 4: each row's 32 bytes as stored
+      // (halves swapped where sw is set), one 32-byte load per plane
+      uint32_t wh[4][8], wl[4][8];
+      auto wload = [&](const TileW& t, int c, uint32_t (&h)[8], uint32_t (&l)[8]) {
         if (t.hi == nullptr || t.cb0 + c >= p.w.cb) return;
-        const uint4* hp = reinterpret_cast<const uint4*>(t.hi + static_cast<int64_t>(c) * kPlaneBlock);
-        const uint4* lp = reinterpret_cast<const uint4*>(t.lo + static_cast<int64_t>(c) * kPlaneBlock);
-        h[0] = hp[sw];
-        h[1] = hp[sw ^ 1];
-        l[0] = __ldcs(lp + sw);
-        l[1] = __ldcs(lp + (sw ^ 1));
+        ld_global_v8(t.hi + static_cast<int64_t>(c) * kPlaneBlock, h);
+        ld_global_v8(t.lo + static_cast<int64_t>(c) * kPlaneBlock, l);
       };
       SegIter ahead = iter;
       Seg cur, nxt;
@@ -539,10 +537,15 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
             uint32_t(&rn)[WC] = (u & 1) ? ra : rb;
             tmem_wait_ld(r);
             if (j + 1 < GCH) tmem_ld_32x32b_x16(tbase + (c + 2) * WC, rn);
-            const uint32_t hw[8] = {wh[u][0].x, wh[u][0].y, wh[u][0].z, wh[u][0].w,
-                                    wh[u][1].x, wh[u][1].y, wh[u][1].z, wh[u][1].w};
-            const uint32_t lw[8] = {wl[u][0].x, wl[u][0].y, wl[u][0].z, wl[u][0].w,
-                                    wl[u][1].x, wl[u][1].y, wl[u][1].z, wl[u][1].w};
+            // columns 2q, 2q+1 sit in stored word q ^ 4*sw
+            uint32_t hw[8], lw[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              hw[q] = sw ? wh[u][q + 4] : wh[u][q];
+              hw[q + 4] = sw ? wh[u][q] : wh[u][q + 4];
+              lw[q] = sw ? wl[u][q + 4] : wl[u][q];
+              lw[q + 4] = sw ? wl[u][q] : wl[u][q + 4];
+            }
             // the planes of the group's chunk j + 3 go into the registers its chunk j - 1 used
             if (j + 3 < GCH)
               wload(tw, c + 6, wh[(u + 3) & 3], wl[(u + 3) & 3]);
@@ -557,12 +560,17 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
                        ho[q], lo[q]);
             }
             if (!failed && tw.hi != nullptr && tw.cb0 + c < p.w.cb) {
-              uint4* hp = reinterpret_cast<uint4*>(tw.hi + static_cast<int64_t>(c) * kPlaneBlock);
-              uint4* lp = reinterpret_cast<uint4*>(tw.lo + static_cast<int64_t>(c) * kPlaneBlock);
-              hp[sw] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
-              hp[sw ^ 1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
-              __stcs(lp + sw, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-              __stcs(lp + (sw ^ 1), make_uint4(lo[4], lo[5], lo[6], lo[7]));
+              // whole 32-byte rows, halves back in stored order
+              uint32_t hs[8], ls8[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                hs[q] = sw ? ho[q + 4] : ho[q];
+                hs[q + 4] = sw ? ho[q] : ho[q + 4];
+                ls8[q] = sw ? lo[q + 4] : lo[q];
+                ls8[q + 4] = sw ? lo[q] : lo[q + 4];
+              }
+              st_global_v8(tw.hi + static_cast<int64_t>(c) * kPlaneBlock, hs);
+              st_global_v8(tw.lo + static_cast<int64_t>(c) * kPlaneBlock, ls8);
             }
           }
         }
