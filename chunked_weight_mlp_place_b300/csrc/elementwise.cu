@@ -252,9 +252,10 @@ __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs
     const int64_t r = r0 + j;
     if (r >= rows) break;
     rw[j] = residual_row(a, r);
-    const float4* accp = reinterpret_cast<const float4*>(a.acc + r * a.d + c);
-    x[j][0] = accp[0];
-    x[j][1] = accp[1];
+    uint32_t w8[8];
+    ld_global_v8(a.acc + r * a.d + c, w8);  // the thread's 32 bytes of sums in one access
+    x[j][0] = make_float4(__uint_as_float(w8[0]), __uint_as_float(w8[1]), __uint_as_float(w8[2]), __uint_as_float(w8[3]));
+    x[j][1] = make_float4(__uint_as_float(w8[4]), __uint_as_float(w8[5]), __uint_as_float(w8[6]), __uint_as_float(w8[7]));
     if (a.R && rw[j].valid)
       vr[j] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.V) + rw[j].orow * a.d + c);
   }
@@ -262,9 +263,8 @@ __global__ void __launch_bounds__(128) residual_kernel_bf16x8(const ResidualArgs
   for (int j = 0; j < kResRows; ++j) {
     const int64_t r = r0 + j;
     if (r >= rows) break;
-    float4* accp = reinterpret_cast<float4*>(a.acc + r * a.d + c);
-    accp[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    accp[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    st_global_v8(a.acc + r * a.d + c, zero8);
     const float4 x0 = x[j][0], x1 = x[j][1];
     if (rw[j].valid) {
       uint4 o;
