@@ -48,7 +48,7 @@ import numpy as np
 
 __all__ = [
     "silu", "gated_activation", "chunk_conv", "make_targets", "mse_loss",
-    "chunk_step", "chunk_engine", "layer_forward", "layer_forward_varlen",
+    "chunk_step", "chunk_engine", "layer_forward", "layer_forward_varlen", "layers_forward",
 ]
 
 
@@ -213,3 +213,23 @@ def layer_forward_varlen(X: np.ndarray, E: np.ndarray, W_g: np.ndarray, W_u: np.
             O[rows], W = chunk_step(Z_k, V_k, W, eta, rule)
         W_fin[i] = W
     return O, W_fin
+
+
+def layers_forward(X: np.ndarray, E: np.ndarray, W_g: np.ndarray, W_u: np.ndarray, W_o0: np.ndarray,
+                   conv_w: np.ndarray, P: np.ndarray, L: int, B: int, eta: float,
+                   rule: str = "mse") -> Tuple[np.ndarray, np.ndarray]:
+    """Several layers' fast-weight MLPs over the same tokens: layer l takes its
+    own hidden states X[l] and its own W_g, W_u, W_o0, conv_w and P, and every
+    layer's target is built from the same token embeddings E (the In-Place TTT
+    layer is the MLP block of each layer it is put in: itsolotime §2.1; the
+    target of §2.3 reads the token embeddings).  Layers do not interact here.
+
+    X is (n_layers, batch*L, d); E (batch*L, d); W_g, W_u (n_layers, d, d_ff);
+    W_o0 (n_layers, d_ff, d) or (n_layers, batch, d_ff, d); conv_w
+    (n_layers, d, 4); P (n_layers, d, d).  Returns O (n_layers, batch*L, d) and
+    W_final (n_layers, batch, d_ff, d).
+    """
+    X = np.asarray(X, np.float64)
+    n = X.shape[0]
+    outs = [layer_forward(X[l], E, W_g[l], W_u[l], W_o0[l], conv_w[l], P[l], L, B, eta, rule) for l in range(n)]
+    return np.stack([o for o, _ in outs]), np.stack([w for _, w in outs])

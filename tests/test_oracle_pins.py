@@ -401,3 +401,51 @@ def test_varlen_rejects_bad_boundaries():
     for cu in ([0, 4, 4, 8], [1, 8], [0, 4, 9]):
         with pytest.raises(ValueError):
             orc.layer_forward_varlen(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"], t["conv_w"], t["P"], cu, 4, 0.1)
+
+
+# --------------------------------------------------- several layers at once
+def _layers(n=3, seed=21, L=12, d=4, d_ff=6, batch=2):
+    rng = np.random.default_rng(seed)
+    T = batch * L
+    return dict(X=rng.standard_normal((n, T, d)), E=rng.standard_normal((T, d)),
+                W_g=rng.standard_normal((n, d, d_ff)) / np.sqrt(d), W_u=rng.standard_normal((n, d, d_ff)) / np.sqrt(d),
+                W_o0=rng.standard_normal((n, d_ff, d)) / np.sqrt(d_ff),
+                conv_w=rng.standard_normal((n, d, 4)) * np.sqrt(0.5), P=rng.standard_normal((n, d, d)) / np.sqrt(d),
+                L=L)
+
+
+@pytest.mark.parametrize("rule", ["mse", "add"])
+def test_layers_match_per_layer_brute_force(rule):
+    """Each layer is its own gated MLP with its own fast weight: per layer and
+    sequence, the per-token brute force on that layer's Z (two matmuls and the
+    logistic function) and targets (per-token conv of the shared E)."""
+    t, B, eta = _layers(), 4, 0.2
+    L = t["L"]
+    O, W = orc.layers_forward(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"], t["conv_w"], t["P"], L, B, eta, rule)
+    assert O.shape == t["X"].shape and W.shape == (3, 2) + t["W_o0"].shape[1:]
+    for l in range(3):
+        a = t["X"][l] @ t["W_g"][l]
+        Z = a * scipy.special.expit(a) * (t["X"][l] @ t["W_u"][l])
+        starts = np.arange(0, 2 * L, L)
+        V = _targets_per_token(t["E"], t["conv_w"][l], t["P"][l], starts, starts + L, B)
+        for s in range(2):
+            r = slice(s * L, (s + 1) * L)
+            Ob, Wb = _brute_force(Z[r], V[r], t["W_o0"][l], B, eta, rule)
+            np.testing.assert_allclose(O[l][r], Ob, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(W[l][s], Wb, rtol=1e-12, atol=1e-12)
+
+
+def test_layers_do_not_interact():
+    t = _layers()
+    O, W = orc.layers_forward(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"], t["conv_w"], t["P"], t["L"], 4, 0.2)
+    t2 = dict(t)
+    t2["W_g"] = t["W_g"].copy()
+    t2["W_g"][1] *= 1.5
+    t2["P"] = t["P"].copy()
+    t2["P"][1] *= -1.0
+    O2, W2 = orc.layers_forward(t2["X"], t2["E"], t2["W_g"], t2["W_u"], t2["W_o0"], t2["conv_w"], t2["P"],
+                                t["L"], 4, 0.2)
+    for l in (0, 2):
+        np.testing.assert_array_equal(O2[l], O[l])
+        np.testing.assert_array_equal(W2[l], W[l])
+    assert not np.allclose(O2[1], O[1])
