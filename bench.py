@@ -34,6 +34,7 @@ from chunked_weight_mlp_place_b300 import inputs  # noqa: E402
 
 METRIC = "fast-weight layer tokens/s and % roofline at d=2560,d_ff=9728,L=128k,B=1024"
 METRIC_DOCS = "packed-document fast-weight layer tokens/s and % roofline at d=2560,d_ff=9728,128k tokens,B=1024"
+METRIC_LAYERS = "multi-layer fast-weight MLP (token x layer)/s and % roofline, one call per step for all layers"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = {  # source files whose change invalidates a stored ncu traffic figure
     "gate_up": ["gemm_tc.cu", "common.cuh", "gemm.h"],
@@ -55,6 +56,8 @@ def parse_args():
     ap.add_argument("--B", type=int, default=None, help="chunk size override (the 4b_sweep points)")
     ap.add_argument("--L", type=int, default=None, help="sequence length override (small profiling cases)")
     ap.add_argument("--rule", choices=["mse", "add"], default="mse")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="this many layers' fast-weight MLPs in one call per step (0: one layer)")
     ap.add_argument("--docs", default=None, choices=sorted(inputs.DOC_MIXES),
                     help="pack the tokens as documents of this length mix (fast weight reset per document)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -85,16 +88,23 @@ def chunk_counts(w, cu=None):
 
 def roofline_tokens_per_s(w, peaks, cu=None):
     """The layer's roofline: the slower of all GEMM FLOPs at the dense bf16 peak
-    and one fp32 read + write of W_o per chunk at the HBM bandwidth."""
+    and one fp32 read + write of W_o per chunk at the HBM bandwidth (per layer:
+    several layers scale both terms alike)."""
     T = w.batch * w.L
     t_flop = flops_per_token(w) * T / (peaks["bf16_tflops"] * 1e12)
     t_hbm = int(chunk_counts(w, cu).sum()) * 2 * w.d_ff * w.d * 4 / (peaks["hbm_gbs"] * 1e9)
     return T / max(t_flop, t_hbm), ("tensor" if t_flop >= t_hbm else "hbm")
 
 
-def kernel_work(w, name, cu=None):
+def kernel_work(w, name, cu=None, layers=1):
     """Algorithmic FLOPs and bytes of ONE launch of kernel `name` in a step (with
-    packed documents, the step's total over its launches of that kernel)."""
+    packed documents, the step's total over its launches of that kernel; with
+    several layers, every launch covers all of them)."""
+    fl, by = _kernel_work_one(w, name, cu)
+    return fl * layers, by * layers
+
+
+def _kernel_work_one(w, name, cu=None):
     T = w.batch * w.L
     n_chunks = chunk_counts(w, cu)
     steps = int(n_chunks.max())  # launches of the chunk kernels per step
@@ -287,21 +297,22 @@ def run_reference(args, w, rank, world):
     el = time.perf_counter() - t0
     tok = args.steps * one.B
     val = tok / el
+    unit = "(token x layer)/s" if args.layers else "tokens/s"  # one layer of one chunk per step
     sample = f"one chunk ({one.B} tokens) of the {w.name} workload per step, float64 oracle"
     print(json.dumps({
-        "impl": "reference", "metric": metric_of(args), "value": val, "unit": "tokens/s", "n_gpus": world,
+        "impl": "reference", "metric": metric_of(args), "value": val, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, args, world,
                             inputs.doc_boundaries(w.batch * w.L, seed=0, mix=args.docs) if args.docs else None),
-        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": val, "unit": unit, "cores": blas_threads(), "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
 def metric_of(args):
-    return METRIC_DOCS if args.docs else METRIC
+    return METRIC_LAYERS if args.layers else (METRIC_DOCS if args.docs else METRIC)
 
 
 def config_of(w, args, world, cu=None):
@@ -310,6 +321,8 @@ def config_of(w, args, world, cu=None):
         lens = np.diff(cu)
         docs = (f" packed as {len(lens)} documents of {int(lens.min())}..{int(lens.max())} tokens "
                 f"({args.docs} mix), fast weight reset per document;")
+    if args.layers:
+        docs += f" {args.layers} layers (own weights and hidden states each, shared token embeddings);"
     return {"workload": f"{w.name}: batch={w.batch} L={w.L} B={w.B} d={w.d} d_ff={w.d_ff} rule={args.rule} "
                         f"eta={w.eta}{docs} bf16 activations, fp32 fast weight",
             "batch_per_gpu": w.batch, "L": w.L, "B": w.B, "d": w.d, "d_ff": w.d_ff, "rule": args.rule,
@@ -348,7 +361,14 @@ def main():
     ip.lib()
 
     peaks, peaks_kind = load_peaks()
+    nl = max(0, args.layers)
     a = inputs.generate(w, seed=1000 + rank)
+    if nl:  # each layer its own hidden states and weights, drawn from seeds of their own
+        per = [a] + [inputs.generate(w, seed=1000 + rank + 7919 * l, want=("X", "W_g", "W_u", "W_o0", "conv_w", "P"))
+                     for l in range(1, nl)]
+        for k in ("X", "W_g", "W_u", "W_o0", "conv_w", "P"):
+            a[k] = np.stack([q[k] for q in per])
+        del per
     bf = torch.bfloat16
     dev = torch.device("cuda", local_rank)
     h = {k: torch.from_numpy(a[k]) for k in ("X", "E", "W_g", "W_u", "P")}
@@ -358,8 +378,8 @@ def main():
     del a
     d = {k: v.to(dev) for k, v in h.items()}
     T = w.batch * w.L
-    O = torch.empty(T, w.d, dtype=bf, device=dev)
-    Wf = torch.empty(w.batch, w.d_ff, w.d, dtype=torch.float32, device=dev)
+    O = torch.empty(((nl,) if nl else ()) + (T, w.d), dtype=bf, device=dev)
+    Wf = torch.empty(((nl,) if nl else ()) + (w.batch, w.d_ff, w.d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     cu = inputs.doc_boundaries(T, seed=rank, mix=args.docs) if args.docs else None
@@ -367,7 +387,10 @@ def main():
         Wf = torch.empty(len(cu) - 1, w.d_ff, w.d, dtype=torch.float32, device=dev)
 
     def step():
-        if cu is not None:
+        if nl:
+            ip.layers_forward(d["X"], d["E"], d["W_g"], d["W_u"], d["W_o0"], d["conv_w"], d["P"], w.L, w.B, w.eta,
+                              args.rule, O, Wf, stream=stream)
+        elif cu is not None:
             ip.layer_forward_varlen(d["X"], d["E"], d["W_g"], d["W_u"], d["W_o0"], d["conv_w"], d["P"], cu, w.B,
                                     w.eta, args.rule, O, Wf, stream=stream)
         else:
@@ -406,8 +429,27 @@ def main():
         t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    tokens = world * T * args.steps
+    tokens = world * T * args.steps * max(1, nl)
     value = tokens / (elapsed_ms / 1e3)
+
+    # ---- several layers: the same layers as one call each, for comparison
+    sequential = None
+    if nl:
+        def step_seq():
+            for l in range(nl):
+                ip.layer_forward(d["X"][l], d["E"], d["W_g"][l], d["W_u"][l], d["W_o0"][l], d["conv_w"][l],
+                                 d["P"][l], w.L, w.B, w.eta, args.rule, O[l], Wf[l], stream=stream)
+
+        step_seq()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step_seq()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_seq = e0.elapsed_time(e1)
+        sequential = {"value": world * T * nl * args.steps / (t_seq / 1e3), "unit": "(token x layer)/s",
+                      "ms_per_step": t_seq / args.steps, "launches_per_step": ip.last_launch_count() * nl}
 
     # ---- end to end: pinned host inputs in, O and W_final out, every step
     e2e = None
@@ -441,7 +483,8 @@ def main():
             t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             t_e2e = float(t.item())
-        e2e = {"value": world * T * n_e2e / (t_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": world * T * max(1, nl) * n_e2e / (t_e2e / 1e3),
+               "unit": "(token x layer)/s" if nl else "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     if rank != 0:
@@ -455,7 +498,7 @@ def main():
     if dom:
         n_launch, total_ms = kt[dom]
         avg_s = total_ms / n_launch / 1e3
-        fl, by = kernel_work(w, dom, cu)
+        fl, by = kernel_work(w, dom, cu, max(1, nl))
         t_f = fl / (peaks["bf16_tflops_sustained"] * 1e12) if fl else 0.0
         t_b = by / (peaks["hbm_gbs"] * 1e9) if by else 0.0
         wk = f"{w.name}-B{w.B}-{args.rule}" + (f"-docs-{args.docs}" if args.docs else "")
@@ -495,6 +538,9 @@ def main():
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
+    if nl:
+        out["unit"] = "(token x layer)/s"
+        out["one_call_per_layer"] = sequential
     print(json.dumps(out))
     if dist:
         dist.destroy_process_group()

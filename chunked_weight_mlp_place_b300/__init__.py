@@ -6,6 +6,6 @@ in-tree build script and the seeded synthetic input generator.
 """
 from ._lib import (  # noqa: F401
     BF16, FP32, RULE_ADD, RULE_MSE, IptttError, chunk_forward, gate_up, kernel_timing, kernel_timing_read,
-    last_launch_count, layer_forward, layer_forward_varlen,
+    last_launch_count, layer_forward, layer_forward_varlen, layers_forward,
     lib, make_targets, make_targets_noalloc, release, status_string, sync_status, version, workspace_size,
 )

@@ -25,7 +25,7 @@ EXPORTS = (
     "ipttt_layer_forward", "ipttt_make_targets", "ipttt_gate_up", "ipttt_chunk_forward",
     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
     "ipttt_status_string", "ipttt_version", "ipttt_kernel_timing", "ipttt_kernel_timing_read",
-    "ipttt_kernel_name", "ipttt_make_targets_noalloc", "ipttt_layer_forward_varlen",
+    "ipttt_kernel_name", "ipttt_make_targets_noalloc", "ipttt_layer_forward_varlen", "ipttt_layers_forward",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
 KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy")
@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int32
         dp = ctypes.POINTER(Dims)
         L.ipttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
+        L.ipttt_layers_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, i32, vp, vp, dp, vp]
         L.ipttt_layer_forward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(i64), i64, i64, f32,
                                                  i32, vp, vp, dp, vp]
         L.ipttt_make_targets.argtypes = [vp, vp, vp, vp, i64, i64, dp, vp]
@@ -177,6 +178,25 @@ def layer_forward_varlen(X, E, W_g, W_u, W_o0, conv_w, P, cu_seqlens, B: int, et
         cu_arr, int(n_docs), int(B), float(eta), _RULES[rule], _ptr(O, "O", act),
         _ptr(W_final, "W_final", torch.float32), ctypes.byref(dm), _stream(stream))
     _check(st, "ipttt_layer_forward_varlen")
+
+
+def layers_forward(X, E, W_g, W_u, W_o0, conv_w, P, L: int, B: int, eta: float, rule, O, W_final,
+                   stream=None) -> None:
+    """ipttt_layers_forward on tensors: X (n_layers, batch*L, d); E (batch*L, d);
+    W_g, W_u (n_layers, d, d_ff); W_o0 (n_layers, d_ff, d) or
+    (n_layers, batch, d_ff, d) fp32; conv_w (n_layers, d, 4) fp32; P (n_layers, d, d);
+    O (n_layers, batch*L, d) out; W_final (n_layers, batch, d_ff, d) fp32 out."""
+    torch = _torch()
+    act = X.dtype
+    n_layers, d, d_ff = W_g.shape
+    batch = X.shape[1] // L if L else W_final.shape[1]
+    dm = dims(batch, d, d_ff, _dtype_code(X), 1 if W_o0.dim() == 4 else 0)
+    st = lib().ipttt_layers_forward(
+        _ptr(X, "X", act), _ptr(E, "E", act), _ptr(W_g, "W_g", act), _ptr(W_u, "W_u", act),
+        _ptr(W_o0, "W_o0", torch.float32), _ptr(conv_w, "conv_w", torch.float32), _ptr(P, "P", act),
+        int(n_layers), int(L), int(B), float(eta), _RULES[rule], _ptr(O, "O", act),
+        _ptr(W_final, "W_final", torch.float32), ctypes.byref(dm), _stream(stream))
+    _check(st, "ipttt_layers_forward")
 
 
 def make_targets(E, conv_w, P, V, L: int, B: int, stream=None) -> None:

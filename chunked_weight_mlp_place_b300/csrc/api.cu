@@ -843,6 +843,92 @@ ipttt_status ipttt_layer_forward_varlen(const void* X, const void* E, const void
                     static_cast<cudaStream_t>(stream));
 }
 
+ipttt_status ipttt_layers_forward(const void* X, const void* E, const void* W_g, const void* W_u, const float* W_o0,
+                                  const float* conv_w, const void* P, int64_t n_layers, int64_t L, int64_t B, float eta,
+                                  ipttt_rule rule, void* O, float* W_final, const ipttt_dims* dims,
+                                  ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, true));
+  IPTTT_TRY(check_chunking(dims, L, B));
+  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta) || n_layers < 0)
+    return IPTTT_ERR_INVALID_ARG;
+  if (n_layers == 0 || dims->batch == 0) return IPTTT_OK;
+  const int64_t batch = dims->batch, d = dims->d, dff = dims->d_ff, nw = dff * d;
+  const int64_t entries = n_layers * batch, T = batch * L, NT = n_layers * T;
+  // token rows, weight rows and fast-weight rows of all layers are TMA coordinates (int32)
+  if (NT > (int64_t{1} << 31) || dff * entries > (int64_t{1} << 31) || n_layers * d > (int64_t{1} << 31))
+    return IPTTT_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Layer l, sequence s is entry l*batch + s of the chunk engine: its rows of Z, V
+  // and O sit at (l*batch + s)*L, and its fast weight at W_final[l][s].
+  if (L == 0) {
+    IPTTT_TRY(check_ptrs({static_cast<const void*>(W_o0), static_cast<const void*>(W_final)}));
+    if (dims->w0_per_seq) {
+      IPTTT_CUDA(launch_copy_w(W_o0, nw, W_final, entries, nw, st));
+    } else {
+      for (int64_t l = 0; l < n_layers; ++l)
+        IPTTT_CUDA(launch_copy_w(W_o0 + l * nw, 0, W_final + l * batch * nw, batch, nw, st));
+    }
+    return IPTTT_OK;
+  }
+  IPTTT_TRY(check_ptrs({X, E, W_g, W_u, static_cast<const void*>(W_o0), static_cast<const void*>(conv_w), P,
+                        static_cast<const void*>(O), static_cast<const void*>(W_final)}));
+  const bool bf16 = dims->dtype == IPTTT_BF16;
+  ipttt_dims dm = *dims;
+  dm.batch = entries;
+  dm.w0_per_seq = 1;
+  const size_t es = act_size(dims);
+  Carve c;
+  const size_t z_off = c.take<uint8_t>(NT * dff * static_cast<int64_t>(es));
+  const size_t v_off = c.take<uint8_t>(NT * d * static_cast<int64_t>(es));
+  const size_t c_off = c.take<uint8_t>(NT * d * static_cast<int64_t>(es));
+  const EngineLayout lay = engine_layout(&dm, L, B, rule, c.off);
+  void* wsv = nullptr;
+  IPTTT_TRY(pool_reserve(lay.total, &wsv));
+  uint8_t* ws = static_cast<uint8_t*>(wsv);
+  // gate of every layer: one GEMM over the layers (batch entry = layer)
+  {
+    GemmProblem p;
+    p.M = T;
+    p.N = dff;
+    p.K = d;
+    p.nb1 = static_cast<int>(n_layers);
+    p.A = mat(X, NT, d, 0, 0, T);
+    p.B = mat(W_g, n_layers * d, dff, 1, 0, d);
+    p.B2 = mat(W_u, n_layers * d, dff, 1, 0, d);
+    p.epi = EPI_GATE;
+    p.kind = K_GATE;
+    p.out_bf16 = bf16;
+    p.D = out(ws + z_off, dff, 0, T, 0, NT);
+    IPTTT_CUDA(gemm(p, bf16, st));
+  }
+  // targets of every layer from the shared embeddings: one conv launch, one projection GEMM
+  IPTTT_CUDA(launch_conv(E, conv_w, ws + c_off, NT, L, B, d, bf16, st, T));
+  {
+    GemmProblem p;
+    p.M = T;
+    p.N = d;
+    p.K = d;
+    p.nb1 = static_cast<int>(n_layers);
+    p.A = mat(ws + c_off, NT, d, 0, 0, T);
+    p.B = mat(P, n_layers * d, d, 1, 0, d);
+    p.epi = EPI_STORE;
+    p.kind = K_PROJ;
+    p.out_bf16 = bf16;
+    p.D = out(ws + v_off, d, 0, T, 0, NT);
+    IPTTT_CUDA(gemm(p, bf16, st));
+  }
+  // each entry's initial fast weight: a per-layer W_o0 shared by the sequences is copied into
+  // W_final first, which the engine reads before it writes its result there
+  const float* W0 = W_o0;
+  if (!dims->w0_per_seq && batch > 1) {
+    for (int64_t l = 0; l < n_layers; ++l)
+      IPTTT_CUDA(launch_copy_w(W_o0 + l * nw, 0, W_final + l * batch * nw, batch, nw, st));
+    W0 = W_final;
+  }
+  return run_engine(ws + z_off, ws + v_off, W0, L, B, eta, rule, O, W_final, &dm, ws, lay, st);
+}
+
 ipttt_status ipttt_sync_status(ipttt_stream stream) {
   const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {

@@ -24,28 +24,33 @@ int grid_for(int64_t work_items) {
 // Sequences are whole chunks (L % B == 0), so chunks start at the multiples of
 // B in the flattened rows.  One thread: 8 channels (16 bytes) x TT consecutive
 // tokens, sliding a 4-row window; its position inside the chunk is computed
-// once and stepped along the rows.
+// once and stepped along the rows.  Several layers at once: output row r is
+// row r % e_rows of E under layer r / e_rows's taps (e_rows a multiple of B
+// and of TT, so an item stays in one layer and its taps past a layer's end
+// are past a chunk end).
 constexpr int kConvThreads = 128;  // three blocks per SM at up to 170 registers a thread
 template <int TT>
 __global__ void __launch_bounds__(kConvThreads, 3) conv_bf16x8_kernel(const __nv_bfloat16* __restrict__ E,
                                                                const float* __restrict__ w,
                                                                __nv_bfloat16* __restrict__ C, int64_t rows,
-                                                               int64_t B, int64_t d) {
+                                                               int64_t B, int64_t d, int64_t e_rows) {
   const int64_t cgroups = d / 8;
   const int64_t total = cgroups * ((rows + TT - 1) / TT);
   for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
        item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t tb = item / cgroups;
     const int64_t c0 = (item - tb * cgroups) * 8, r0 = tb * TT;
+    const int64_t layer = r0 / e_rows, er0 = r0 - layer * e_rows;  // the item's layer and its first E row
     // window of rows r0 .. r0+TT+2, all loads in flight before any arithmetic
     uint4 raw[TT + 3];
 #pragma unroll
     for (int i = 0; i < TT + 3; ++i)
-      raw[i] = (r0 + i < rows) ? *reinterpret_cast<const uint4*>(E + (r0 + i) * d + c0) : make_uint4(0, 0, 0, 0);
+      raw[i] = (r0 + i < rows && er0 + i < e_rows) ? *reinterpret_cast<const uint4*>(E + (er0 + i) * d + c0)
+                                                   : make_uint4(0, 0, 0, 0);
     float wt[4][8];
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
-      const float4 q = *reinterpret_cast<const float4*>(w + (c0 + v) * 4);
+      const float4 q = *reinterpret_cast<const float4*>(w + (layer * d + c0 + v) * 4);
       wt[0][v] = q.x;
       wt[1][v] = q.y;
       wt[2][v] = q.z;
@@ -173,18 +178,21 @@ __global__ void __launch_bounds__(kThreads) conv_scalar_varlen_kernel(const floa
   }
 }
 
-// Scalar-weight variant for fp32 mode with any d: one channel per thread.
+// Scalar-weight variant for fp32 mode with any d: one channel per thread
+// (several layers as in conv_bf16x8_kernel).
 __global__ void __launch_bounds__(kThreads) conv_kernel_scalar(const float* __restrict__ E,
                                                                const float* __restrict__ w, float* __restrict__ C,
-                                                               int64_t rows, int64_t L, int64_t B, int64_t d) {
+                                                               int64_t rows, int64_t L, int64_t B, int64_t d,
+                                                               int64_t e_rows) {
   const int64_t total = rows * d;
   for (int64_t item = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; item < total;
        item += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t c = item % d, r = item / d;
-    const int64_t t = r % L;
+    const int64_t layer = r / e_rows, er = r - layer * e_rows;
+    const int64_t t = er % L;
     const int64_t room = (t / B + 1) * B - t;
     float acc = 0.0f;
-    for (int j = 0; j < 4 && j < room; ++j) acc = fmaf(w[c * 4 + j], E[(r + j) * d + c], acc);
+    for (int j = 0; j < 4 && j < room; ++j) acc = fmaf(w[(layer * d + c) * 4 + j], E[(er + j) * d + c], acc);
     C[r * d + c] = acc;
   }
 }
@@ -450,20 +458,22 @@ __global__ void __launch_bounds__(kThreads) group_scan_planes_kernel(const float
 }  // namespace
 
 cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t rows, int64_t L, int64_t B, int64_t d,
-                        bool bf16, cudaStream_t stream) {
+                        bool bf16, cudaStream_t stream, int64_t e_rows) {
   if (rows <= 0) return cudaSuccess;
+  if (e_rows <= 0) e_rows = rows;
+  if (rows % e_rows || e_rows % L || L % B) return cudaErrorInvalidValue;
   LaunchMark mark(K_CONV, stream);
   if (bf16) {
-    if (d % 8 || L % B) return cudaErrorInvalidValue;
+    if (d % 8 || e_rows % 8) return cudaErrorInvalidValue;
     constexpr int TT = 8;
     const int64_t items = (d / 8) * ((rows + TT - 1) / TT);
     const int64_t waves = static_cast<int64_t>(device_sm_count()) * 3;
     const int64_t blocks = std::min<int64_t>((items + kConvThreads - 1) / kConvThreads, waves * 4);
     conv_bf16x8_kernel<TT><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), kConvThreads, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(E), conv_w, static_cast<__nv_bfloat16*>(C), rows, B, d);
+        static_cast<const __nv_bfloat16*>(E), conv_w, static_cast<__nv_bfloat16*>(C), rows, B, d, e_rows);
   } else {
     conv_kernel_scalar<<<grid_for(rows * d), kThreads, 0, stream>>>(static_cast<const float*>(E), conv_w,
-                                                                     static_cast<float*>(C), rows, L, B, d);
+                                                                     static_cast<float*>(C), rows, L, B, d, e_rows);
   }
   return cudaGetLastError();
 }

@@ -72,8 +72,11 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream);    // bf1
 cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream);  // fp32 operands, CUDA cores
 
 // C = chunk-padded depthwise conv of E (width 4, taps t..t+3), rows = batch*L.
+// Several layers at once: rows = n_layers * e_rows, output row r is E row
+// r % e_rows under the taps conv_w[r / e_rows] (conv_w: n_layers x d x 4);
+// e_rows <= 0 means one layer (e_rows = rows).
 cudaError_t launch_conv(const void* E, const float* conv_w, void* C, int64_t rows, int64_t L, int64_t B, int64_t d,
-                        bool bf16, cudaStream_t stream);
+                        bool bf16, cudaStream_t stream, int64_t e_rows = 0);
 // The same over packed documents: document i holds rows cu[i] .. cu[i+1]-1
 // (cu: n_docs+1 device int64, rising from 0 to rows); chunks of B tokens are
 // counted from each document's first row and the last one ends with it.

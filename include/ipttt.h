@@ -149,6 +149,35 @@ ipttt_status ipttt_layer_forward_varlen(const void* X, const void* E, const void
                                         const ipttt_dims* dims, ipttt_stream stream);
 
 /*
+ * Several layers' fast-weight MLPs over the same tokens in one call: every
+ * step is one launch for all layers (the gate and projection GEMMs batched over
+ * the layers, one conv launch, and each chunk's apply / residual / update over
+ * all layers and sequences).  Layer l takes its own hidden states and weights;
+ * every layer's target is built from the same token embeddings E (the In-Place
+ * TTT layer is the MLP block of each layer it is put in, itsolotime §2.1; its
+ * target reads the token embeddings, §2.3).  Layers do not interact.
+ *
+ *   X      [n_layers, batch*L, d]     act   hidden states entering each layer's MLP
+ *   E      [batch*L, d]               act   token embeddings, shared by the layers
+ *   W_g    [n_layers, d, d_ff]        act   per-layer gate projections
+ *   W_u    [n_layers, d, d_ff]        act   per-layer up projections
+ *   W_o0   [n_layers, d_ff, d] fp32         per-layer initial fast weight, or
+ *                                           [n_layers, batch, d_ff, d] if dims->w0_per_seq
+ *   conv_w [n_layers, d, 4] fp32            per-layer conv taps
+ *   P      [n_layers, d, d]           act   per-layer target projections
+ *   O      [n_layers, batch*L, d]     act   out
+ *   W_final[n_layers, batch, d_ff, d] fp32  out (also the scratch that holds each
+ *                                           sequence's start when W_o0 is per layer)
+ *
+ * L, B, eta, rule and errors as in ipttt_layer_forward; n_layers == 0 does
+ * nothing.  W_o0 must not overlap W_final.
+ */
+ipttt_status ipttt_layers_forward(const void* X, const void* E, const void* W_g, const void* W_u,
+                                  const float* W_o0, const float* conv_w, const void* P, int64_t n_layers,
+                                  int64_t L, int64_t B, float eta, ipttt_rule rule, void* O, float* W_final,
+                                  const ipttt_dims* dims, ipttt_stream stream);
+
+/*
  * Targets only: V = Proj(Conv(E)) with the conv zero-padded at every chunk's
  * end (itsolotime §2.3; the next-token case is conv one-hot at tap 1, P = I).
  *

@@ -102,6 +102,25 @@ def test_varlen_arguments_are_checked_on_the_host(L):
     assert st in (_lib.ERR_UNSUPPORTED, _lib.OK, _lib.ERR_INVALID_ARG)
 
 
+def test_layers_arguments_are_checked_on_the_host(L):
+    E = _lib.ERR_INVALID_ARG
+    dm = _dims(batch=2)
+
+    def call(n_layers=3, Lseq=256, B=64, eta=0.1, rule=0, d=dm):
+        return L.ipttt_layers_forward(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, n_layers, Lseq, B, eta, rule,
+                                      FAKE, FAKE, ctypes.byref(d), None)
+
+    assert call(n_layers=-1) == E
+    assert call(Lseq=250) == E                                          # L % B != 0
+    assert call(B=24) == E                                              # bf16 needs B % 16 == 0
+    assert call(rule=7) == E
+    assert call(eta=float("nan")) == E
+    assert call(d=_dims(d=60)) == E
+    assert call(n_layers=0) == _lib.OK                                  # nothing to do
+    assert call(d=_dims(batch=0)) == _lib.OK
+    assert call() in (_lib.ERR_UNSUPPORTED, _lib.OK, _lib.ERR_INVALID_ARG)  # reaches the device check
+
+
 def test_fp32_mode_takes_any_sizes_on_the_host_checks(L):
     # fp32 accepts ragged sizes; with valid arguments the call reaches the device
     # check, which on a machine without a B300 says "unsupported".
