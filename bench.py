@@ -55,7 +55,7 @@ def parse_args():
     ap.add_argument("--workload", default="4b", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--B", type=int, default=None, help="chunk size override (the 4b_sweep points)")
     ap.add_argument("--L", type=int, default=None, help="sequence length override (small profiling cases)")
-    ap.add_argument("--rule", choices=["mse", "add"], default="mse")
+    ap.add_argument("--rule", choices=["mse", "add", "add_blockcausal"], default="mse")
     ap.add_argument("--layers", type=int, default=0,
                     help="this many layers' fast-weight MLPs in one call per step (0: one layer)")
     ap.add_argument("--docs", default=None, choices=sorted(inputs.DOC_MIXES),
@@ -96,10 +96,18 @@ def roofline_tokens_per_s(w, peaks, cu=None):
     return T / max(t_flop, t_hbm), ("tensor" if t_flop >= t_hbm else "hbm")
 
 
-def kernel_work(w, name, cu=None, layers=1):
+def kernel_work(w, name, cu=None, layers=1, rule="mse"):
     """Algorithmic FLOPs and bytes of ONE launch of kernel `name` in a step (with
     packed documents, the step's total over its launches of that kernel; with
     several layers, every launch covers all of them)."""
+    if rule == "add_blockcausal" and name in ("scores", "apply", "group_sum"):
+        # the quadratic form: kept (query, key) pairs per sequence = B^2 K (K-1) / 2
+        K = w.L // w.B
+        pairs = w.batch * w.B * w.B * K * (K - 1) / 2
+        T = w.batch * w.L
+        fl = {"scores": 2.0 * w.d_ff * pairs, "apply": 2.0 * T * w.d * w.d_ff + 2.0 * w.d * pairs,
+              "group_sum": 2.0 * T * w.d * w.d_ff}[name]
+        return fl * layers, 0.0
     fl, by = _kernel_work_one(w, name, cu)
     return fl * layers, by * layers
 
@@ -279,7 +287,7 @@ def run_reference(args, w, rank, world):
     from oracle import ipttt_oracle as orc  # the reference arm is the oracle, on the host
     one = w.replace(batch=1)
     a = inputs.generate(one, seed=0, n_tokens=one.B)
-    rule = args.rule
+    rule = "mse" if args.rule == "mse" else "add"  # the block-causal form has the additive rule's outputs
 
     def step():
         if args.docs:  # one document of one chunk through the packed-document oracle
@@ -498,7 +506,7 @@ def main():
     if dom:
         n_launch, total_ms = kt[dom]
         avg_s = total_ms / n_launch / 1e3
-        fl, by = kernel_work(w, dom, cu, max(1, nl))
+        fl, by = kernel_work(w, dom, cu, max(1, nl), args.rule)
         t_f = fl / (peaks["bf16_tflops_sustained"] * 1e12) if fl else 0.0
         t_b = by / (peaks["hbm_gbs"] * 1e9) if by else 0.0
         wk = f"{w.name}-B{w.B}-{args.rule}" + (f"-docs-{args.docs}" if args.docs else "")

@@ -17,8 +17,9 @@ LIB_PATH = os.path.join(HERE, "libipttt.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALLOC, ERR_LAUNCH, ERR_TIMEOUT, ERR_CUDA = range(7)
 FP32, BF16 = 0, 1
-RULE_MSE, RULE_ADD = 0, 1
-_RULES = {"mse": RULE_MSE, "add": RULE_ADD, RULE_MSE: RULE_MSE, RULE_ADD: RULE_ADD}
+RULE_MSE, RULE_ADD, RULE_ADD_BLOCKCAUSAL = 0, 1, 2
+_RULES = {"mse": RULE_MSE, "add": RULE_ADD, "add_blockcausal": RULE_ADD_BLOCKCAUSAL,
+          RULE_MSE: RULE_MSE, RULE_ADD: RULE_ADD, RULE_ADD_BLOCKCAUSAL: RULE_ADD_BLOCKCAUSAL}
 
 # Every symbol include/ipttt.h declares (checked by the ABI tests).
 EXPORTS = (
@@ -28,7 +29,8 @@ EXPORTS = (
     "ipttt_kernel_name", "ipttt_make_targets_noalloc", "ipttt_layer_forward_varlen", "ipttt_layers_forward",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
-KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy")
+KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy",
+                "scores")
 
 
 class Dims(ctypes.Structure):

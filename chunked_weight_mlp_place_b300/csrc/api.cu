@@ -329,6 +329,10 @@ ipttt_status run_targets(const void* E, const float* conv_w, const void* P, void
   return IPTTT_OK;
 }
 
+bool valid_rule(ipttt_rule r) {
+  return r == IPTTT_RULE_MSE || r == IPTTT_RULE_ADD || r == IPTTT_RULE_ADD_BLOCKCAUSAL;
+}
+
 // Number of groups of the additive scan: the largest divisor of K not above 8.
 int64_t scan_groups(int64_t K) {
   for (int64_t G = std::min<int64_t>(8, K); G > 1; --G)
@@ -337,7 +341,7 @@ int64_t scan_groups(int64_t K) {
 }
 
 struct EngineLayout {
-  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, total = 0;
+  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, ac = 0, bc = 0, total = 0;
 };
 
 // Plane geometry of one d_ff x d fast weight (tile-major blocks, see common.cuh).
@@ -367,7 +371,14 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
   const int64_t K = L / B;
   const int64_t nw = dm->d_ff * dm->d;
   const int64_t np = plane_rb(dm) * plane_cb(dm) * kPlaneBlock;  // plane elements per entry
-  if (rule == IPTTT_RULE_MSE) {
+  if (rule == IPTTT_RULE_ADD_BLOCKCAUSAL) {
+    // [Z | S] per sequence (L x (d_ff + L)), [W_0 ; V] per sequence ((d_ff + L) x d), Z^T V
+    const int64_t kc = dm->d_ff + L;
+    const int64_t es = static_cast<int64_t>(act_size(dm));
+    e.ac = c.take<uint8_t>(dm->batch * L * kc * es);
+    e.bc = c.take<uint8_t>(dm->batch * kc * dm->d * es);
+    e.d = c.take<float>(dm->batch * nw);
+  } else if (rule == IPTTT_RULE_MSE) {
     e.o_acc = c.take<float>(dm->batch * B * dm->d);
     e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
     if (bf16) {
@@ -387,6 +398,79 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
   return e;
 }
 
+// The additive rule in its block-causal quadratic form (IPTTT_RULE_ADD_BLOCKCAUSAL):
+//   O = Z W_0 + (eta/B) mask(Z Z^T) V,  W_final = W_0 + (eta/B) Z^T V,
+// mask keeping, for a token of chunk q, the tokens of chunks < q.  Per sequence:
+// AC = [Z | S] (L x (d_ff + L)) with S = (eta/B) mask(Z Z^T) written by one GEMM
+// that skips the tiles the mask clears; BC = [W_0 ; V] ((d_ff + L) x d); then
+// O = AC BC is one GEMM with K = d_ff + L, and W_final the sum GEMM plus a
+// one-group scan.
+ipttt_status run_quadratic(const void* Z, const void* V, const float* W0, int64_t L, int64_t B, float eta, void* O,
+                           float* Wf, const ipttt_dims* dm, uint8_t* ws, const EngineLayout& lay, cudaStream_t st) {
+  const bool bf16 = dm->dtype == IPTTT_BF16;
+  const int64_t batch = dm->batch, d = dm->d, dff = dm->d_ff, nw = dff * d, kc = dff + L;
+  const int64_t w0s = dm->w0_per_seq ? nw : 0;
+  const int bint = static_cast<int>(batch);
+  const size_t es = act_size(dm);
+  uint8_t* AC = ws + lay.ac;
+  uint8_t* BC = ws + lay.bc;
+  float* D = reinterpret_cast<float*>(ws + lay.d);
+  const float alpha = eta / static_cast<float>(B);
+  IPTTT_CUDA(cudaMemcpy2DAsync(AC, kc * es, Z, dff * es, dff * es, batch * L, cudaMemcpyDeviceToDevice, st));
+  IPTTT_CUDA(cudaMemset2DAsync(AC + dff * es, kc * es, 0, L * es, batch * L, st));
+  IPTTT_CUDA(launch_to_act(W0, w0s, BC, kc * d, batch, nw, bf16, st));
+  IPTTT_CUDA(cudaMemcpy2DAsync(BC + dff * d * es, kc * d * es, V, L * d * es, L * d * es, batch,
+                               cudaMemcpyDeviceToDevice, st));
+  {  // S = alpha * mask(Z Z^T), B operand Z read K-major (row n of Z is column n of Z^T)
+    GemmProblem p;
+    p.M = L;
+    p.N = L;
+    p.K = dff;
+    p.nb1 = bint;
+    p.A = mat(AC, batch * L, dff, 0, 0, L);
+    p.A.ld = kc;
+    p.B = p.A;
+    p.epi = EPI_STORE;
+    p.kind = K_SCORES;
+    p.out_bf16 = bf16;
+    p.alpha = alpha;
+    p.causal = B;
+    p.D = out(AC + dff * es, kc, 0, L, 0, batch * L);
+    IPTTT_CUDA(gemm(p, bf16, st));
+  }
+  {  // O = [Z | S] [W_0 ; V]
+    GemmProblem p;
+    p.M = L;
+    p.N = d;
+    p.K = kc;
+    p.nb1 = bint;
+    p.A = mat(AC, batch * L, kc, 0, 0, L);
+    p.B = mat(BC, batch * kc, d, 1, 0, kc);
+    p.epi = EPI_STORE;
+    p.kind = K_APPLY;
+    p.out_bf16 = bf16;
+    p.D = out(O, d, 0, L, 0, batch * L);
+    IPTTT_CUDA(gemm(p, bf16, st));
+  }
+  {  // W_final = W_0 + alpha Z^T V
+    GemmProblem p;
+    p.M = dff;
+    p.N = d;
+    p.K = L;
+    p.nb1 = bint;
+    p.A = mat(AC, batch * L, dff, 1, 0, L);
+    p.A.ld = kc;
+    p.B = mat(V, batch * L, d, 1, 0, L);
+    p.epi = EPI_STORE;
+    p.kind = K_GROUP_SUM;
+    p.out_bf16 = 0;
+    p.D = out(D, d, 0, dff, 0, batch * dff);
+    IPTTT_CUDA(gemm(p, bf16, st));
+  }
+  IPTTT_CUDA(launch_group_scan(D, W0, w0s, Wf, 1, batch, nw, alpha, st));
+  return IPTTT_OK;
+}
+
 ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L, int64_t B, float eta,
                         ipttt_rule rule, void* O, float* Wf, const ipttt_dims* dm, uint8_t* ws, const EngineLayout& lay,
                         cudaStream_t st) {
@@ -399,6 +483,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   uint16_t* hi = bf16 ? reinterpret_cast<uint16_t*>(ws + lay.hi) : nullptr;
   uint16_t* lo = bf16 ? reinterpret_cast<uint16_t*>(ws + lay.lo) : nullptr;
 
+  if (rule == IPTTT_RULE_ADD_BLOCKCAUSAL) return run_quadratic(Z, V, W0, L, B, eta, O, Wf, dm, ws, lay, st);
   if (rule == IPTTT_RULE_MSE) {
     void* R = ws + lay.r;
     const Planes w = planes_of(dm, hi, lo, batch, 1, 0);
@@ -686,7 +771,7 @@ ipttt_status run_varlen(const void* X, const void* E, const void* W_g, const voi
     ra.o_y0 = i * B;
     ra.otab = starts_d;
     ra.lens = lens_d;
-    ra.r_from_v = rule == IPTTT_RULE_ADD;
+    ra.r_from_v = rule != IPTTT_RULE_MSE;
     IPTTT_CUDA(launch_residual(ra, bf16, st));
     GemmProblem u;
     u.M = dff;
@@ -727,7 +812,7 @@ ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, 
                                   int32_t with_activations, size_t* bytes) {
   IPTTT_TRY(check_dims(dims, true));
   IPTTT_TRY(check_chunking(dims, L, B));
-  if (!bytes || (rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD)) return IPTTT_ERR_INVALID_ARG;
+  if (!bytes || !valid_rule(rule)) return IPTTT_ERR_INVALID_ARG;
   size_t base = 0;
   if (with_activations) {
     Carve c;
@@ -771,7 +856,7 @@ ipttt_status ipttt_chunk_forward(const void* Z, const void* V, const float* W_o0
   LaunchScope scope;
   IPTTT_TRY(check_dims(dims, true));
   IPTTT_TRY(check_chunking(dims, L, B));
-  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
+  if (!valid_rule(rule) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
   if (dims->batch == 0) return IPTTT_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t nw = dims->d_ff * dims->d;
@@ -795,7 +880,7 @@ ipttt_status ipttt_layer_forward(const void* X, const void* E, const void* W_g, 
   LaunchScope scope;
   IPTTT_TRY(check_dims(dims, true));
   IPTTT_TRY(check_chunking(dims, L, B));
-  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
+  if (!valid_rule(rule) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
   if (dims->batch == 0) return IPTTT_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t nw = dims->d_ff * dims->d;
@@ -828,7 +913,7 @@ ipttt_status ipttt_layer_forward_varlen(const void* X, const void* E, const void
                                         ipttt_stream stream) {
   LaunchScope scope;
   IPTTT_TRY(check_dims(dims, false));
-  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
+  if (!valid_rule(rule) || !std::isfinite(eta)) return IPTTT_ERR_INVALID_ARG;
   if (B < 1 || n_docs < 0 || !cu_seqlens) return IPTTT_ERR_INVALID_ARG;
   if (dims->dtype == IPTTT_BF16 && B % 16) return IPTTT_ERR_INVALID_ARG;
   VarlenPlan pl;
@@ -850,7 +935,7 @@ ipttt_status ipttt_layers_forward(const void* X, const void* E, const void* W_g,
   LaunchScope scope;
   IPTTT_TRY(check_dims(dims, true));
   IPTTT_TRY(check_chunking(dims, L, B));
-  if ((rule != IPTTT_RULE_MSE && rule != IPTTT_RULE_ADD) || !std::isfinite(eta) || n_layers < 0)
+  if (!valid_rule(rule) || !std::isfinite(eta) || n_layers < 0)
     return IPTTT_ERR_INVALID_ARG;
   if (n_layers == 0 || dims->batch == 0) return IPTTT_OK;
   const int64_t batch = dims->batch, d = dims->d, dff = dims->d_ff, nw = dff * d;
@@ -984,8 +1069,8 @@ ipttt_status ipttt_kernel_timing_read(int32_t kind, int64_t* launches, double* t
 }
 
 const char* ipttt_kernel_name(int32_t kind) {
-  static const char* names[K_COUNT] = {"gate_up", "conv", "proj", "apply", "residual",
-                                       "update", "group_sum", "scan", "weight_copy"};
+  static const char* names[K_COUNT] = {"gate_up", "conv", "proj",      "apply", "residual",
+                                       "update",  "group_sum", "scan", "weight_copy", "scores"};
   return (kind >= 0 && kind < K_COUNT) ? names[kind] : "unknown";
 }
 

@@ -532,6 +532,32 @@ cudaError_t launch_merge_planes(const Planes& w, float* W, int64_t R, int64_t C,
   return cudaGetLastError();
 }
 
+// dst[e*dst_stride + i] = act(src[e*src_stride + i]) for e < entries, i < n.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) to_act_kernel(const float* __restrict__ src, int64_t src_stride,
+                                                          T* __restrict__ dst, int64_t dst_stride, int64_t entries,
+                                                          int64_t n) {
+  const int64_t total = entries * n;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = idx / n, i = idx % n;
+    dst[e * dst_stride + i] = from_f32<T>(src[e * src_stride + i]);
+  }
+}
+
+cudaError_t launch_to_act(const float* src, int64_t src_stride, void* dst, int64_t dst_stride, int64_t entries,
+                          int64_t n, bool bf16, cudaStream_t stream) {
+  if (entries * n <= 0) return cudaSuccess;
+  LaunchMark mark(K_WEIGHT, stream);
+  if (bf16)
+    to_act_kernel<__nv_bfloat16><<<grid_for(entries * n), kThreads, 0, stream>>>(
+        src, src_stride, static_cast<__nv_bfloat16*>(dst), dst_stride, entries, n);
+  else
+    to_act_kernel<float><<<grid_for(entries * n), kThreads, 0, stream>>>(src, src_stride, static_cast<float*>(dst),
+                                                                        dst_stride, entries, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream) {
   LaunchMark mark(K_WEIGHT, stream);

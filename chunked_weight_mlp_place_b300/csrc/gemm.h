@@ -17,7 +17,7 @@
 namespace ipttt {
 
 enum EpiKind : int {
-  EPI_STORE = 0,  // D = acc                                  (D in the act dtype)
+  EPI_STORE = 0,  // D = alpha * acc, block-causal mask if set   (D in the act dtype or fp32)
   EPI_GATE = 1,   // D = SiLU(acc_g) * acc_u, acc_u from B2   (D in the act dtype)
   EPI_ACCUM = 2,  // D += acc, fp32 reductions in L2          (D fp32; partial sums)
   EPI_AXPY = 3,   // D = src + alpha * acc, fp32 (CUDA cores) or split hi/lo planes (tensor cores)
@@ -84,6 +84,10 @@ struct GemmProblem {
   Planes w;
   int b_planes = 0;
   float alpha = 1.0f;
+  // STORE: chunk size of a block-causal mask (0: none).  Element (m, n) of a batch entry
+  // is kept where n lies in an earlier chunk than m (n < (m / causal) * causal), else 0;
+  // on the tensor cores, tiles with no kept element are skipped (their output stays as it was).
+  int64_t causal = 0;
   int split_k = 0;   // tensor-core path: 1 = balance (tile, k-block) work over CTAs (needs EPI_ACCUM)
   int kind = 0;      // KernelKind label (launch counting / timing)
 };

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmProblem p
       const float v = acc[i][j];
       switch (p.epi) {
         case EPI_STORE:
-          *d = v;
+          *d = (p.causal && n >= (m / p.causal) * p.causal) ? 0.0f : p.alpha * v;
           break;
         case EPI_GATE:
           *d = silu_f(v) * acc2[i][j];

@@ -102,6 +102,10 @@ struct Sched {
   int split;
   int pair;
   int64_t total_iters;
+  // block-causal STORE: tiles whose every column lies in the chunk of its last row or later hold
+  // no kept element and are skipped by every role
+  int64_t mask_chunk, mask_m;
+  int bn;
 
   __device__ void tile_coords(int64_t t, int& bi, int64_t& mt, int64_t& nt) const {
     bi = static_cast<int>(t / tiles_per_batch);
@@ -113,6 +117,15 @@ struct Sched {
     const int64_t q = r % gsz;
     mt = first_m + q % gm;
     nt = q / gm;
+  }
+  __device__ bool masked(int64_t t) const {
+    if (!mask_chunk) return false;
+    int bi;
+    int64_t mt, nt;
+    tile_coords(t, bi, mt, nt);
+    const int64_t rows = pair ? 2 * BM : BM;
+    const int64_t m_last = min(mask_m - 1, (mt + 1) * rows - 1);
+    return nt * bn >= (m_last / mask_chunk) * mask_chunk;
   }
   // Split mode: worker c (a CTA, or a CTA pair) owns iterations [floor(c*T/G), floor((c+1)*T/G)).
   __device__ int64_t worker() const { return pair ? (blockIdx.x >> 1) : blockIdx.x; }
@@ -142,6 +155,7 @@ struct SegIter {
       it += g.kb1 - g.kb0;
       return true;
     }
+    while (t < s->total_tiles && s->masked(t)) t += s->workers();
     if (t >= s->total_tiles) return false;
     g.tile = t;
     g.kb0 = 0;
@@ -245,7 +259,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
       if constexpr (EPI == EPI_GATE)
         v[i] = silu_f(a) * __uint_as_float(u[i]);
       else
-        v[i] = a;
+        v[i] = p.alpha * a;
+    }
+    if constexpr (EPI == EPI_STORE) {
+      if (p.causal) {  // keep columns of earlier chunks than row m's
+        const int64_t lim = (m / p.causal) * p.causal;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n + i >= lim) v[i] = 0.0f;
+      }
     }
     const int64_t row = row_of(p.D, b1, b2) + m;
     if constexpr (OUT_BF16) {
@@ -807,6 +829,9 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   s.group_m = static_cast<int>(s.n_mt < 16 ? s.n_mt : 16);
   s.split = p.split_k ? 1 : 0;
   s.total_iters = s.total_tiles * s.kb_total;
+  s.mask_chunk = (EPI == EPI_STORE && !s.split) ? p.causal : 0;
+  s.mask_m = p.M;
+  s.bn = BN;
   const int64_t workers =
       std::min<int64_t>(max_workers[dev], s.split ? s.total_iters : s.total_tiles);
   if (workers <= 0) return cudaSuccess;
@@ -849,6 +874,8 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
                           : run_any<128, 2, false, true, EPI_GATE, false>(p, stream);
       break;
     case EPI_STORE:
+      // B K-major (B[k][n] read from rows n, e.g. Z^T): single CTAs (pairs split an MN-major B)
+      if (!a_mn && !b_mn && p.out_bf16) return run<256, 1, false, false, EPI_STORE, true, false, false>(p, stream);
       if (!a_mn && b_mn)
         return p.out_bf16 ? run_any<256, 1, false, true, EPI_STORE, true>(p, stream)
                           : run_any<256, 1, false, true, EPI_STORE, false>(p, stream);

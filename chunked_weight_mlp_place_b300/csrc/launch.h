@@ -20,7 +20,8 @@ enum KernelKind : int {
   K_GROUP_SUM = 6, // additive scan: per-group Z^T V
   K_SCAN = 7,      // additive scan: exclusive prefix over groups
   K_WEIGHT = 8,    // fast-weight conversions (W_o0 -> split planes -> W_final, W_o0 -> W_final)
-  K_COUNT = 9
+  K_SCORES = 9,    // additive rule, block-causal form: (eta/B) mask(Z Z^T)
+  K_COUNT = 10
 };
 
 // Every kernel launch of the library sits inside one LaunchMark: it counts the
@@ -111,6 +112,9 @@ cudaError_t launch_residual(const ResidualArgs& a, bool bf16, cudaStream_t strea
 cudaError_t launch_split_planes(const float* W0, int64_t w0_stride, const Planes& w, int64_t R, int64_t C,
                                 cudaStream_t stream);
 cudaError_t launch_merge_planes(const Planes& w, float* W, int64_t R, int64_t C, cudaStream_t stream);
+// dst[e*dst_stride + i] = act(src[e*src_stride + i]) (act = bf16 or fp32) for e < entries, i < n.
+cudaError_t launch_to_act(const float* src, int64_t src_stride, void* dst, int64_t dst_stride, int64_t entries,
+                          int64_t n, bool bf16, cudaStream_t stream);
 // W[s] = W0[s or 0] (fp32 copy) for s < batch.
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream);

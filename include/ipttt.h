@@ -74,7 +74,16 @@ typedef enum ipttt_dtype { IPTTT_FP32 = 0, IPTTT_BF16 = 1 } ipttt_dtype;
 
 typedef enum ipttt_rule {
   IPTTT_RULE_MSE = 0, /* W <- W - (eta/B) Z_k^T (Z_k W - V_k): sequential over chunks */
-  IPTTT_RULE_ADD = 1  /* W <- W + (eta/B) Z_k^T V_k: chunk-parallel prefix scan */
+  IPTTT_RULE_ADD = 1, /* W <- W + (eta/B) Z_k^T V_k: chunk-parallel prefix scan */
+  /* The additive rule's outputs from its block-causal quadratic form, without a
+   * fast weight per chunk: O = Z W_0 + (eta/B) mask(Z Z^T) V with mask keeping
+   * the tokens of earlier chunks, and W_final = W_0 + (eta/B) Z^T V (itsolotime
+   * §2.3: the additive rule is associative; §3.2: parallel equals serial).  The
+   * same results as IPTTT_RULE_ADD; work and scratch grow as L^2 per sequence
+   * (batch*L*(d_ff+L) act elements of scratch), so it pays at small B, where
+   * the scan streams a fast weight per chunk.  Packed documents
+   * (ipttt_layer_forward_varlen) run it as IPTTT_RULE_ADD. */
+  IPTTT_RULE_ADD_BLOCKCAUSAL = 2
 } ipttt_rule;
 
 /* Sizes shared by the calls.  batch = independent sequences; d = model width;
@@ -258,7 +267,7 @@ int64_t ipttt_last_launch_count(void);
  * for the recorded events and returns, for one kernel kind, the launches and
  * their summed device time in milliseconds since the last start.  Kinds:
  * 0 gate_up, 1 conv, 2 proj, 3 apply, 4 residual, 5 update, 6 group_sum,
- * 7 scan, 8 weight_copy (names from ipttt_kernel_name).  Host only. */
+ * 7 scan, 8 weight_copy, 9 scores (names from ipttt_kernel_name).  Host only. */
 ipttt_status ipttt_kernel_timing(int32_t enable);
 ipttt_status ipttt_kernel_timing_read(int32_t kind, int64_t* launches, double* total_ms);
 const char* ipttt_kernel_name(int32_t kind);
