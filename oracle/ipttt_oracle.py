@@ -20,7 +20,7 @@ library matmul as the only building block:
   (outputs of the whole chunk first, then the gradient accumulated over the
   chunk, one update).
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
 
 * loss: ``l_k(W) = ||Z_k W - V_k||_F^2 / (2B)`` ("make W z_t close to v_t",
   su666666 "second axe"), so one gradient step is
