@@ -280,6 +280,23 @@ def oracle_sample_docs(w, cu, seconds):
     return tok / el, desc, blas_threads()
 
 
+# ------------------------------------------------------------------ ranks
+def rank_seed(rank):
+    """Seed of the inputs rank `rank` draws: every rank runs its own sequences
+    (weak scaling, no data shared between ranks and no collective on the path)."""
+    return 1000 + rank
+
+
+def max_over_ranks(value, dist, device):
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, w, rank, world):
     if rank != 0:
@@ -370,9 +387,9 @@ def main():
 
     peaks, peaks_kind = load_peaks()
     nl = max(0, args.layers)
-    a = inputs.generate(w, seed=1000 + rank)
+    a = inputs.generate(w, seed=rank_seed(rank))
     if nl:  # each layer its own hidden states and weights, drawn from seeds of their own
-        per = [a] + [inputs.generate(w, seed=1000 + rank + 7919 * l, want=("X", "W_g", "W_u", "W_o0", "conv_w", "P"))
+        per = [a] + [inputs.generate(w, seed=rank_seed(rank) + 7919 * l, want=("X", "W_g", "W_u", "W_o0", "conv_w", "P"))
                      for l in range(1, nl)]
         for k in ("X", "W_g", "W_u", "W_o0", "conv_w", "P"):
             a[k] = np.stack([q[k] for q in per])
@@ -433,10 +450,7 @@ def main():
     if ip.sync_status(stream) != 0:
         raise RuntimeError("device error in the timed region")
     kt = ip.kernel_timing_read()
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     tokens = world * T * args.steps * max(1, nl)
     value = tokens / (elapsed_ms / 1e3)
 
@@ -455,7 +469,7 @@ def main():
             step_seq()
         e1.record(stream)
         torch.cuda.synchronize()
-        t_seq = e0.elapsed_time(e1)
+        t_seq = max_over_ranks(e0.elapsed_time(e1), dist, dev)
         sequential = {"value": world * T * nl * args.steps / (t_seq / 1e3), "unit": "(token x layer)/s",
                       "ms_per_step": t_seq / args.steps, "launches_per_step": ip.last_launch_count() * nl}
 
@@ -487,10 +501,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         t_e2e = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([t_e2e], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_e2e = float(t.item())
+        t_e2e = max_over_ranks(t_e2e, dist, dev)
         e2e = {"value": world * T * max(1, nl) * n_e2e / (t_e2e / 1e3),
                "unit": "(token x layer)/s" if nl else "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
