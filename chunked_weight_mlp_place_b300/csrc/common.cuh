@@ -49,18 +49,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
-// Arrive on `bar` only once `dep` is available: the arrive takes `dep` as an
-// operand, so it cannot issue before the loads that produce `dep` completed.
-__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float dep) {
-  asm volatile(
-      "{\n\t.reg .b32 t;\n\t"
-      "mov.b32 t, %1;\n\t"
-      "mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar)),
-      "f"(dep)
-      : "memory");
-}
-// Order this thread's earlier generic-proxy shared-memory accesses before later
-// async-proxy (TMA) accesses to the same memory.
 // 32-byte global load / store of one thread (address 32-byte aligned): a whole
 // sector per lane.
 __device__ __forceinline__ void ld_global_v8(const void* g, uint32_t (&v)[8]) {
@@ -74,6 +62,8 @@ __device__ __forceinline__ void st_global_v8(void* g, const uint32_t (&v)[8]) {
                : "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses to the same memory.
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -133,37 +123,6 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// L2 eviction-priority policies for TMA copies (createpolicy): data read or
-// written once per pass is marked evict-first, so it does not push out data
-// that the next kernel reads again.
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-// 2-D tiled copy global -> shared with an L2 cache policy.
-__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                                 uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
-      "{%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-// 2-D tiled copy shared -> global (elements outside the tensor are skipped).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const void* smem_src, int x, int y,
-                                                  uint64_t policy) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "l"(policy)
-               : "memory");
-}
 // 2-D tiled element-wise fp32 addition shared -> global, performed in L2.
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src, int x, int y) {
   asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -335,11 +294,6 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cl, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cl),
-               "r"(bytes)
-               : "memory");
-}
 // TMEM allocation shared by the pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -385,9 +339,6 @@ __device__ __forceinline__ void split_w(float w, uint32_t& hi, uint32_t& lo) {
   const uint32_t b = __float_as_uint(w) + 0x8000u;
   hi = b >> 16;
   lo = b & 0xFFFFu;
-}
-__device__ __forceinline__ float join_w(uint32_t hi, uint32_t lo) {
-  return __uint_as_float(((hi << 16) | lo) - 0x8000u);
 }
 // The same on two elements whose halves are packed in 32-bit words (element 0
 // in the low half): hi2/lo2 hold the hi/lo halves of w0 and w1.
