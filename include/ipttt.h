@@ -33,12 +33,16 @@
  *   default stream) and never synchronise it.  A call returns IPTTT_OK once its
  *   kernels are queued; a device-side failure (a capped wait that ran out) is
  *   recorded on the device and reported by ipttt_sync_status().
- * - Scratch memory (activations Z and V inside ipttt_layer_forward, partial
- *   sums, the bf16 copy of the fast weight, group states of the additive
- *   scan) comes from a per-device pool owned by the library: grown with
- *   cudaMalloc on first need (a call that needs to grow it synchronises the
- *   device), reused by later calls, freed by ipttt_release().  Calls that share
- *   the pool must be ordered (one stream, or the caller's own events).
+ * - Scratch memory (activations Z and V inside the layer calls, partial sums,
+ *   the split planes of the fast weight, group states of the additive scan,
+ *   the [Z | S] and [W_0 ; V] blocks of the block-causal form, the tables of
+ *   packed documents) comes from a per-device pool owned by the library: grown
+ *   with cudaMalloc on first need (a call that needs to grow it synchronises
+ *   the device), reused by later calls, freed by ipttt_release().  Calls that
+ *   share the pool must be ordered (one stream, or the caller's own events).
+ *   ipttt_workspace_size reports the need of ipttt_layer_forward and
+ *   ipttt_chunk_forward; the packed-document and multi-layer calls need the
+ *   same per document or per layer and sequence.
  * - No call aborts, throws or traps.  Errors come back as an ipttt_status.
  *   Arguments are checked before any launch: null pointers, non-positive or
  *   inconsistent sizes, L not a multiple of B, misaligned pointers, host
