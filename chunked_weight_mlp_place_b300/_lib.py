@@ -27,6 +27,7 @@ EXPORTS = (
     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
     "ipttt_status_string", "ipttt_version", "ipttt_kernel_timing", "ipttt_kernel_timing_read",
     "ipttt_kernel_name", "ipttt_make_targets_noalloc", "ipttt_layer_forward_varlen", "ipttt_layers_forward",
+    "ipttt_additive_sums", "ipttt_weight_axpy",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
 KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy",
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int32
         dp = ctypes.POINTER(Dims)
         L.ipttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
+        L.ipttt_additive_sums.argtypes = [vp, vp, i64, vp, dp, vp]
+        L.ipttt_weight_axpy.argtypes = [vp, vp, f32, i64, vp]
         L.ipttt_layers_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, i32, vp, vp, dp, vp]
         L.ipttt_layer_forward_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, ctypes.POINTER(i64), i64, i64, f32,
                                                  i32, vp, vp, dp, vp]
@@ -254,6 +257,36 @@ def chunk_forward(Z, V, W_o0, L: int, B: int, eta: float, rule, O, W_final, stre
                                    int(L), int(B), float(eta), _RULES[rule], _ptr(O, "O", act),
                                    _ptr(W_final, "W_final", torch.float32), ctypes.byref(dm), _stream(stream))
     _check(st, "ipttt_chunk_forward")
+
+
+def copy_weights(W_o0, W, stream=None) -> None:
+    """W[s] = W_o0 (or W_o0[s] when W_o0 is per sequence) for every sequence s of
+    W (batch, d_ff, d): ipttt_chunk_forward over zero tokens."""
+    torch = _torch()
+    d_ff, d = W_o0.shape[-2], W_o0.shape[-1]
+    dm = dims(W.shape[0], d, d_ff, FP32, 1 if W_o0.dim() == 3 else 0)
+    _check(lib().ipttt_chunk_forward(None, None, _ptr(W_o0, "W_o0", torch.float32), 0, 1, 0.0, RULE_ADD, None,
+                                     _ptr(W, "W", torch.float32), ctypes.byref(dm), _stream(stream)),
+           "ipttt_chunk_forward")
+
+
+def additive_sums(Z, V, L: int, S, stream=None) -> None:
+    """ipttt_additive_sums: S[s] = Z_s^T V_s (fp32, (batch, d_ff, d)) over L tokens per sequence."""
+    torch = _torch()
+    act = Z.dtype
+    batch = Z.shape[0] // L if L else S.shape[0]
+    dm = dims(batch, V.shape[1], Z.shape[1], _dtype_code(Z))
+    _check(lib().ipttt_additive_sums(_ptr(Z, "Z", act), _ptr(V, "V", act), int(L), _ptr(S, "S", torch.float32),
+                                     ctypes.byref(dm), _stream(stream)), "ipttt_additive_sums")
+
+
+def weight_axpy(W, S, alpha: float, stream=None) -> None:
+    """ipttt_weight_axpy: W += alpha * S on fp32 tensors of the same size."""
+    torch = _torch()
+    if W.numel() != S.numel():
+        raise ValueError("W and S differ in size")
+    _check(lib().ipttt_weight_axpy(_ptr(W, "W", torch.float32), _ptr(S, "S", torch.float32), float(alpha),
+                                   int(W.numel()), _stream(stream)), "ipttt_weight_axpy")
 
 
 def workspace_size(batch: int, d: int, d_ff: int, dtype: int, L: int, B: int, rule, with_activations=True) -> int:

@@ -1014,6 +1014,48 @@ ipttt_status ipttt_layers_forward(const void* X, const void* E, const void* W_g,
   return run_engine(ws + z_off, ws + v_off, W0, L, B, eta, rule, O, W_final, &dm, ws, lay, st);
 }
 
+ipttt_status ipttt_additive_sums(const void* Z, const void* V, int64_t L, float* S, const ipttt_dims* dims,
+                                 ipttt_stream stream) {
+  LaunchScope scope;
+  IPTTT_TRY(check_dims(dims, true));
+  if (L < 0) return IPTTT_ERR_INVALID_ARG;
+  // the contraction runs over a window of token rows: whole 16-token tensor-core steps
+  if (dims->dtype == IPTTT_BF16 && L % 16) return IPTTT_ERR_INVALID_ARG;
+  if (dims->batch > 0 && (L > (int64_t{1} << 31) / dims->batch || dims->d_ff * dims->batch > (int64_t{1} << 31)))
+    return IPTTT_ERR_INVALID_ARG;
+  if (dims->batch == 0) return IPTTT_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (L == 0) {
+    IPTTT_TRY(check_ptrs({static_cast<const void*>(S)}));
+    IPTTT_CUDA(cudaMemsetAsync(S, 0, sizeof(float) * dims->batch * dims->d_ff * dims->d, st));
+    return IPTTT_OK;
+  }
+  IPTTT_TRY(check_ptrs({Z, V, static_cast<const void*>(S)}));
+  const bool bf16 = dims->dtype == IPTTT_BF16;
+  GemmProblem p;
+  p.M = dims->d_ff;
+  p.N = dims->d;
+  p.K = L;
+  p.nb1 = static_cast<int>(dims->batch);
+  p.A = mat(Z, dims->batch * L, dims->d_ff, 1, 0, L);
+  p.B = mat(V, dims->batch * L, dims->d, 1, 0, L);
+  p.epi = EPI_STORE;
+  p.kind = K_GROUP_SUM;
+  p.out_bf16 = 0;
+  p.D = out(S, dims->d, 0, dims->d_ff, 0, dims->batch * dims->d_ff);
+  IPTTT_CUDA(gemm(p, bf16, st));
+  return IPTTT_OK;
+}
+
+ipttt_status ipttt_weight_axpy(float* W, const float* S, float alpha, int64_t n, ipttt_stream stream) {
+  LaunchScope scope;
+  if (n < 0 || !std::isfinite(alpha)) return IPTTT_ERR_INVALID_ARG;
+  if (n == 0) return IPTTT_OK;
+  IPTTT_TRY(check_ptrs({static_cast<const void*>(W), static_cast<const void*>(S)}));
+  IPTTT_CUDA(launch_axpy(W, S, alpha, n, static_cast<cudaStream_t>(stream)));
+  return IPTTT_OK;
+}
+
 ipttt_status ipttt_sync_status(ipttt_stream stream) {
   const cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {

@@ -558,6 +558,20 @@ cudaError_t launch_to_act(const float* src, int64_t src_stride, void* dst, int64
   return cudaGetLastError();
 }
 
+__global__ void __launch_bounds__(kThreads) axpy_kernel(float* __restrict__ W, const float* __restrict__ S,
+                                                        float alpha, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    W[i] = fmaf(alpha, S[i], W[i]);
+}
+
+cudaError_t launch_axpy(float* W, const float* S, float alpha, int64_t n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  LaunchMark mark(K_WEIGHT, stream);
+  axpy_kernel<<<grid_for(n), kThreads, 0, stream>>>(W, S, alpha, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream) {
   LaunchMark mark(K_WEIGHT, stream);

@@ -115,6 +115,8 @@ cudaError_t launch_merge_planes(const Planes& w, float* W, int64_t R, int64_t C,
 // dst[e*dst_stride + i] = act(src[e*src_stride + i]) (act = bf16 or fp32) for e < entries, i < n.
 cudaError_t launch_to_act(const float* src, int64_t src_stride, void* dst, int64_t dst_stride, int64_t entries,
                           int64_t n, bool bf16, cudaStream_t stream);
+// W[i] += alpha * S[i] for i < n (fp32).
+cudaError_t launch_axpy(float* W, const float* S, float alpha, int64_t n, cudaStream_t stream);
 // W[s] = W0[s or 0] (fp32 copy) for s < batch.
 cudaError_t launch_copy_w(const float* W0, int64_t w0_stride, float* W, int64_t batch, int64_t n,
                           cudaStream_t stream);

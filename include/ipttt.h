@@ -246,7 +246,24 @@ ipttt_status ipttt_make_targets_noalloc(const void* E, const float* conv_w, cons
                                         int64_t L, int64_t B, const ipttt_dims* dims,
                                         ipttt_stream stream);
 
-/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or
+/*
+ * Pieces of the additive rule over one sequence split across GPUs (context
+ * parallelism: each rank holds a run of whole chunks).  The rule's weight after
+ * a run of chunks is the weight before it plus (eta/B) times the run's sum of
+ * Z_k^T V_k (itsolotime §2.3: the additive rule is associative), so a rank
+ * starts from W_0 plus the sums of the ranks before it and then runs its chunks
+ * with ipttt_chunk_forward (rule IPTTT_RULE_ADD, per-sequence W_o0).
+ *
+ * ipttt_additive_sums: S[s] = Z_s^T V_s over the L tokens of each sequence s.
+ *   Z [batch*L, d_ff] act, V [batch*L, d] act, S [batch, d_ff, d] fp32 (out).
+ *   In IPTTT_BF16 mode L must be a multiple of 16.  L == 0 writes zeros.
+ * ipttt_weight_axpy: W[i] += alpha * S[i] for i < n, fp32 device arrays.
+ */
+ipttt_status ipttt_additive_sums(const void* Z, const void* V, int64_t L, float* S, const ipttt_dims* dims,
+                                 ipttt_stream stream);
+ipttt_status ipttt_weight_axpy(float* W, const float* S, float alpha, int64_t n, ipttt_stream stream);
+
+/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or
  * ipttt_chunk_forward (with_activations = 0) needs for these sizes.  Host only. */
 ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, ipttt_rule rule,
                                   int32_t with_activations, size_t* bytes);

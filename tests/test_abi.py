@@ -121,6 +121,19 @@ def test_layers_arguments_are_checked_on_the_host(L):
     assert call() in (_lib.ERR_UNSUPPORTED, _lib.OK, _lib.ERR_INVALID_ARG)  # reaches the device check
 
 
+def test_context_parallel_pieces_are_checked_on_the_host(L):
+    E = _lib.ERR_INVALID_ARG
+    dm = _dims(batch=2)
+    assert L.ipttt_additive_sums(FAKE, FAKE, 100, FAKE, ctypes.byref(dm), None) == E   # bf16: L % 16
+    assert L.ipttt_additive_sums(FAKE, FAKE, -16, FAKE, ctypes.byref(dm), None) == E
+    assert L.ipttt_additive_sums(FAKE, FAKE, 64, FAKE, None, None) == E
+    assert L.ipttt_additive_sums(FAKE, FAKE, 64, FAKE, ctypes.byref(_dims(batch=0)), None) == _lib.OK
+    assert L.ipttt_weight_axpy(FAKE, FAKE, 0.5, -1, None) == E
+    assert L.ipttt_weight_axpy(FAKE, FAKE, float("nan"), 8, None) == E
+    assert L.ipttt_weight_axpy(FAKE, FAKE, 0.5, 0, None) == _lib.OK
+    assert L.ipttt_weight_axpy(0, FAKE, 0.5, 8, None) == E                              # null pointer
+
+
 def test_fp32_mode_takes_any_sizes_on_the_host_checks(L):
     # fp32 accepts ragged sizes; with valid arguments the call reaches the device
     # check, which on a machine without a B300 says "unsupported".
