@@ -120,7 +120,7 @@ typedef void* ipttt_stream; /* a cudaStream_t */
  *   P      [d, d]            act   target projection
  *   L, B                           tokens per sequence, tokens per chunk; L % B == 0
  *   eta                            step size (the step is eta/B times the chunk sum)
- *   rule                           IPTTT_RULE_MSE or IPTTT_RULE_ADD
+ *   rule                           IPTTT_RULE_MSE, IPTTT_RULE_ADD or IPTTT_RULE_ADD_BLOCKCAUSAL
  *   O      [batch*L, d]      act   out: O_k = Z_k W_k, chunk by chunk
  *   W_final[batch, d_ff, d] fp32   out: the fast weight after the last chunk
  *
