@@ -169,6 +169,11 @@ def test_workspace_size_is_host_only(L):
     # additive scan: 8 groups of fp32 sums + split hi/lo states
     assert L.ipttt_workspace_size(ctypes.byref(dm), 32768, 64, 1, 0, ctypes.byref(out)) == _lib.OK
     assert out.value >= 8 * 9728 * 2560 * 8
+    # block-causal additive form: [Z | S] (L x (d_ff + L)) and [W_0 ; V] ((d_ff + L) x d) act, Z^T V fp32
+    assert L.ipttt_workspace_size(ctypes.byref(dm), 32768, 64, 2, 0, ctypes.byref(out)) == _lib.OK
+    kc = 9728 + 32768
+    quad = 32768 * kc * 2 + kc * 2560 * 2 + 9728 * 2560 * 4
+    assert quad <= out.value <= quad + 4096
     assert L.ipttt_workspace_size(ctypes.byref(dm), 100, 64, 0, 0, ctypes.byref(out)) == _lib.ERR_INVALID_ARG
     assert L.ipttt_workspace_size(None, 128, 64, 0, 0, ctypes.byref(out)) == _lib.ERR_INVALID_ARG
 
