@@ -263,7 +263,7 @@ ipttt_status ipttt_additive_sums(const void* Z, const void* V, int64_t L, float*
                                  ipttt_stream stream);
 ipttt_status ipttt_weight_axpy(float* W, const float* S, float alpha, int64_t n, ipttt_stream stream);
 
-/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or
+/* Bytes of pool scratch ipttt_layer_forward (with_activations = 1) or
  * ipttt_chunk_forward (with_activations = 0) needs for these sizes.  Host only. */
 ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, ipttt_rule rule,
                                   int32_t with_activations, size_t* bytes);

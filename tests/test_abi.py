@@ -201,3 +201,31 @@ def test_noalloc_targets_size_limit_is_checked_on_the_host(L):
     assert L.ipttt_make_targets_noalloc(FAKE, FAKE, FAKE, FAKE, 100, 64, ctypes.byref(dm), None) == \
         _lib.ERR_INVALID_ARG
     assert L.ipttt_make_targets_noalloc(0, 0, 0, 0, 0, 64, ctypes.byref(dm), None) == _lib.OK
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
+    """The boundary is a C ABI: a C program (gcc, not a C++ compiler) includes the
+    header, links against the built library and calls its host-only functions."""
+    import shutil
+    import subprocess
+
+    build()
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use_ipttt.c"
+    src.write_text(
+        '#include <stdio.h>\n#include "ipttt.h"\n'
+        "int main(void) {\n"
+        "  ipttt_dims dm = {1, 64, 256, IPTTT_BF16, 0};\n"
+        "  size_t bytes = 0;\n"
+        "  if (ipttt_workspace_size(&dm, 256, 64, IPTTT_RULE_MSE, 1, &bytes) != IPTTT_OK || bytes == 0) return 1;\n"
+        "  if (ipttt_layer_forward(0, 0, 0, 0, 0, 0, 0, 250, 64, 0.1f, IPTTT_RULE_MSE, 0, 0, &dm, 0)\n"
+        "      != IPTTT_ERR_INVALID_ARG) return 2;\n"
+        '  printf("%d %s\\n", ipttt_version(), ipttt_status_string(IPTTT_ERR_TIMEOUT));\n'
+        "  return 0;\n}\n")
+    exe = tmp_path / "use_ipttt"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe), "-L", libdir, "-lipttt", "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == _lib.lib().ipttt_version() and "wait" in " ".join(out[1:])
