@@ -27,7 +27,7 @@ EXPORTS = (
     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
     "ipttt_status_string", "ipttt_version", "ipttt_kernel_timing", "ipttt_kernel_timing_read",
     "ipttt_kernel_name", "ipttt_make_targets_noalloc", "ipttt_layer_forward_varlen", "ipttt_layers_forward",
-    "ipttt_additive_sums", "ipttt_weight_axpy",
+    "ipttt_additive_sums", "ipttt_weight_axpy", "ipttt_set_pool_limit",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
 KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy",
@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
         vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int32
         dp = ctypes.POINTER(Dims)
         L.ipttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
+        L.ipttt_set_pool_limit.argtypes = [ctypes.c_size_t]
         L.ipttt_additive_sums.argtypes = [vp, vp, i64, vp, dp, vp]
         L.ipttt_weight_axpy.argtypes = [vp, vp, f32, i64, vp]
         L.ipttt_layers_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, i32, vp, vp, dp, vp]
@@ -257,6 +258,12 @@ def chunk_forward(Z, V, W_o0, L: int, B: int, eta: float, rule, O, W_final, stre
                                    int(L), int(B), float(eta), _RULES[rule], _ptr(O, "O", act),
                                    _ptr(W_final, "W_final", torch.float32), ctypes.byref(dm), _stream(stream))
     _check(st, "ipttt_chunk_forward")
+
+
+def set_pool_limit(nbytes: int) -> None:
+    """ipttt_set_pool_limit: calls needing more scratch than `nbytes` fail with
+    IPTTT_ERR_ALLOC before queuing anything (0 = no limit)."""
+    _check(lib().ipttt_set_pool_limit(int(nbytes)), "ipttt_set_pool_limit")
 
 
 def copy_weights(W_o0, W, stream=None) -> None:

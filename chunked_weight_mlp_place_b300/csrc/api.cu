@@ -16,7 +16,10 @@
 //       apply O_k = Z_k W; update W += (eta/B) Z_k^T V_k (not after the last)
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -77,8 +80,17 @@ void drain_timing_locked() {
 
 void reset_launch_count() { t_launches = 0; }
 
+const char* kind_name(int k) {
+  static const char* names[K_COUNT] = {"gate_up", "conv", "proj",      "apply", "residual",
+                                       "update",  "group_sum", "scan", "weight_copy", "scores"};
+  return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
+}
+
+// Every launch also sits in an NVTX range named after its kind (a no-op unless a
+// profiler is attached), so traces show which step of the layer queued it.
 LaunchMark::LaunchMark(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
   ++t_launches;
+  nvtxRangePushA(kind_name(k));
   std::lock_guard<std::mutex> g(g_timing_mu);
   if (!g_timing_on || k < 0 || k >= K_COUNT) return;
   TimingRec r{k, take_event(), take_event()};
@@ -88,6 +100,7 @@ LaunchMark::LaunchMark(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
 }
 
 LaunchMark::~LaunchMark() {
+  nvtxRangePop();
   if (slot < 0) return;
   std::lock_guard<std::mutex> g(g_timing_mu);
   if (slot < static_cast<int>(g_timing_pending.size()) && g_timing_pending[slot].stop)
@@ -124,7 +137,11 @@ struct Pool {
 std::mutex g_pool_mu;
 Pool g_pools[64];
 
+std::atomic<size_t> g_pool_limit{0};  // 0: no limit
+
 ipttt_status pool_reserve(size_t bytes, void** out) {
+  const size_t limit = g_pool_limit.load();
+  if (limit && bytes > limit) return IPTTT_ERR_ALLOC;  // refused before anything is queued
   const int dev = current_device();
   if (dev < 0 || dev >= 64) return IPTTT_ERR_CUDA;
   std::lock_guard<std::mutex> g(g_pool_mu);
@@ -1088,6 +1105,11 @@ ipttt_status ipttt_release(void) {
 
 int64_t ipttt_last_launch_count(void) { return t_launches; }
 
+ipttt_status ipttt_set_pool_limit(size_t bytes) {
+  g_pool_limit.store(bytes);
+  return IPTTT_OK;
+}
+
 ipttt_status ipttt_kernel_timing(int32_t enable) {
   std::lock_guard<std::mutex> g(g_timing_mu);
   if (enable) {
@@ -1110,11 +1132,7 @@ ipttt_status ipttt_kernel_timing_read(int32_t kind, int64_t* launches, double* t
   return IPTTT_OK;
 }
 
-const char* ipttt_kernel_name(int32_t kind) {
-  static const char* names[K_COUNT] = {"gate_up", "conv", "proj",      "apply", "residual",
-                                       "update",  "group_sum", "scan", "weight_copy", "scores"};
-  return (kind >= 0 && kind < K_COUNT) ? names[kind] : "unknown";
-}
+const char* ipttt_kernel_name(int32_t kind) { return kind_name(kind); }
 
 const char* ipttt_status_string(ipttt_status s) {
   switch (s) {

@@ -277,6 +277,12 @@ ipttt_status ipttt_sync_status(ipttt_stream stream);
  * must make sure no queued call still uses it (synchronise first). */
 ipttt_status ipttt_release(void);
 
+/* Cap the scratch one call may take from the pool (bytes; 0 = no cap, the
+ * default): a call that needs more returns IPTTT_ERR_ALLOC before queuing
+ * anything.  For processes that share the GPU with another allocator.  It does
+ * not shrink a pool grown before; ipttt_release() does.  Host only. */
+ipttt_status ipttt_set_pool_limit(size_t bytes);
+
 /* Kernels queued by the last call made from this host thread (a count of this
  * library's launches, for profiling).  Host only. */
 int64_t ipttt_last_launch_count(void);

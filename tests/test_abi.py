@@ -134,6 +134,11 @@ def test_context_parallel_pieces_are_checked_on_the_host(L):
     assert L.ipttt_weight_axpy(0, FAKE, 0.5, 8, None) == E                              # null pointer
 
 
+def test_pool_limit_is_host_only(L):
+    assert L.ipttt_set_pool_limit(1 << 20) == _lib.OK
+    assert L.ipttt_set_pool_limit(0) == _lib.OK
+
+
 def test_fp32_mode_takes_any_sizes_on_the_host_checks(L):
     # fp32 accepts ragged sizes; with valid arguments the call reaches the device
     # check, which on a machine without a B300 says "unsupported".

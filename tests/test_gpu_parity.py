@@ -224,3 +224,18 @@ def test_repeated_runs_stay_within_tolerance(shape, rule):
         ip.chunk_forward(Zt, Vt, W0t, L, B, 0.05, rule, O, Wf)
         assert ip.sync_status() == 0
         _check_engine(down(O), down(Wf), Oref, Wref[None], W0[None], TOL["bf16"])
+
+
+def test_pool_limit_refuses_a_call_before_queuing_anything():
+    w = inputs.workload("500m", batch=1, L=256, B=64, d=128, d_ff=256)
+    a = inputs.generate(w, seed=12)
+    ip.set_pool_limit(4096)
+    try:
+        with pytest.raises(ip.IptttError) as e:
+            run_layer(w, a, "mse")
+        assert e.value.status == ip._lib.ERR_ALLOC
+        assert ip.last_launch_count() == 0
+    finally:
+        ip.set_pool_limit(0)
+    O, Wf = run_layer(w, a, "mse")
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(Wf))
