@@ -1,5 +1,5 @@
 """Context-parallel additive rule (chunked_weight_mlp_place_b300.context_parallel)
-as two gloo ranks on CPU, each holding half of every sequence, against the
+as two and three gloo ranks on CPU, each holding a run of every sequence, against the
 float64 oracle's one-pass additive layer.  Each rank's steps run on a float64
 stand-in of the library built from the oracle's functions; the exchange and the
 start weights are the module's own."""
@@ -8,6 +8,7 @@ import socket
 import sys
 
 import numpy as np
+import pytest
 import torch
 import torch.multiprocessing as mp
 
@@ -96,9 +97,10 @@ def _run(world, cfg):
     return got
 
 
-def test_two_ranks_equal_the_one_pass_additive_layer():
+@pytest.mark.parametrize("world,batch", [(2, 2), (3, 1)])
+def test_ranks_equal_the_one_pass_additive_layer(world, batch):
     from oracle import ipttt_oracle as orc
-    world, batch, L, B, d, d_ff, eta = 2, 2, 12, 4, 5, 7, 0.2
+    L, B, d, d_ff, eta = 12, 4, 5, 7, 0.2
     got = _run(world, (batch, L, B, d, d_ff, eta))
     a = _inputs(batch, world * L, d, d_ff)
     O_ref, W_ref = orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"],
