@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t kc = 0;
+      uint32_t kc = 0, pst = 0, pph = 0;  // k-blocks issued; stage and phase of the next one
       uint32_t issued_mask = 0;
       bool ok = true;
       while (ok && iter.next(seg)) {
@@ -388,7 +388,11 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         const int64_t ra = row_of(p.A, b1, b2), rb = row_of(p.B, b1, b2), rb2 = row_of(p.B2, b1, b2);
         const int64_t pb0 = (b1 * p.w.es1 + b2 * p.w.es2) * p.w.rb;  // plane B operand: first row block
         for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++kc) {
-          const uint32_t st = kc % C::STAGES, ph = (kc / C::STAGES) & 1;
+          const uint32_t st = pst, ph = pph;
+          if (++pst == C::STAGES) {
+            pst = 0;
+            pph ^= 1;
+          }
           if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1, abort_flag, 1, &g_device_error)) {
             ok = false;
             break;
@@ -438,36 +442,54 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     // issued by a single thread, and a lone waiter cannot diverge from itself.
     if (lane == 0 && mma_cta) {
       constexpr uint32_t idesc = make_idesc_bf16(C::M_MMA, C::N_MMA, A_MN, B_MN);
-      uint32_t kc = 0, ls = 0;
+      // Descriptors of stage 0, k step 0.  A stage or a k step moves only the start-address field
+      // (bits 0-13, address >> 4; shared addresses stay below 256 KB, so the add never carries out).
+      const uint32_t s0 = smem_u32(stages);
+      const uint64_t a0 = operand_desc<A_MN>(s0, 0), b0 = operand_desc<B_MN, B_PL>(s0 + C::A_BYTES, 0);
+      constexpr uint32_t A_KSTEP = (A_MN ? 2048u : 32u) >> 4;
+      constexpr uint32_t B_KSTEP = (B_PL ? 512u : (B_MN ? 2048u : 32u)) >> 4;
+      const int kb_full = static_cast<int>(p.K / BK);  // k-blocks with all BK/16 steps inside K
+      uint32_t ls = 0, st = 0, ph = 0;  // tiles done; stage and phase of the next k-block
       bool ok = true;
       while (ok && iter.next(seg)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kAccStride;
-        for (int kb = seg.kb0; kb < seg.kb1; ++kb, ++kc) {
-          const uint32_t st = kc % C::STAGES, ph = (kc / C::STAGES) & 1;
+        for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
           if (!mbar_wait_bounded(&full_bar[st], ph, abort_flag, 2, &g_device_error)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(stages + st * C::STAGE_BYTES);
-          const uint32_t sb = sa + C::A_BYTES;
-          const int64_t krem = p.K - static_cast<int64_t>(kb) * BK;
-          const int ksteps = static_cast<int>(min(static_cast<int64_t>(BK / 16), (krem + 15) / 16));
-          for (int ks = 0; ks < ksteps; ++ks) {
-            const uint32_t accum = (kb > seg.kb0 || ks > 0) ? 1u : 0u;
-            const uint64_t ad = operand_desc<A_MN>(sa, ks), bd = operand_desc<B_MN, B_PL>(sb, ks);
-            if constexpr (PAIR)
-              umma_bf16_pair(d_tmem, ad, bd, idesc, accum);
-            else
-              umma_bf16(d_tmem, ad, bd, idesc, accum);
+          const uint32_t soff = (st * C::STAGE_BYTES) >> 4;
+          const uint64_t ad = a0 + soff, bd = b0 + soff;
+          const uint32_t first = (kb == seg.kb0) ? 0u : 1u;
+          if (kb < kb_full) {
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks) {
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, ad + ks * A_KSTEP, bd + ks * B_KSTEP, idesc, ks ? 1u : first);
+              else
+                umma_bf16(d_tmem, ad + ks * A_KSTEP, bd + ks * B_KSTEP, idesc, ks ? 1u : first);
+            }
+          } else {
+            const int ksteps = static_cast<int>((p.K - static_cast<int64_t>(kb) * BK + 15) / 16);
+            for (int ks = 0; ks < ksteps; ++ks) {
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, ad + ks * A_KSTEP, bd + ks * B_KSTEP, idesc, ks ? 1u : first);
+              else
+                umma_bf16(d_tmem, ad + ks * A_KSTEP, bd + ks * B_KSTEP, idesc, ks ? 1u : first);
+            }
           }
           if constexpr (PAIR)
             umma_commit_pair_both(&empty_bar[st]);
           else
             umma_commit(&empty_bar[st]);
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1;
+          }
         }
         if (!ok) break;
         if constexpr (PAIR)
