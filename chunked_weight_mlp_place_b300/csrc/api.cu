@@ -364,6 +364,10 @@ struct EngineLayout {
 // Plane geometry of one d_ff x d fast weight (tile-major blocks, see common.cuh).
 int64_t plane_rb(const ipttt_dims* dm) { return (dm->d_ff + kPlaneRows - 1) / kPlaneRows; }
 int64_t plane_cb(const ipttt_dims* dm) { return (dm->d + kPlaneCols - 1) / kPlaneCols; }
+// Whether the hi planes of all entries (2 bytes an element) take at most half of the 126 MB L2.
+bool planes_fit_l2(const Planes& w) {
+  return w.entries * w.rb * w.cb * kPlaneBlock * 2 <= (int64_t{63} << 20);
+}
 Planes planes_of(const ipttt_dims* dm, uint16_t* hi, uint16_t* lo, int64_t entries, int64_t es1, int64_t es2) {
   Planes w;
   w.hi = hi;
@@ -507,6 +511,9 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     if (bf16) IPTTT_CUDA(launch_split_planes(W0, w0s, w, dff, d, st));
     IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * B * d, st));
     const int64_t w0_rows = (dm->w0_per_seq ? batch : 1) * dff;
+    // The hi planes stay in L2 from one chunk to the next when they take at most half of it.
+    const bool keep_hi = bf16 && planes_fit_l2(w);
+    const int64_t zrow = dff * static_cast<int64_t>(act_size(dm));  // bytes of a row of Z
     for (int64_t k = 0; k < K; ++k) {
       // apply: O_acc[s] = Z_k[s] W_k[s], split over d_ff
       GemmProblem a;
@@ -519,6 +526,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
         a.B = mat(hi, batch * dff, d, 1, 0, dff);
         a.w = w;
         a.b_planes = 1;
+        a.l2_b = keep_hi ? L2_EVICT_LAST : L2_NORMAL;
       } else
         a.B = (k == 0) ? mat(W0, w0_rows, d, 1, 0, w0r) : mat(Wf, batch * dff, d, 1, 0, dff);
       a.epi = EPI_ACCUM;
@@ -550,6 +558,14 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       u.kind = K_UPDATE;
       if (bf16) {
         u.w = w;
+        u.planes_l2 = keep_hi ? 1 : 0;
+        u.l2_a = L2_EVICT_FIRST;  // the last read of Z_k
+        if (k + 1 < K) {          // the next apply's Z_{k+1}, fetched into L2 as the update ends
+          u.pf_ptr = static_cast<const uint8_t*>(Z) + (k + 1) * B * zrow;
+          u.pf_bytes = B * zrow;
+          u.pf_stride = L * zrow;
+          u.pf_count = bint;
+        }
       } else {
         u.D = out(Wf, d, 0, dff, 0, batch * dff);
         u.src = (k == 0) ? out(const_cast<float*>(W0), d, 0, w0r, 0, w0_rows) : out(Wf, d, 0, dff, 0, batch * dff);

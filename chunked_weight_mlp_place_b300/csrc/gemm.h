@@ -16,6 +16,9 @@
 
 namespace ipttt {
 
+// L2 eviction priority of the lines an access touches.
+enum L2Hint : int { L2_NORMAL = 0, L2_EVICT_FIRST = 1, L2_EVICT_LAST = 2 };
+
 enum EpiKind : int {
   EPI_STORE = 0,  // D = alpha * acc, block-causal mask if set   (D in the act dtype or fp32)
   EPI_GATE = 1,   // D = SiLU(acc_g) * acc_u, acc_u from B2   (D in the act dtype)
@@ -90,6 +93,17 @@ struct GemmProblem {
   int64_t causal = 0;
   int split_k = 0;   // tensor-core path: 1 = balance (tile, k-block) work over CTAs (needs EPI_ACCUM)
   int kind = 0;      // KernelKind label (launch counting / timing)
+  // Tensor-core path, L2 eviction priority (L2Hint in common.cuh) of the lines the A and B
+  // operand copies read, and, for the AXPY epilogue, planes_l2 = 1: the hi plane's lines
+  // kept (evict last) and the lo plane's given up first -- the hi plane is read again by
+  // the next apply, the lo plane only by the next update.
+  int l2_a = 0, l2_b = 0, planes_l2 = 0;
+  // Tensor-core path: once a CTA has issued all its operand copies it asks L2 to fetch
+  // its share of pf_count ranges of pf_bytes bytes, pf_stride bytes apart, from pf_ptr
+  // (the next kernel's operand; 16-byte aligned).  No result depends on it.
+  const void* pf_ptr = nullptr;
+  int64_t pf_bytes = 0, pf_stride = 0;
+  int pf_count = 0;
 };
 
 }  // namespace ipttt

@@ -145,6 +145,8 @@ struct SegIter {
       t = s->worker();
     }
   }
+  // MASK: the problem may carry a block-causal mask (STORE kernels only).
+  template <bool MASK>
   __device__ bool next(Seg& g) {
     if (s->split) {
       if (it >= it_end) return false;
@@ -155,7 +157,8 @@ struct SegIter {
       it += g.kb1 - g.kb0;
       return true;
     }
-    while (t < s->total_tiles && s->masked(t)) t += s->workers();
+    if constexpr (MASK)
+      while (t < s->total_tiles && s->masked(t)) t += s->workers();
     if (t >= s->total_tiles) return false;
     g.tile = t;
     g.kb0 = 0;
@@ -185,12 +188,12 @@ __device__ __forceinline__ int64_t row_of(const OutRef& o, int b1, int b2) { ret
 // (cluster address bar_cl).
 template <bool MN, int EXT, bool PAIR>
 __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, uint32_t bar_cl,
-                                             int64_t row0, int64_t i0, int64_t k0) {
+                                             int64_t row0, int64_t i0, int64_t k0, uint64_t pol) {
   auto copy = [&](uint8_t* d, int x, int y) {
     if constexpr (PAIR)
-      tma_load_2d_pair(d, map, bar_cl, x, y);
+      tma_load_2d_pair(d, map, bar_cl, x, y, pol);
     else
-      tma_load_2d(d, map, bar, x, y);
+      tma_load_2d(d, map, bar, x, y, pol);
   };
   if constexpr (MN) {
 #pragma unroll
@@ -208,13 +211,14 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
 // the 32-byte-swizzle layout (gemm.h::plane_index).
 template <int EXT, bool PAIR>
 __device__ __forceinline__ void load_plane_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                                   uint32_t bar_cl, int64_t rb0, int64_t cb, int64_t n0, int64_t k0) {
+                                                   uint32_t bar_cl, int64_t rb0, int64_t cb, int64_t n0, int64_t k0,
+                                                   uint64_t pol) {
   const int c1 = static_cast<int>((k0 % kPlaneRows) / 16);
   const int c2 = static_cast<int>((rb0 + k0 / kPlaneRows) * cb + n0 / kPlaneCols);
   if constexpr (PAIR)
-    tma_load_3d_pair(dst, map, bar_cl, 0, c1, c2);
+    tma_load_3d_pair(dst, map, bar_cl, 0, c1, c2, pol);
   else
-    tma_load_3d(dst, map, bar, 0, c1, c2);
+    tma_load_3d(dst, map, bar, 0, c1, c2, pol);
 }
 
 // Shared-memory descriptor of the k-th 16-wide K step of an operand tile.
@@ -379,7 +383,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       uint32_t kc = 0, pst = 0, pph = 0;  // k-blocks issued; stage and phase of the next one
       uint32_t issued_mask = 0;
       bool ok = true;
-      while (ok && iter.next(seg)) {
+      const uint64_t pol_a = l2_policy(p.l2_a), pol_b = l2_policy(p.l2_b);
+      while (ok && iter.next<EPI == EPI_STORE>(seg)) {
         int bi;
         int64_t mt, nt;
         kp.s.tile_coords(seg.tile, bi, mt, nt);
@@ -404,23 +409,36 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           if (mma_cta) mbar_arrive_expect_tx(&full_bar[st], (PAIR ? 2 : 1) * C::STAGE_BYTES);
           issued_mask |= 1u << st;
           const int64_t k0 = static_cast<int64_t>(kb) * BK;
-          load_operand<A_MN, BM, PAIR>(sa, &tmA, &full_bar[st], bar_cl, ra, mt * BM, k0);
+          load_operand<A_MN, BM, PAIR>(sa, &tmA, &full_bar[st], bar_cl, ra, mt * BM, k0, pol_a);
           if constexpr (B_PL) {
             load_plane_operand<C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, pb0, p.w.cb,
-                                                nt * BN + rank * C::B_COLS, k0);
+                                                nt * BN + rank * C::B_COLS, k0, pol_b);
           } else if constexpr (PAIR && NB == 2) {
             // the even CTA holds the first B operand, its peer the second
             if (rank == 0)
-              load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN, k0);
+              load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN, k0, pol_b);
             else
-              load_operand<B_MN, BN, PAIR>(sb, &tmB2, &full_bar[st], bar_cl, rb2, nt * BN, k0);
+              load_operand<B_MN, BN, PAIR>(sb, &tmB2, &full_bar[st], bar_cl, rb2, nt * BN, k0, pol_b);
           } else if constexpr (PAIR) {
-            load_operand<B_MN, C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN + rank * C::B_COLS, k0);
+            load_operand<B_MN, C::B_COLS, PAIR>(sb, &tmB, &full_bar[st], bar_cl, rb, nt * BN + rank * C::B_COLS, k0,
+                                                pol_b);
           } else {
-            load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], 0u, rb, nt * BN, k0);
+            load_operand<B_MN, BN, PAIR>(sb, &tmB, &full_bar[st], 0u, rb, nt * BN, k0, pol_b);
             if constexpr (NB == 2)
-              load_operand<B_MN, BN, PAIR>(sb + BN * BK * 2, &tmB2, &full_bar[st], 0u, rb2, nt * BN, k0);
+              load_operand<B_MN, BN, PAIR>(sb + BN * BK * 2, &tmB2, &full_bar[st], 0u, rb2, nt * BN, k0, pol_b);
           }
+        }
+      }
+      // This CTA's share of the next kernel's operand, into L2 (see GemmProblem::pf_ptr).
+      if (ok && p.pf_ptr) {
+        const int64_t total = p.pf_bytes * p.pf_count;
+        const int64_t lo = (total * blockIdx.x / gridDim.x) & ~int64_t{255};
+        const int64_t hi = (blockIdx.x + 1 == gridDim.x) ? total : ((total * (blockIdx.x + 1) / gridDim.x) & ~int64_t{255});
+        for (int64_t off = lo; off < hi;) {
+          const int64_t e = off / p.pf_bytes, in = off - e * p.pf_bytes;
+          const int64_t n = min(min(hi - off, p.pf_bytes - in), int64_t{65536});
+          prefetch_l2_bulk(static_cast<const uint8_t*>(p.pf_ptr) + e * p.pf_stride + in, static_cast<uint32_t>(n));
+          off += n;
         }
       }
       // Teardown: every copy issued here must have landed before the CTA's
@@ -451,7 +469,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       const int kb_full = static_cast<int>(p.K / BK);  // k-blocks with all BK/16 steps inside K
       uint32_t ls = 0, st = 0, ph = 0;  // tiles done; stage and phase of the next k-block
       bool ok = true;
-      while (ok && iter.next(seg)) {
+      while (ok && iter.next<EPI == EPI_STORE>(seg)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error)) break;
         tc_fence_after();
@@ -550,20 +568,22 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       // planes of the chunks in flight, indexed by chunk % 4: each row's 32 bytes as stored
       // (halves swapped where sw is set), one 32-byte load per plane
       uint32_t wh[4][8], wl[4][8];
+      const uint64_t pol_hi = l2_policy(p.planes_l2 ? L2_EVICT_LAST : L2_NORMAL);
+      const uint64_t pol_lo = l2_policy(p.planes_l2 ? L2_EVICT_FIRST : L2_NORMAL);
       auto wload = [&](const TileW& t, int c, uint32_t (&h)[8], uint32_t (&l)[8]) {
         if (t.hi == nullptr || t.cb0 + c >= p.w.cb) return;
-        ld_global_v8(t.hi + static_cast<int64_t>(c) * kPlaneBlock, h);
-        ld_global_v8(t.lo + static_cast<int64_t>(c) * kPlaneBlock, l);
+        ld_global_v8_hint(t.hi + static_cast<int64_t>(c) * kPlaneBlock, h, pol_hi);
+        ld_global_v8_hint(t.lo + static_cast<int64_t>(c) * kPlaneBlock, l, pol_lo);
       };
       SegIter ahead = iter;
       Seg cur, nxt;
-      bool have = ahead.next(cur);
+      bool have = ahead.next<EPI == EPI_STORE>(cur);
       TileW tw = have ? tile_w(cur) : TileW{nullptr, nullptr, 0};
       wload(tw, group, wh[0], wl[0]);
       wload(tw, group + 2, wh[1], wl[1]);
       wload(tw, group + 4, wh[2], wl[2]);
       while (have) {
-        const bool have_next = ahead.next(nxt);
+        const bool have_next = ahead.next<EPI == EPI_STORE>(nxt);
         const TileW tn = have_next ? tile_w(nxt) : TileW{nullptr, nullptr, 0};
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         if (!failed)
@@ -613,8 +633,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
                 ls8[q] = sw ? lo[q + 4] : lo[q];
                 ls8[q + 4] = sw ? lo[q] : lo[q + 4];
               }
-              st_global_v8(tw.hi + static_cast<int64_t>(c) * kPlaneBlock, hs);
-              st_global_v8(tw.lo + static_cast<int64_t>(c) * kPlaneBlock, ls8);
+              st_global_v8_hint(tw.hi + static_cast<int64_t>(c) * kPlaneBlock, hs, pol_hi);
+              st_global_v8_hint(tw.lo + static_cast<int64_t>(c) * kPlaneBlock, ls8, pol_lo);
             }
           }
         }
@@ -634,7 +654,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       }
     } else {
       uint32_t sc = 0;
-      while (iter.next(seg)) {
+      while (iter.next<EPI == EPI_STORE>(seg)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
         if (!failed)
