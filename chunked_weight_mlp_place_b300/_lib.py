@@ -27,7 +27,7 @@ EXPORTS = (
     "ipttt_workspace_size", "ipttt_sync_status", "ipttt_release", "ipttt_last_launch_count",
     "ipttt_status_string", "ipttt_version", "ipttt_kernel_timing", "ipttt_kernel_timing_read",
     "ipttt_kernel_name", "ipttt_make_targets_noalloc", "ipttt_layer_forward_varlen", "ipttt_layers_forward",
-    "ipttt_additive_sums", "ipttt_weight_axpy", "ipttt_set_pool_limit",
+    "ipttt_additive_sums", "ipttt_weight_axpy", "ipttt_set_pool_limit", "ipttt_set_wait_limit",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
 KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy",
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         dp = ctypes.POINTER(Dims)
         L.ipttt_layer_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, f32, i32, vp, vp, dp, vp]
         L.ipttt_set_pool_limit.argtypes = [ctypes.c_size_t]
+        L.ipttt_set_wait_limit.argtypes = [ctypes.c_uint64]
+        L.ipttt_set_wait_limit.restype = i32
         L.ipttt_additive_sums.argtypes = [vp, vp, i64, vp, dp, vp]
         L.ipttt_weight_axpy.argtypes = [vp, vp, f32, i64, vp]
         L.ipttt_layers_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, i32, vp, vp, dp, vp]
@@ -135,6 +137,27 @@ def _ptr(t, name: str, dtype=None) -> int:
     return t.data_ptr()
 
 
+def _shape(t, shape, name: str) -> None:
+    """The C-ABI takes sizes, not tensors: a tensor smaller than the sizes say
+    would be read or written past its end on the device, so shapes are checked
+    here, before the call."""
+    if t is not None and tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(int(x) for x in shape)}")
+
+
+def _rows_per_seq(rows: int, L: int, name: str) -> int:
+    if L <= 0 or rows % L:
+        raise ValueError(f"{name} has {rows} rows, not a whole number of sequences of L={L}")
+    return rows // L
+
+
+def _w0_shapes(W_o0, batch: int, d_ff: int, d: int):
+    if W_o0.dim() == 3:
+        _shape(W_o0, (batch, d_ff, d), "W_o0")
+    else:
+        _shape(W_o0, (d_ff, d), "W_o0")
+
+
 def _stream(stream) -> int:
     torch = _torch()
     if stream is None:
@@ -155,7 +178,12 @@ def layer_forward(X, E, W_g, W_u, W_o0, conv_w, P, L: int, B: int, eta: float, r
     torch = _torch()
     act = X.dtype
     d, d_ff = W_g.shape
-    batch = X.shape[0] // L if L else W_final.shape[0]
+    batch = _rows_per_seq(X.shape[0], L, "X") if L else W_final.shape[0]
+    for t, shp, nm in ((X, (batch * L, d), "X"), (E, (batch * L, d), "E"), (W_u, (d, d_ff), "W_u"),
+                       (conv_w, (d, 4), "conv_w"), (P, (d, d), "P"), (O, (batch * L, d), "O"),
+                       (W_final, (batch, d_ff, d), "W_final")):
+        _shape(t, shp, nm)
+    _w0_shapes(W_o0, batch, d_ff, d)
     dm = dims(batch, d, d_ff, _dtype_code(X), 1 if W_o0.dim() == 3 else 0)
     st = lib().ipttt_layer_forward(
         _ptr(X, "X", act), _ptr(E, "E", act), _ptr(W_g, "W_g", act), _ptr(W_u, "W_u", act),
@@ -176,6 +204,13 @@ def layer_forward_varlen(X, E, W_g, W_u, W_o0, conv_w, P, cu_seqlens, B: int, et
     d, d_ff = W_g.shape
     cu = [int(c) for c in cu_seqlens]
     n_docs = len(cu) - 1
+    T = X.shape[0]
+    if n_docs < 0 or cu[-1] != T:
+        raise ValueError(f"cu_seqlens must end at the number of rows of X ({T})")
+    for t, shp, nm in ((E, (T, d), "E"), (W_u, (d, d_ff), "W_u"), (conv_w, (d, 4), "conv_w"), (P, (d, d), "P"),
+                       (O, (T, d), "O"), (W_final, (n_docs, d_ff, d), "W_final")):
+        _shape(t, shp, nm)
+    _w0_shapes(W_o0, n_docs, d_ff, d)
     cu_arr = (ctypes.c_int64 * max(1, len(cu)))(*cu)
     dm = dims(n_docs, d, d_ff, _dtype_code(X), 1 if W_o0.dim() == 3 else 0)
     st = lib().ipttt_layer_forward_varlen(
@@ -195,7 +230,15 @@ def layers_forward(X, E, W_g, W_u, W_o0, conv_w, P, L: int, B: int, eta: float, 
     torch = _torch()
     act = X.dtype
     n_layers, d, d_ff = W_g.shape
-    batch = X.shape[1] // L if L else W_final.shape[1]
+    batch = _rows_per_seq(X.shape[1], L, "X") if L else W_final.shape[1]
+    for t, shp, nm in ((X, (n_layers, batch * L, d), "X"), (E, (batch * L, d), "E"), (W_u, (n_layers, d, d_ff), "W_u"),
+                       (conv_w, (n_layers, d, 4), "conv_w"), (P, (n_layers, d, d), "P"),
+                       (O, (n_layers, batch * L, d), "O"), (W_final, (n_layers, batch, d_ff, d), "W_final")):
+        _shape(t, shp, nm)
+    if W_o0.dim() == 4:
+        _shape(W_o0, (n_layers, batch, d_ff, d), "W_o0")
+    else:
+        _shape(W_o0, (n_layers, d_ff, d), "W_o0")
     dm = dims(batch, d, d_ff, _dtype_code(X), 1 if W_o0.dim() == 4 else 0)
     st = lib().ipttt_layers_forward(
         _ptr(X, "X", act), _ptr(E, "E", act), _ptr(W_g, "W_g", act), _ptr(W_u, "W_u", act),
@@ -205,11 +248,21 @@ def layers_forward(X, E, W_g, W_u, W_o0, conv_w, P, L: int, B: int, eta: float, 
     _check(st, "ipttt_layers_forward")
 
 
+def _targets_shapes(E, conv_w, P, V, L: int) -> None:
+    d = E.shape[1]
+    if L:
+        _rows_per_seq(E.shape[0], L, "E")
+    _shape(V, E.shape, "V")
+    _shape(P, (d, d), "P")
+    _shape(conv_w, (d, 4), "conv_w")
+
+
 def make_targets(E, conv_w, P, V, L: int, B: int, stream=None) -> None:
     """ipttt_make_targets: V = Proj(Conv(E)) with chunk-end padding."""
     torch = _torch()
     act = E.dtype
     d = E.shape[1]
+    _targets_shapes(E, conv_w, P, V, L)
     dm = dims(E.shape[0] // L if L else 0, d, 8, _dtype_code(E))
     st = lib().ipttt_make_targets(_ptr(E, "E", act), _ptr(conv_w, "conv_w", torch.float32), _ptr(P, "P", act),
                                   _ptr(V, "V", act), int(L), int(B), ctypes.byref(dm), _stream(stream))
@@ -225,6 +278,7 @@ def make_targets_noalloc(E, conv_w, P, V, L: int, B: int, stream=None) -> None:
     torch = _torch()
     act = E.dtype
     d = E.shape[1]
+    _targets_shapes(E, conv_w, P, V, L)
     dm = dims(E.shape[0] // L if L else 0, d, 8, _dtype_code(E))
     st = lib().ipttt_make_targets_noalloc(_ptr(E, "E", act), _ptr(conv_w, "conv_w", torch.float32),
                                           _ptr(P, "P", act), _ptr(V, "V", act), int(L), int(B), ctypes.byref(dm),
@@ -240,6 +294,9 @@ def gate_up(X, W_g, W_u, Z, stream=None) -> None:
     """ipttt_gate_up: Z = SiLU(X W_g) * (X W_u)."""
     act = X.dtype
     d, d_ff = W_g.shape
+    T = X.shape[0]
+    for t, shp, nm in ((X, (T, d), "X"), (W_u, (d, d_ff), "W_u"), (Z, (T, d_ff), "Z")):
+        _shape(t, shp, nm)
     dm = dims(1, d, d_ff, _dtype_code(X))
     st = lib().ipttt_gate_up(_ptr(X, "X", act), _ptr(W_g, "W_g", act), _ptr(W_u, "W_u", act), _ptr(Z, "Z", act),
                              int(X.shape[0]), ctypes.byref(dm), _stream(stream))
@@ -252,7 +309,10 @@ def chunk_forward(Z, V, W_o0, L: int, B: int, eta: float, rule, O, W_final, stre
     act = Z.dtype
     d_ff = Z.shape[1]
     d = V.shape[1]
-    batch = Z.shape[0] // L if L else W_final.shape[0]
+    batch = _rows_per_seq(Z.shape[0], L, "Z") if L else W_final.shape[0]
+    for t, shp, nm in ((V, (batch * L, d), "V"), (O, (batch * L, d), "O"), (W_final, (batch, d_ff, d), "W_final")):
+        _shape(t, shp, nm)
+    _w0_shapes(W_o0, batch, d_ff, d)
     dm = dims(batch, d, d_ff, _dtype_code(Z), 1 if W_o0.dim() == 3 else 0)
     st = lib().ipttt_chunk_forward(_ptr(Z, "Z", act), _ptr(V, "V", act), _ptr(W_o0, "W_o0", torch.float32),
                                    int(L), int(B), float(eta), _RULES[rule], _ptr(O, "O", act),
@@ -264,6 +324,13 @@ def set_pool_limit(nbytes: int) -> None:
     """ipttt_set_pool_limit: calls needing more scratch than `nbytes` fail with
     IPTTT_ERR_ALLOC before queuing anything (0 = no limit)."""
     _check(lib().ipttt_set_pool_limit(int(nbytes)), "ipttt_set_pool_limit")
+
+
+def set_wait_limit(ns: int) -> None:
+    """ipttt_set_wait_limit: soft limit (ns) of the tensor-core kernels' pipeline
+    waits on the current device; 0 restores the default.  A longer wait makes
+    the call's outputs unspecified and ipttt_sync_status report ERR_TIMEOUT."""
+    _check(lib().ipttt_set_wait_limit(int(ns)), "ipttt_set_wait_limit")
 
 
 def copy_weights(W_o0, W, stream=None) -> None:
@@ -281,7 +348,9 @@ def additive_sums(Z, V, L: int, S, stream=None) -> None:
     """ipttt_additive_sums: S[s] = Z_s^T V_s (fp32, (batch, d_ff, d)) over L tokens per sequence."""
     torch = _torch()
     act = Z.dtype
-    batch = Z.shape[0] // L if L else S.shape[0]
+    batch = _rows_per_seq(Z.shape[0], L, "Z") if L else S.shape[0]
+    _shape(V, (batch * L, V.shape[1]), "V")
+    _shape(S, (batch, Z.shape[1], V.shape[1]), "S")
     dm = dims(batch, V.shape[1], Z.shape[1], _dtype_code(Z))
     _check(lib().ipttt_additive_sums(_ptr(Z, "Z", act), _ptr(V, "V", act), int(L), _ptr(S, "S", torch.float32),
                                      ctypes.byref(dm), _stream(stream)), "ipttt_additive_sums")

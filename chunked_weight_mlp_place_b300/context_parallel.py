@@ -26,7 +26,7 @@ import torch.distributed as dist
 
 from . import _lib as ip
 
-__all__ = ["LibraryBackend", "additive_forward"]
+__all__ = ["LibraryBackend", "additive_forward", "allgather_earlier"]
 
 
 class LibraryBackend:
@@ -57,27 +57,36 @@ class LibraryBackend:
         ip.chunk_forward(Z, V, W_start, L, B, eta, "add", O, W_final)
 
 
+def allgather_earlier(S, group=None):
+    """The chunk sums of the ranks before this one, by one all-gather over `group`
+    (every rank receives world - 1 sums of batch x d_ff x d fp32); none without
+    an initialised process group."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size(group) == 1:
+        return []
+    gathered = [torch.empty_like(S) for _ in range(dist.get_world_size(group))]
+    dist.all_gather(gathered, S, group=group)
+    return gathered[:dist.get_rank(group)]
+
+
 def additive_forward(X, E, W_g, W_u, W_o0, conv_w, P, L: int, B: int, eta: float, O, W_final, group=None,
-                     backend=None) -> None:
+                     backend=None, exchange=None) -> None:
     """This rank's part of the additive rule over sequences split across the ranks of `group`.
 
     X, E: this rank's run of every sequence, (batch*L, d), sequence s in rows
     s*L .. s*L+L-1; W_g, W_u, conv_w, P, W_o0 as in ipttt_layer_forward (the
     same on every rank).  O (batch*L, d): this rank's outputs; W_final
     (batch, d_ff, d): the fast weight after this rank's chunks (the sequence's
-    final weight on the last rank).  Without an initialised process group the
-    call is one rank: the plain additive rule.
+    final weight on the last rank).
+
+    ``exchange(S, group)`` returns the chunk sums of the earlier ranks given this
+    rank's own; the default is :func:`allgather_earlier` (without an initialised
+    process group: none, so the call is the plain additive rule).  Passing one
+    lets the ranks run in turn in one process, each handing its sum to the next.
     """
     be = backend if backend is not None else LibraryBackend()
-    on = dist.is_available() and dist.is_initialized()
-    world = dist.get_world_size(group) if on else 1
-    rank = dist.get_rank(group) if on else 0
     Z, V = be.gate_targets(X, E, W_g, W_u, conv_w, P, L, B)
     S = be.sums(Z, V, L)
     W_start = be.start(W_o0, S.shape[0], B)
-    if world > 1:
-        gathered = [torch.empty_like(S) for _ in range(world)]
-        dist.all_gather(gathered, S, group=group)
-        for r in range(rank):
-            be.axpy(W_start, gathered[r], eta / B)
+    for S_r in (exchange or allgather_earlier)(S, group):
+        be.axpy(W_start, S_r, eta / B)
     be.chunk_forward(Z, V, W_start, L, B, eta, O, W_final)

@@ -26,6 +26,7 @@
 #include <vector>
 
 #include "ipttt.h"
+#include "checks.h"
 #include "gemm.h"
 #include "launch.h"
 
@@ -216,7 +217,30 @@ ipttt_status from_cuda(cudaError_t e) {
     }                                          \
   } while (0)
 
+}  // namespace
+
+// ------------------------------------------------------------- checks
+// (declared in checks.h: every entry point, the allocation-free one included, validates
+// its arguments through these, so the same bad argument gives the same status everywhere)
+namespace {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pointer must be non-null, 16-byte aligned and reachable from the device.
+ipttt_status check_ptr_host(const void* p) {
+  if (!p || !aligned16(p)) return IPTTT_ERR_INVALID_ARG;
+  return IPTTT_OK;
+}
+ipttt_status check_ptr_device(const void* p) {
+  cudaPointerAttributes a;
+  const cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return IPTTT_ERR_INVALID_ARG;
+  }
+  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return IPTTT_ERR_INVALID_ARG;
+  return IPTTT_OK;
+}
+}  // namespace
 
 ipttt_status check_dims(const ipttt_dims* dims, bool need_batch) {
   if (!dims) return IPTTT_ERR_INVALID_ARG;
@@ -238,22 +262,6 @@ ipttt_status check_chunking(const ipttt_dims* dims, int64_t L, int64_t B) {
   return IPTTT_OK;
 }
 
-// Pointer must be non-null, 16-byte aligned and reachable from the device.
-ipttt_status check_ptr_host(const void* p) {
-  if (!p || !aligned16(p)) return IPTTT_ERR_INVALID_ARG;
-  return IPTTT_OK;
-}
-ipttt_status check_ptr_device(const void* p) {
-  cudaPointerAttributes a;
-  const cudaError_t e = cudaPointerGetAttributes(&a, p);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return IPTTT_ERR_INVALID_ARG;
-  }
-  if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return IPTTT_ERR_INVALID_ARG;
-  return IPTTT_OK;
-}
-
 ipttt_status check_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -271,13 +279,14 @@ ipttt_status check_device() {
 }
 
 // All pointers: host-side checks first (no CUDA call), then the device checks.
-template <size_t N>
-ipttt_status check_ptrs(const void* const (&ps)[N]) {
-  for (const void* p : ps) IPTTT_TRY(check_ptr_host(p));
+ipttt_status check_ptr_list(const void* const* ps, int n) {
+  for (int i = 0; i < n; ++i) IPTTT_TRY(check_ptr_host(ps[i]));
   IPTTT_TRY(check_device());
-  for (const void* p : ps) IPTTT_TRY(check_ptr_device(p));
+  for (int i = 0; i < n; ++i) IPTTT_TRY(check_ptr_device(ps[i]));
   return IPTTT_OK;
 }
+
+namespace {
 
 cudaError_t gemm(const GemmProblem& p, bool bf16, cudaStream_t st) {
   return bf16 ? launch_gemm_tc(p, st) : launch_gemm_simt(p, st);
@@ -1101,6 +1110,12 @@ ipttt_status ipttt_sync_status(ipttt_stream stream) {
     return IPTTT_ERR_CUDA;
   }
   return code ? IPTTT_ERR_TIMEOUT : IPTTT_OK;
+}
+
+ipttt_status ipttt_set_wait_limit(uint64_t ns) {
+  IPTTT_TRY(check_device());
+  IPTTT_CUDA(set_wait_soft_limit(ns));
+  return IPTTT_OK;
 }
 
 ipttt_status ipttt_release(void) {

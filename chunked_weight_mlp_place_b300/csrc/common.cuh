@@ -110,19 +110,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase of `bar` with the given parity has completed.  Gives
-// up when `*abort` becomes non-zero (another role gave up) or after
-// kWaitLimitNs; in the latter case it raises `*abort`, records `code` in
-// `*err_word` (if it still holds 0) and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  int code, int* err_word) {
+// Levels of a CTA's shared abort word.  kAbortSoft: a wait ran past the soft
+// limit; the CTA stops issuing MMAs and global writes but keeps every
+// handshake, so that each copy and MMA already issued completes before it
+// exits.  kAbortHard: a wait ran past kWaitLimitNs; that role gives up and the
+// others stop waiting.
+constexpr int kAbortSoft = 1, kAbortHard = 2;
+
+// Wait until the phase of `bar` with the given parity has completed.  Past
+// `soft_ns` it raises the abort word to kAbortSoft and records `code` in
+// `*err_word` (if that still holds 0), and keeps waiting; past kWaitLimitNs, or
+// once another role has given up (kAbortHard), it returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int code,
+                                                  int* err_word, uint64_t soft_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
+    const int a = *abort;
+    if (a == kAbortHard) return false;
+    const uint64_t el = globaltimer_ns() - t0;
+    if (el > soft_ns && a == 0) {
+      atomicMax(const_cast<int*>(abort), kAbortSoft);
+      atomicCAS(err_word, 0, code);
+    }
+    if (el > kWaitLimitNs) {
+      atomicMax(const_cast<int*>(abort), kAbortHard);
+      atomicCAS(err_word, 0, code);
+      return false;
+    }
+  }
+}
+
+// Teardown: wait for a phase that copies or MMAs already issued complete,
+// whatever the abort word says, for at most kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int code, int* err_word) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
       atomicCAS(err_word, 0, code);
       return false;
     }

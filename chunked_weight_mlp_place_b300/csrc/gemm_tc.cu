@@ -52,6 +52,11 @@ namespace ipttt {
 // and cleared through read_clear_device_error().  Codes: 1 = TMA-producer
 // wait, 2 = MMA-issuer wait, 3 = epilogue wait, 4 = teardown drain.
 __device__ int g_device_error = 0;
+// Soft limit of the pipeline waits (ns): past it a CTA records a code in g_device_error and
+// stops issuing MMAs and global writes, but completes its handshakes (common.cuh,
+// mbar_wait_bounded).  Set from the host (ipttt_set_wait_limit); by default it equals the
+// hard limit, so only a wait that hangs trips it.
+__device__ unsigned long long g_wait_soft_ns = kWaitLimitNs;
 
 namespace tc {
 
@@ -372,6 +377,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
   // the previous kernel's tail.  Global memory from here on.
   pdl_wait();
   pdl_trigger();
+  const uint64_t soft_ns = g_wait_soft_ns;
 
   SegIter iter;
   iter.init(&kp.s);
@@ -398,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
             pst = 0;
             pph ^= 1;
           }
-          if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1, abort_flag, 1, &g_device_error)) {
+          if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1, abort_flag, 1, &g_device_error, soft_ns)) {
             ok = false;
             break;
           }
@@ -449,9 +455,9 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         if (!(issued_mask & (1u << st))) continue;
         const uint32_t f = (kc - 1 - st) / C::STAGES;  // last fill of stage st
         if (PAIR && !mma_cta)
-          mbar_wait_bounded(&empty_bar[st], f & 1, abort_flag, 4, &g_device_error);
+          mbar_wait_drain(&empty_bar[st], f & 1, 4, &g_device_error);
         else
-          mbar_wait_bounded(&full_bar[st], f & 1, abort_flag, 4, &g_device_error);
+          mbar_wait_drain(&full_bar[st], f & 1, 4, &g_device_error);
       }
     }
   } else if (warp == 1) {
@@ -471,11 +477,11 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       bool ok = true;
       while (ok && iter.next<EPI == EPI_STORE>(seg)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
-        if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error)) break;
+        if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error, soft_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kAccStride;
         for (int kb = seg.kb0; kb < seg.kb1; ++kb) {
-          if (!mbar_wait_bounded(&full_bar[st], ph, abort_flag, 2, &g_device_error)) {
+          if (!mbar_wait_bounded(&full_bar[st], ph, abort_flag, 2, &g_device_error, soft_ns)) {
             ok = false;
             break;
           }
@@ -483,7 +489,9 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           const uint32_t soff = (st * C::STAGE_BYTES) >> 4;
           const uint64_t ad = a0 + soff, bd = b0 + soff;
           const uint32_t first = (kb == seg.kb0) ? 0u : 1u;
-          if (kb < kb_full) {
+          if (*abort_flag) {
+            // aborted: no more MMAs; the commit below still frees the stage
+          } else if (kb < kb_full) {
 #pragma unroll
             for (int ks = 0; ks < BK / 16; ++ks) {
               if constexpr (PAIR)
@@ -521,7 +529,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         umma_commit_pair_both(drain_bar);
       else
         umma_commit(drain_bar);
-      mbar_wait_bounded(drain_bar, 0, abort_flag, 4, &g_device_error);
+      mbar_wait_drain(drain_bar, 0, 4, &g_device_error);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -587,7 +595,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         const TileW tn = have_next ? tile_w(nxt) : TileW{nullptr, nullptr, 0};
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         if (!failed)
-          failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error));
+          failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error, soft_ns));
         tc_fence_after();
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
         uint32_t ra[WC], rb[WC];
@@ -623,7 +631,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               split_w2(fmaf(p.alpha, __uint_as_float(r[2 * q]), w0), fmaf(p.alpha, __uint_as_float(r[2 * q + 1]), w1),
                        ho[q], lo[q]);
             }
-            if (!failed && tw.hi != nullptr && tw.cb0 + c < p.w.cb) {
+            if (!failed && !*abort_flag && tw.hi != nullptr && tw.cb0 + c < p.w.cb) {
               // whole 32-byte rows, halves back in stored order
               uint32_t hs[8], ls8[8];
 #pragma unroll
@@ -658,7 +666,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
         if (!failed)
-          failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error));
+          failed = !__all_sync(0xffffffffu, mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error, soft_ns));
         tc_fence_after();
         int bi;
         int64_t mt, nt;
@@ -691,7 +699,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               fence_proxy_async_shared();
               if (issuer) bulk_wait_group_read<0>();  // the other buffer, written next chunk, is free
               epi_barrier(0);
-              if (issuer && !failed) {
+              if (issuer && !failed && !*abort_flag) {
                 tma_reduce_add_2d(&tmD, sbuf, static_cast<int>(n), static_cast<int>(row_of(p.D, b1, b2) + mt * BM));
                 bulk_commit_group();
               }
@@ -699,7 +707,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               continue;
             }
           }
-          if (m < p.M && !failed) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
+          if (m < p.M && !failed && !*abort_flag) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
         }
         // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
         tc_fence_before();
@@ -890,6 +898,11 @@ static cudaError_t run_any(const GemmProblem& p, cudaStream_t stream) {
 }
 
 }  // namespace tc
+
+cudaError_t set_wait_soft_limit(uint64_t ns) {
+  const unsigned long long v = (ns == 0 || ns > kWaitLimitNs) ? kWaitLimitNs : ns;
+  return cudaMemcpyToSymbol(g_wait_soft_ns, &v, sizeof(v));
+}
 
 cudaError_t read_clear_device_error(int* code) {
   const int zero = 0;

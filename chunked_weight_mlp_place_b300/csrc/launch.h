@@ -68,6 +68,8 @@ int device_sm_count();    // SMs of the current device (cached)
 
 // Read the device error word of the current device (0 = no capped wait ran out) and clear it.
 cudaError_t read_clear_device_error(int* code);
+// Soft limit of the tensor-core kernels' pipeline waits on the current device (0: the hard limit).
+cudaError_t set_wait_soft_limit(uint64_t ns);
 
 cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream);    // bf16 operands, tcgen05
 cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream);  // fp32 operands, CUDA cores

@@ -18,8 +18,7 @@
 // writes every byte the projection reads before the projection runs.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
+#include "checks.h"
 #include "gemm.h"
 #include "ipttt.h"
 #include "launch.h"
@@ -30,57 +29,23 @@ static_assert(IPTTT_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
 
 // The conv output of ipttt_make_targets_noalloc.  In host code this name is a
 // host-side stand-in, not a device address: the address kernels use comes
-// from cudaGetSymbolAddress, per device.
+// from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[IPTTT_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
-std::mutex g_addr_mu;
-void* g_addr[64] = {};  // device address of g_noalloc_scratch, per device
-
-// Device address of the scratch array on the current device.  The first call
-// on a device looks it up (this may load the library's kernels on that device).
+// Device address of the scratch array in the current device's context, looked up
+// on every call (cheap once the module is loaded; the first call on a device
+// loads it), so that no address outlives the context it belongs to.
 ipttt_status scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
     cudaGetLastError();
-    return IPTTT_ERR_UNSUPPORTED;
+    return IPTTT_ERR_CUDA;
   }
-  if (dev < 0 || dev >= 64) return IPTTT_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> g(g_addr_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return IPTTT_ERR_CUDA;
-    }
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
+  *out = p;
   return IPTTT_OK;
-}
-
-bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-ipttt_status device_ptr_ok(const void* p) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return IPTTT_ERR_INVALID_ARG;
-  }
-  return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) ? IPTTT_OK : IPTTT_ERR_INVALID_ARG;
-}
-
-ipttt_status device_ok() {
-  int dev = -1, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return IPTTT_ERR_UNSUPPORTED;
-  }
-  return (major == 10 && minor == 3) ? IPTTT_OK : IPTTT_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -92,25 +57,18 @@ extern "C" ipttt_status ipttt_make_targets_noalloc(const void* E, const float* c
                                                    int64_t L, int64_t B, const ipttt_dims* dims,
                                                    ipttt_stream stream) {
   reset_launch_count();
-  if (!dims || (dims->dtype != IPTTT_FP32 && dims->dtype != IPTTT_BF16) || dims->d < 1 || dims->d > (1 << 20) ||
-      dims->batch < 0)
-    return IPTTT_ERR_INVALID_ARG;
-  const bool bf16 = dims->dtype == IPTTT_BF16;
-  if (bf16 && dims->d % 8) return IPTTT_ERR_INVALID_ARG;
-  if (L < 0 || B < 1 || L % B || (bf16 && B % 16)) return IPTTT_ERR_INVALID_ARG;
-  if (dims->batch > 0 && L > (int64_t{1} << 31) / dims->batch) return IPTTT_ERR_INVALID_ARG;
+  // the same checks, in the same order, as ipttt_make_targets
+  ipttt_status st = check_dims(dims, true);
+  if (st != IPTTT_OK) return st;
+  if ((st = check_chunking(dims, L, B)) != IPTTT_OK) return st;
   const int64_t rows = dims->batch * L;
   if (rows == 0) return IPTTT_OK;
+  const bool bf16 = dims->dtype == IPTTT_BF16;
   // The conv output must fit the fixed array: rows * d elements of the act type.
   const int64_t esz = bf16 ? 2 : 4;
   if (rows > static_cast<int64_t>(IPTTT_NOALLOC_SCRATCH_BYTES) / (dims->d * esz)) return IPTTT_ERR_INVALID_ARG;
-  const void* ptrs[4] = {E, conv_w, P, V};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return IPTTT_ERR_INVALID_ARG;
-  ipttt_status st = device_ok();
-  if (st != IPTTT_OK) return st;
-  for (const void* p : ptrs)
-    if ((st = device_ptr_ok(p)) != IPTTT_OK) return st;
+  if ((st = check_ptrs({E, static_cast<const void*>(conv_w), P, static_cast<const void*>(V)})) != IPTTT_OK)
+    return st;
   void* C = nullptr;
   if ((st = scratch_address(&C)) != IPTTT_OK) return st;
 

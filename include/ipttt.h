@@ -233,8 +233,10 @@ ipttt_status ipttt_chunk_forward(const void* Z, const void* V, const float* W_o0
  *   the tokens into chunk-aligned pieces (the conv never reads past a chunk).
  * - The array takes IPTTT_NOALLOC_SCRATCH_BYTES on every GPU that loads the
  *   library, until the process exits.
- * - The first call on a device looks the array's address up on that device
- *   (with that device current); make that first call before any stream
+ * - Every call looks the array's device address up for the current device
+ *   and CUDA context (cudaGetSymbolAddress), so a device reset or another
+ *   device never sees a stale address.  The first call on a device also loads
+ *   the library's kernels there: make that first call before any stream
  *   capture.
  * - Every call shares the array: calls that overlap on the GPU (unordered
  *   streams) race on it.  Nothing in it needs clearing between calls.
@@ -272,6 +274,23 @@ ipttt_status ipttt_workspace_size(const ipttt_dims* dims, int64_t L, int64_t B, 
  * current device: IPTTT_ERR_TIMEOUT if a capped wait ran out since the last
  * check, IPTTT_ERR_CUDA for a CUDA error, else IPTTT_OK. */
 ipttt_status ipttt_sync_status(ipttt_stream stream);
+
+/* Soft limit, in nanoseconds, of the pipeline waits inside the tensor-core
+ * kernels on the current device (0 restores the default, the 2 s hard limit;
+ * larger values are clamped to it).  No counterpart on the pages: it is the
+ * failure-detection hook of the library.  A wait that lasts longer records
+ * IPTTT_ERR_TIMEOUT for ipttt_sync_status(); its CTA then issues no more
+ * tensor-core work and writes no more results, but keeps every handshake of
+ * its pipeline until the copies and MMAs already in flight have completed, so
+ * that the kernel still ends cleanly and the context stays usable.  The
+ * outputs of such a call are unspecified.  Only a wait that reaches the hard
+ * limit gives up outright.  Set it below the length of a real wait (a few
+ * hundred ns) to make the detection fire on purpose; every later call on the
+ * device uses the new value until it is restored.  Synchronous; do not call
+ * it while kernels of the library run on the device.
+ * Errors: IPTTT_ERR_UNSUPPORTED (no compute capability 10.3 device),
+ * IPTTT_ERR_CUDA. */
+ipttt_status ipttt_set_wait_limit(uint64_t ns);
 
 /* Free the scratch pool of every device the library has used.  The caller
  * must make sure no queued call still uses it (synchronise first). */

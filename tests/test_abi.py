@@ -234,3 +234,47 @@ def test_header_is_plain_c_and_the_library_links_from_c(tmp_path):
                     str(exe), "-L", libdir, "-lipttt", "-Wl,-rpath," + libdir], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
     assert int(out[0]) == _lib.lib().ipttt_version() and "wait" in " ".join(out[1:])
+
+
+def test_noalloc_and_pooled_targets_give_the_same_status_for_the_same_bad_argument(L):
+    """Both target builders validate through the same checks: each bad argument
+    below is refused on the host, with the same status, by both entry points."""
+    cases = [
+        (_dims(d_ff=0), FAKE, 256, 64),          # d_ff < 1
+        (_dims(w0=2), FAKE, 256, 64),            # w0_per_seq outside 0/1
+        (_dims(dtype=7), FAKE, 256, 64),         # unknown dtype
+        (_dims(d=60), FAKE, 256, 64),            # bf16 mode, d not a multiple of 8
+        (_dims(), FAKE, 250, 64),                # L not a multiple of B
+        (_dims(), FAKE, 256, 24),                # bf16 mode, B not a multiple of 16
+        (_dims(batch=-1), FAKE, 256, 64),        # negative batch
+        (_dims(), 0, 256, 64),                   # null pointer
+        (_dims(), FAKE + 8, 256, 64),            # pointer not 16-byte aligned
+    ]
+    for dm, ptr, Lseq, B in cases:
+        a = L.ipttt_make_targets(ptr, FAKE, FAKE, FAKE, Lseq, B, ctypes.byref(dm), None)
+        b = L.ipttt_make_targets_noalloc(ptr, FAKE, FAKE, FAKE, Lseq, B, ctypes.byref(dm), None)
+        assert a == b == _lib.ERR_INVALID_ARG, (dm.d, dm.d_ff, dm.dtype, Lseq, B, ptr, a, b)
+    assert L.ipttt_make_targets(FAKE, FAKE, FAKE, FAKE, 256, 64, None, None) == \
+        L.ipttt_make_targets_noalloc(FAKE, FAKE, FAKE, FAKE, 256, 64, None, None) == _lib.ERR_INVALID_ARG
+
+
+def test_binding_checks_shapes_before_the_call():
+    """The C-ABI takes sizes, not tensors, so the binding checks the tensors' shapes
+    against them first (a tensor smaller than the sizes say would be read or
+    written past its end on the device)."""
+    import torch
+    E = torch.zeros(256, 64, dtype=torch.bfloat16)
+    ok = dict(conv_w=torch.zeros(64, 4), P=torch.zeros(64, 64, dtype=torch.bfloat16),
+              V=torch.zeros(256, 64, dtype=torch.bfloat16))
+    for fn in (_lib.make_targets, _lib.make_targets_noalloc):
+        for bad in (dict(V=torch.zeros(128, 64, dtype=torch.bfloat16)), dict(P=torch.zeros(32, 64, dtype=torch.bfloat16)),
+                    dict(conv_w=torch.zeros(64, 3))):
+            kw = dict(ok, **bad)
+            with pytest.raises(ValueError, match="shape"):
+                fn(E, kw["conv_w"], kw["P"], kw["V"], 128, 64)
+        with pytest.raises(ValueError, match="whole number"):
+            fn(E, ok["conv_w"], ok["P"], ok["V"], 96, 32)  # 256 rows are not sequences of 96
+    Z = torch.zeros(256, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="shape"):
+        _lib.chunk_forward(Z, torch.zeros(256, 64, dtype=torch.bfloat16), torch.zeros(128, 64), 128, 64, 0.1, "mse",
+                           torch.zeros(256, 64, dtype=torch.bfloat16), torch.zeros(1, 128, 64))  # W_final: batch 2

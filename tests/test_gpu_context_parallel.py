@@ -45,3 +45,49 @@ def test_one_rank_is_the_additive_layer():
     assert rel(down(O), Oref) <= TOL["bf16"]
     assert rel(down(Wf), Wref) <= TOL["bf16"]
     assert rel(down(Wf) - a["W_o0"], Wref - a["W_o0"]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_ranks_in_turn_through_the_library_equal_the_one_pass_additive_layer(world):
+    """The sequence split into `world` runs of whole chunks; the ranks run one after
+    another in this process, every step through the library (LibraryBackend), each
+    rank's chunk sum handed to the later ranks by the exchange.  The concatenated
+    outputs and the last rank's W_final equal the oracle's one-pass additive layer;
+    the first rank's W_final equals the oracle's over its own chunks only."""
+    batch, L, B, d, d_ff = 2, 256, 64, 128, 256
+    w = inputs.workload("tiny", batch=batch, L=world * L, B=B, d=d, d_ff=d_ff, dtype="bf16", eta=0.05)
+    a = inputs.generate(w, seed=20 + world)
+    t = {k: up(a[k], torch.bfloat16) for k in ("W_g", "W_u", "P")}
+    W0 = torch.from_numpy(a["W_o0"]).cuda()
+    cw = torch.from_numpy(a["conv_w"]).cuda()
+
+    def run_of(k, r):  # rank r's run of L tokens of every sequence
+        x = a[k].reshape(batch, world, L, d)[:, r].reshape(batch * L, d)
+        return np.ascontiguousarray(x)
+
+    sums = []
+
+    def exchange(S, group):  # the earlier ranks' sums; this rank's kept for the later ones
+        earlier = list(sums)
+        sums.append(S.clone())
+        return earlier
+
+    Os, Wfs = [], []
+    for r in range(world):
+        O = torch.empty(batch * L, d, dtype=torch.bfloat16, device="cuda")
+        Wf = torch.empty(batch, d_ff, d, device="cuda")
+        cp.additive_forward(up(run_of("X", r), torch.bfloat16), up(run_of("E", r), torch.bfloat16), t["W_g"],
+                            t["W_u"], W0, cw, t["P"], L, B, w.eta, O, Wf, exchange=exchange)
+        assert ip.sync_status() == 0
+        Os.append(down(O).reshape(batch, L, d))
+        Wfs.append(down(Wf))
+    Oref, Wref = orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"], world * L, B,
+                                   w.eta, "add")
+    O_cat = np.concatenate(Os, axis=1).reshape(batch * world * L, d)
+    assert rel(O_cat, Oref) <= TOL["bf16"], rel(O_cat, Oref)
+    assert rel(Wfs[-1], Wref) <= TOL["bf16"]
+    assert rel(Wfs[-1] - a["W_o0"], Wref - a["W_o0"]) <= TOL["bf16"]
+    O0, W0ref = orc.layer_forward(run_of("X", 0), run_of("E", 0), a["W_g"], a["W_u"], a["W_o0"], a["conv_w"],
+                                  a["P"], L, B, w.eta, "add")
+    assert rel(Os[0].reshape(batch * L, d), O0) <= TOL["bf16"]
+    assert rel(Wfs[0] - a["W_o0"], W0ref - a["W_o0"]) <= TOL["bf16"]

@@ -14,7 +14,7 @@ import torch
 import chunked_weight_mlp_place_b300 as ip
 from chunked_weight_mlp_place_b300 import inputs
 from chunked_weight_mlp_place_b300.build import build
-from gpu_util import TOL, down, rel, up
+from gpu_util import down, up
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,8 @@ def test_noalloc_targets_match_the_pooled_entry_point(dtype, batch, L, B, d):
         assert ip.sync_status() == 0
         a, b = down(V_fixed), down(V_pool)
         assert np.all(np.isfinite(a))
-        assert rel(a, b) <= TOL[dtype], (call, rel(a, b))
+        # the same kernels on the same inputs with a deterministic store epilogue: bit for bit equal
+        np.testing.assert_array_equal(a, b, err_msg=f"call {call}")
 
 
 def test_noalloc_targets_refuse_more_than_the_fixed_scratch():
