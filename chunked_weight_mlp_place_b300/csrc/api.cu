@@ -82,8 +82,8 @@ void drain_timing_locked() {
 void reset_launch_count() { t_launches = 0; }
 
 const char* kind_name(int k) {
-  static const char* names[K_COUNT] = {"gate_up", "conv", "proj",      "apply", "residual",
-                                       "update",  "group_sum", "scan", "weight_copy", "scores"};
+  static const char* names[K_COUNT] = {"gate_up", "conv",  "proj",        "apply",  "residual", "update",
+                                       "group_sum", "scan", "weight_copy", "scores", "engine"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 
@@ -367,8 +367,14 @@ int64_t scan_groups(int64_t K) {
 }
 
 struct EngineLayout {
-  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, ac = 0, bc = 0, total = 0;
+  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, ac = 0, bc = 0, cnt = 0, total = 0;
 };
+
+// Slices of d_ff per apply tile in the persistent MSE engine.
+int engine_parts(const ipttt_dims* dm) { return static_cast<int>(std::min<int64_t>(4, dm->d_ff / 256)); }
+bool use_engine(const ipttt_dims* dm, int64_t B) {
+  return dm->dtype == IPTTT_BF16 && engine_mse_supported(B, dm->d, dm->d_ff);
+}
 
 // Plane geometry of one d_ff x d fast weight (tile-major blocks, see common.cuh).
 int64_t plane_rb(const ipttt_dims* dm) { return (dm->d_ff + kPlaneRows - 1) / kPlaneRows; }
@@ -415,6 +421,7 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
       e.hi = c.take<uint16_t>(dm->batch * np);
       e.lo = c.take<uint16_t>(dm->batch * np);
     }
+    if (use_engine(dm, B)) e.cnt = c.take<uint32_t>(engine_counter_words(dm->batch, L, B, dm->d, engine_parts(dm)));
   } else {
     const int64_t G = scan_groups(K);
     e.o_acc = c.take<float>(G * dm->batch * B * dm->d);
@@ -522,6 +529,30 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
     const int64_t w0_rows = (dm->w0_per_seq ? batch : 1) * dff;
     // The hi planes stay in L2 from one chunk to the next when they take at most half of it.
     const bool keep_hi = bf16 && planes_fit_l2(w);
+    if (use_engine(dm, B)) {
+      // the whole chunk loop in one persistent kernel
+      EngineMse em;
+      em.Z = Z;
+      em.V = V;
+      em.O = O;
+      em.acc = o_acc;
+      em.R = R;
+      em.counters = reinterpret_cast<uint32_t*>(ws + lay.cnt);
+      em.w = w;
+      em.batch = batch;
+      em.L = L;
+      em.B = B;
+      em.d = d;
+      em.d_ff = dff;
+      em.parts = engine_parts(dm);
+      em.alpha = -eta / static_cast<float>(B);
+      em.keep_hi = keep_hi ? 1 : 0;
+      IPTTT_CUDA(cudaMemsetAsync(em.counters, 0,
+                                 sizeof(uint32_t) * engine_counter_words(batch, L, B, d, em.parts), st));
+      IPTTT_CUDA(launch_engine_mse(em, st));
+      IPTTT_CUDA(launch_merge_planes(w, Wf, dff, d, st));
+      return IPTTT_OK;
+    }
     const int64_t zrow = dff * static_cast<int64_t>(act_size(dm));  // bytes of a row of Z
     for (int64_t k = 0; k < K; ++k) {
       // apply: O_acc[s] = Z_k[s] W_k[s], split over d_ff

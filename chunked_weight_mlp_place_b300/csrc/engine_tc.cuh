@@ -1,0 +1,658 @@
+// The MSE chunk loop of the In-Place TTT layer (itsolotime §2.2 and Fig. 1:
+// apply the fast weight to a chunk, then take one gradient step on it) as one
+// persistent kernel over every chunk of every sequence, for sm_103a.
+//
+// The rule is independent across the columns of W_o: column block n (256
+// columns) of O_k, R_k and W_{k+1} depends only on column block n of W_k.  So
+// the loop is cut into work items per column block,
+//
+//   apply  (k, s, n, m, p)  the 256 x 256 tile m of O_k[:, n] summed over slice p
+//                           of d_ff, fp32 partial sums added into `acc` by TMA
+//                           reductions; the item that completes a tile's sum
+//                           (a counter) turns it into O_k and R_k = O_k - V_k and
+//                           clears `acc`;
+//   update (k, s, n, r)     rows 256r .. 256r+255 of W[:, n] += alpha Z_k^T R_k,
+//                           on the split hi/lo planes (common.cuh split_w),
+//
+// and an item waits only for what it reads: an update for the residual of its
+// column block, an apply of chunk k+1 for the update rows of its slice.  Items
+// run in a fixed order of phases A_0, U_0, A_1, U_1, ... (the applies of a chunk,
+// then its updates), each phase column block by column block, and CTA pair w
+// takes items w, w + P, w + 2P, ... of it.  So the updates of the first column
+// blocks start while the last applies of the chunk are still running, the
+// applies of the next chunk while its last updates are, and no kernel boundary,
+// wave tail or separate residual pass stands between the steps.  (A staggered
+// order that mixes the phases of different blocks was measured slower: it
+// spreads the working set over two chunks' activations.)
+// Every dependency points to an earlier item, and a pair finishes an item
+// without waiting for later ones, so the order cannot deadlock; the grid is
+// launched co-resident.
+//
+// Roles as in the GEMM template (gemm_tc.cu): warp 0 the TMA producer (it also
+// waits for an item's inputs), warp 1 the MMA issuer (cta_group::2, 256 x 256
+// x 16 per instruction, two TMEM accumulators), warps 2..9 the epilogue as two
+// groups of four.  Counters between CTAs: a writer fences its generic stores
+// for the async proxy and releases; a reader acquires and fences before its
+// TMA copies.  A wait past the soft limit stops the CTA's MMAs and writes but
+// keeps every handshake and counter, so the grid still ends cleanly.
+//
+// This file is part of gemm_tc.cu's translation unit (the device error word
+// and the soft wait limit are shared).
+
+namespace ipttt {
+namespace tc {
+
+constexpr int kEngStages = 6;
+constexpr int kEngEpiWarps = 8;
+constexpr int kEngThreads = 64 + 32 * kEngEpiWarps;
+constexpr int kEngHalf = 128 * BK * 2;                 // one CTA's A (or B) operand of a stage
+constexpr int kEngStageBytes = 2 * kEngHalf;
+constexpr int kEngStgBytes = 128 * 32 * 4;             // a group's staging tile: 128 rows x 32 fp32
+constexpr int kEngSmem = 1024 + kEngStages * kEngStageBytes + 2 * kEngStgBytes + 512;
+static_assert(kEngSmem <= 227 * 1024, "shared memory");
+
+struct EngParams {
+  EngineMse a;
+  int64_t K, NB, MT, RT;    // chunks; column blocks, token tiles and d_ff tiles of 256
+  int64_t NAb, NUb;         // items of one column block's apply phase and update phase
+  int64_t slots;            // phase slots of the order: 2K
+  int64_t off_apply, off_resid, off_upd;  // counter regions (words)
+};
+
+struct EItem {
+  int upd;  // 0: apply, 1: update
+  int s, n, m, p, r;
+  int64_t k;
+  int kb0, kb1;  // k-blocks of its contraction
+};
+
+// First d_ff tile (of 256 rows) of slice p.
+__device__ __forceinline__ int eng_part_begin(int p, int P, int64_t RT) {
+  return static_cast<int>(static_cast<int64_t>(p) * RT / P);
+}
+__device__ __forceinline__ int eng_part_of(int r, int P, int64_t RT) {
+  int p = 0;
+  while (p + 1 < P && eng_part_begin(p + 1, P, RT) <= r) ++p;
+  return p;
+}
+
+__device__ __forceinline__ int64_t eng_phase_items(const EngParams& e, int64_t ph) { return (ph & 1) ? e.NUb : e.NAb; }
+
+// Items of slot tau: every column block's phase tau (applies at even slots).
+__device__ __forceinline__ int64_t eng_slot_items(const EngParams& e, int64_t tau) {
+  return e.NB * eng_phase_items(e, tau);
+}
+
+// Position in the order: item j of phase slot tau (slot 2k: the applies of chunk k, every
+// column block's in turn; slot 2k + 1: its updates).  Each role walks its pair's items, w, w + P, ...
+struct ECursor {
+  int64_t tau, j;
+  __device__ void normalize(const EngParams& e) {
+    while (tau < e.slots) {
+      const int64_t c = eng_slot_items(e, tau);
+      if (j < c) return;
+      j -= c;
+      ++tau;
+    }
+  }
+  __device__ void start(const EngParams& e, int64_t first) {
+    tau = 0;
+    j = first;
+    normalize(e);
+  }
+  __device__ void advance(const EngParams& e, int64_t step) {
+    j += step;
+    normalize(e);
+  }
+  __device__ bool done(const EngParams& e) const { return tau >= e.slots; }
+};
+
+__device__ __forceinline__ EItem eng_decode(const EngParams& e, const ECursor& cur) {
+  EItem it;
+  const int64_t c = eng_phase_items(e, cur.tau);
+  const int64_t n = cur.j / c;
+  int64_t rem = cur.j - n * c;
+  const int64_t ph = cur.tau;
+  it.k = ph / 2;
+  it.n = static_cast<int>(n);
+  const int P = e.a.parts;
+  if (!(ph & 1)) {
+    it.upd = 0;
+    it.p = static_cast<int>(rem % P);
+    rem /= P;
+    it.m = static_cast<int>(rem % e.MT);
+    it.s = static_cast<int>(rem / e.MT);
+    it.r = 0;
+    it.kb0 = eng_part_begin(it.p, P, e.RT) * 4;
+    it.kb1 = eng_part_begin(it.p + 1, P, e.RT) * 4;
+  } else {
+    it.upd = 1;
+    it.r = static_cast<int>(rem % e.RT);
+    it.s = static_cast<int>(rem / e.RT);
+    it.m = it.p = 0;
+    it.kb0 = 0;
+    it.kb1 = static_cast<int>(e.a.B / BK);
+  }
+  return it;
+}
+
+__device__ __forceinline__ uint32_t* eng_cnt_apply(const EngParams& e, const EItem& it, uint32_t rank) {
+  return e.a.counters + e.off_apply + (((it.s * e.K + it.k) * e.NB + it.n) * e.MT + it.m) * 2 + rank;
+}
+__device__ __forceinline__ uint32_t* eng_cnt_resid(const EngParams& e, int s, int64_t k, int n) {
+  return e.a.counters + e.off_resid + (s * e.K + k) * e.NB + n;
+}
+__device__ __forceinline__ uint32_t* eng_cnt_upd(const EngParams& e, int s, int64_t k, int n, int p) {
+  return e.a.counters + e.off_upd + ((s * e.K + k) * e.NB + n) * e.a.parts + p;
+}
+
+// Wait until *c >= target (acquire).  Past the soft limit the CTA aborts softly (error code 5);
+// past the hard limit the wait gives up and the item goes ahead on whatever is there.
+__device__ __forceinline__ void eng_wait_count(const uint32_t* c, uint32_t target, volatile int* abort,
+                                               uint64_t soft_ns) {
+  if (ld_acquire_u32(c) >= target) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_u32(c) < target) {
+    if (*abort == kAbortHard) return;
+    const uint64_t el = globaltimer_ns() - t0;
+    if (el > soft_ns && *abort == 0) {
+      atomicMax(const_cast<int*>(abort), kAbortSoft);
+      atomicCAS(&g_device_error, 0, 5);
+    }
+    if (el > kWaitLimitNs) {
+      atomicMax(const_cast<int*>(abort), kAbortHard);
+      atomicCAS(&g_device_error, 0, 5);
+      return;
+    }
+    __nanosleep(64);
+  }
+}
+
+// The 256 epilogue threads (both groups).
+__device__ __forceinline__ void eng_epi_all_barrier() {
+  __syncwarp();
+  asm volatile("bar.sync 3, 256;" ::: "memory");
+}
+
+// O_k and R_k of this CTA's 128 rows x 256 columns of an apply tile, from the finished fp32
+// sums, which are cleared for the next chunk.  Warp ew takes rows ew, ew + 8, ...; lane l
+// columns 8l .. 8l+7, so every row is one coalesced pass.
+__device__ __forceinline__ void eng_residual(const EngParams& e, const EItem& it, uint32_t rank, int ew, int lane) {
+  const EngineMse& a = e.a;
+  const int64_t row0 = it.m * 256 + rank * 128;           // in the chunk
+  const int64_t arow0 = it.s * a.B + row0;                  // acc and R rows
+  const int64_t trow0 = it.s * a.L + it.k * a.B + row0;     // O and V rows
+  const int64_t c0 = static_cast<int64_t>(it.n) * 256 + lane * 8;
+  const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(a.V);
+  __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.O);
+  __nv_bfloat16* R = static_cast<__nv_bfloat16*>(a.R);
+#pragma unroll 1
+  for (int i = ew; i < 128; i += 2 * kEngEpiWarps) {
+    uint32_t x[2][8];
+    uint4 v[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t ii = i + h * kEngEpiWarps;
+      ld_global_v8(a.acc + (arow0 + ii) * a.d + c0, x[h]);
+      v[h] = *reinterpret_cast<const uint4*>(V + (trow0 + ii) * a.d + c0);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t ii = i + h * kEngEpiWarps;
+      const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      st_global_v8(a.acc + (arow0 + ii) * a.d + c0, zero8);
+      const __nv_bfloat162* vh = reinterpret_cast<const __nv_bfloat162*>(&v[h]);
+      uint32_t o4[4], r4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float s0 = __uint_as_float(x[h][2 * q]), s1 = __uint_as_float(x[h][2 * q + 1]);
+        const float2 t = __bfloat1622float2(vh[q]);
+        o4[q] = pack_bf16x2(s0, s1);
+        r4[q] = pack_bf16x2(s0 - t.x, s1 - t.y);
+      }
+      *reinterpret_cast<uint4*>(O + (trow0 + ii) * a.d + c0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      *reinterpret_cast<uint4*>(R + (arow0 + ii) * a.d + c0) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kEngThreads, 1)
+    engine_mse_kernel(const __grid_constant__ CUtensorMap tmZk, const __grid_constant__ CUtensorMap tmZm,
+                      const __grid_constant__ CUtensorMap tmHi, const __grid_constant__ CUtensorMap tmR,
+                      const __grid_constant__ CUtensorMap tmAcc, const __grid_constant__ EngParams e) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_s + 1023u) & ~1023u) - raw_s);
+  uint8_t* stages = smem;
+  uint8_t* stg = smem + kEngStages * kEngStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + 2 * kEngStgBytes);
+  uint64_t* full_bar = bars;                          // [kEngStages]
+  uint64_t* empty_bar = bars + kEngStages;            // [kEngStages]
+  uint64_t* tfull_bar = bars + 2 * kEngStages;        // [2]
+  uint64_t* tempty_bar = bars + 2 * kEngStages + 2;   // [2]
+  uint64_t* drain_bar = bars + 2 * kEngStages + 4;    // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kEngStages + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+
+  const EngineMse& a = e.a;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool mma_cta = (rank == 0);
+  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < kEngStages; ++i) {
+        mbar_init(&full_bar[i], 1);
+        mbar_init(&empty_bar[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&tfull_bar[i], 1);
+        mbar_init(&tempty_bar[i], 2 * kEngEpiWarps);  // every epilogue warp of both CTAs
+      }
+      mbar_init(drain_bar, 1);
+      *abort_flag = 0;
+      *last_flag = 0;
+      fence_mbarrier_init();
+      tma_prefetch_desc(&tmZk);
+      tma_prefetch_desc(&tmZm);
+      tma_prefetch_desc(&tmHi);
+      tma_prefetch_desc(&tmR);
+      tma_prefetch_desc(&tmAcc);
+    }
+    __syncwarp();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t soft_ns = g_wait_soft_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kc = 0, pst = 0, pph = 0, issued_mask = 0;
+      bool ok = true;
+      const uint64_t pol_hi = l2_policy(a.keep_hi ? L2_EVICT_LAST : L2_NORMAL);
+      const uint64_t pol_n = l2_policy(L2_NORMAL);
+      ECursor cur;
+      for (cur.start(e, pair); ok && !cur.done(e); cur.advance(e, npairs)) {
+        const EItem it = eng_decode(e, cur);
+        // what the item reads must be written: the residual of its column block (update), or
+        // the previous chunk's update of its d_ff slice (apply)
+        if (it.upd) {
+          eng_wait_count(eng_cnt_resid(e, it.s, it.k, it.n), static_cast<uint32_t>(2 * e.MT), abort_flag, soft_ns);
+        } else if (it.k > 0) {
+          const int nt = eng_part_begin(it.p + 1, a.parts, e.RT) - eng_part_begin(it.p, a.parts, e.RT);
+          eng_wait_count(eng_cnt_upd(e, it.s, it.k - 1, it.n, it.p), static_cast<uint32_t>(2 * nt), abort_flag,
+                         soft_ns);
+        }
+        fence_proxy_async_global();
+        const int64_t col = static_cast<int64_t>(it.n) * 256 + rank * 128;  // this CTA's B columns
+        for (int kb = it.kb0; kb < it.kb1; ++kb, ++kc) {
+          const uint32_t st = pst, ph = pph;
+          if (++pst == kEngStages) {
+            pst = 0;
+            pph ^= 1;
+          }
+          if (!mbar_wait_bounded(&empty_bar[st], ph ^ 1, abort_flag, 1, &g_device_error, soft_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = stages + st * kEngStageBytes;
+          uint8_t* sb = sa + kEngHalf;
+          const uint32_t bar_cl = mapa_shared(smem_u32(&full_bar[st]), 0);
+          if (mma_cta) mbar_arrive_expect_tx(&full_bar[st], 2 * kEngStageBytes);
+          issued_mask |= 1u << st;
+          const int64_t k0 = static_cast<int64_t>(kb) * BK;
+          if (!it.upd) {
+            // A: rows of Z_k (this CTA's 128 of the 256-token tile), d_ff columns k0 ..
+            const int64_t zrow = it.s * a.L + it.k * a.B + it.m * 256 + rank * 128;
+            tma_load_2d_pair(sa, &tmZk, bar_cl, static_cast<int>(k0), static_cast<int>(zrow), pol_n);
+            // B: the hi plane, d_ff rows k0 .., this CTA's 128 columns of block n
+            const int c1 = static_cast<int>((k0 % kPlaneRows) / 16);
+            const int c2 = static_cast<int>((it.s * a.w.rb + k0 / kPlaneRows) * a.w.cb + col / kPlaneCols);
+            tma_load_3d_pair(sb, &tmHi, bar_cl, 0, c1, c2, pol_hi);
+          } else {
+            // A: Z_k^T, tokens k0 .. of the chunk, this CTA's 128 d_ff rows of tile r
+            const int64_t trow = it.s * a.L + it.k * a.B + k0;
+            const int64_t frow = static_cast<int64_t>(it.r) * 256 + rank * 128;
+            // B: R_k, the same tokens, this CTA's 128 columns of block n
+            const int64_t rrow = it.s * a.B + k0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              tma_load_2d_pair(sa + j * (64 * BK * 2), &tmZm, bar_cl, static_cast<int>(frow + 64 * j),
+                               static_cast<int>(trow), pol_n);
+              tma_load_2d_pair(sb + j * (64 * BK * 2), &tmR, bar_cl, static_cast<int>(col + 64 * j),
+                               static_cast<int>(rrow), pol_n);
+            }
+          }
+        }
+      }
+      // Teardown: every copy issued here has landed before shared memory is released.  The
+      // copies complete on the MMA CTA's barriers; its peer learns of them from its empty
+      // barriers (the MMAs that read them have finished).
+      for (uint32_t st = 0; st < kEngStages; ++st) {
+        if (!(issued_mask & (1u << st))) continue;
+        const uint32_t f = (kc - 1 - st) / kEngStages;  // last fill of stage st
+        if (!mma_cta)
+          mbar_wait_drain(&empty_bar[st], f & 1, 4, &g_device_error);
+        else
+          mbar_wait_drain(&full_bar[st], f & 1, 4, &g_device_error);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && mma_cta) {
+      constexpr uint32_t idesc_apply = make_idesc_bf16(2 * BM, 256, false, true);
+      constexpr uint32_t idesc_upd = make_idesc_bf16(2 * BM, 256, true, true);
+      const uint32_t s0 = smem_u32(stages);
+      const uint64_t a_apply = operand_desc<false>(s0, 0), b_apply = operand_desc<true, true>(s0 + kEngHalf, 0);
+      const uint64_t a_upd = operand_desc<true>(s0, 0), b_upd = operand_desc<true>(s0 + kEngHalf, 0);
+      uint32_t ls = 0, st = 0, ph = 0;
+      bool ok = true;
+      ECursor cur;
+      for (cur.start(e, pair); ok && !cur.done(e); cur.advance(e, npairs)) {
+        const EItem it = eng_decode(e, cur);
+        const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error, soft_ns)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kAccStride;
+        const uint64_t a0 = it.upd ? a_upd : a_apply, b0 = it.upd ? b_upd : b_apply;
+        const uint32_t idesc = it.upd ? idesc_upd : idesc_apply;
+        const uint32_t ak = it.upd ? (2048u >> 4) : (32u >> 4);   // a k step: 16 rows MN-major, 32 bytes K-major
+        const uint32_t bk = it.upd ? (2048u >> 4) : (512u >> 4);  // 16 rows MN-major, 512 bytes of plane rows
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[st], ph, abort_flag, 2, &g_device_error, soft_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!*abort_flag) {
+            const uint32_t soff = (st * kEngStageBytes) >> 4;
+            const uint32_t first = (kb == it.kb0) ? 0u : 1u;
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              umma_bf16_pair(d_tmem, a0 + soff + ks * ak, b0 + soff + ks * bk, idesc, ks ? 1u : first);
+          }
+          umma_commit_pair_both(&empty_bar[st]);
+          if (++st == kEngStages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_both(&tfull_bar[acc]);
+        ++ls;
+      }
+      umma_commit_pair_both(drain_bar);
+      mbar_wait_drain(drain_bar, 0, 4, &g_device_error);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;                // 0 .. 7
+    const int grp = ew / 4;                 // two groups of four warps
+    const int quarter = warp % 4;           // TMEM lanes 32*quarter .. +31
+    const int trow = quarter * 32 + lane;   // row of this CTA's 128 that this thread finishes
+    const bool issuer = (quarter == 0 && lane == 0);  // one per group: the TMA reductions
+    uint8_t* buf = stg + grp * kEngStgBytes;
+    const uint64_t pol_hi = l2_policy(a.keep_hi ? L2_EVICT_LAST : L2_NORMAL);
+    const uint64_t pol_lo = l2_policy(a.keep_hi ? L2_EVICT_FIRST : L2_NORMAL);
+    const int sw = (trow >> 2) & 1;  // this row's 16-byte halves trade places in a plane block
+    bool failed = false;
+    uint32_t ls = 0;
+    ECursor cur;
+    for (cur.start(e, pair); !cur.done(e); cur.advance(e, npairs)) {
+      const EItem it = eng_decode(e, cur);
+      const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
+      if (!failed)
+        failed = !__all_sync(0xffffffffu,
+                             mbar_wait_bounded(&tfull_bar[acc], aph, abort_flag, 3, &g_device_error, soft_ns));
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAccStride;
+      if (!it.upd) {
+        // ---- apply: this slice's partial sums of the tile, added into acc by TMA reductions
+        const int64_t orow = it.s * a.B + it.m * 256 + rank * 128;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const int c = grp + 2 * j;  // 32-column chunk of the tile
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, r);
+          tmem_wait_ld();
+          if (issuer) bulk_wait_group_read<0>();  // the buffer's last reduction has read it
+          epi_barrier(grp);
+          if (!failed) {
+            // 128-byte swizzle: 16-byte chunk q of row t sits at chunk q ^ (t % 8)
+            float4* srow = reinterpret_cast<float4*>(buf + trow * 128);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              srow[q ^ (trow & 7)] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          }
+          fence_proxy_async_shared();
+          epi_barrier(grp);
+          if (issuer && !failed && !*abort_flag) {
+            if (j == 0) fence_proxy_async_global();  // after the clearing of acc by the last residual
+            tma_reduce_add_2d(&tmAcc, buf, static_cast<int>(static_cast<int64_t>(it.n) * 256 + c * 32),
+                              static_cast<int>(orow));
+            bulk_commit_group();
+          }
+        }
+        // the accumulator has been read: hand it back to the MMA issuer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        // this slice's sums are in memory before it is counted
+        if (issuer) {
+          bulk_wait_group<0>();
+          fence_proxy_async_global();
+        }
+        eng_epi_all_barrier();
+        if (ew == 0 && lane == 0) {
+          fence_acq_rel_gpu();
+          const uint32_t old = atom_add_acq_rel_u32(eng_cnt_apply(e, it, rank), 1u);
+          *last_flag = (old + 1 == static_cast<uint32_t>(a.parts)) ? 1u : 0u;
+        }
+        eng_epi_all_barrier();
+        if (*last_flag) {
+          // the last slice of this half tile: every slice's sums are in acc
+          fence_acq_rel_gpu();
+          if (!failed && !*abort_flag) eng_residual(e, it, rank, ew, lane);
+          fence_proxy_async_global();  // R is read next by TMA copies
+          eng_epi_all_barrier();
+          if (ew == 0 && lane == 0) {
+            fence_acq_rel_gpu();
+            red_add_release_u32(eng_cnt_resid(e, it.s, it.k, it.n), 1u);
+          }
+        }
+      } else {
+        // ---- update: W = W + alpha * acc on this CTA's 128 plane rows of the tile.  The rows
+        // are one row of plane blocks; group g takes the 16-column chunks g, g + 2, ...; each
+        // thread reads and writes its row's 32 bytes of each plane, three chunks ahead.
+        constexpr int WC = kPlaneCols;
+        constexpr int GCH = 256 / WC / 2;  // chunks per group
+        const int64_t rbk = it.s * a.w.rb + static_cast<int64_t>(it.r) * 2 + rank;
+        const int64_t cb0 = static_cast<int64_t>(it.n) * (256 / WC);
+        const int64_t off = plane_index(rbk, cb0, a.w.cb, 0, 0) + trow * kPlaneCols;
+        uint16_t* const hi = a.w.hi + off;
+        uint16_t* const lo = a.w.lo + off;
+        uint32_t wh[4][8], wl[4][8];
+        auto wload = [&](int c, uint32_t (&h)[8], uint32_t (&l)[8]) {
+          ld_global_v8_hint(hi + static_cast<int64_t>(c) * kPlaneBlock, h, pol_hi);
+          ld_global_v8_hint(lo + static_cast<int64_t>(c) * kPlaneBlock, l, pol_lo);
+        };
+        wload(grp, wh[0], wl[0]);
+        wload(grp + 2, wh[1], wl[1]);
+        wload(grp + 4, wh[2], wl[2]);
+        uint32_t ra[WC], rb[WC];
+        tmem_ld_32x32b_x16(tbase + grp * WC, ra);
+#pragma unroll 1
+        for (int j4 = 0; j4 < GCH; j4 += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int jj = j4 + u, c = grp + 2 * jj;
+            uint32_t(&rr)[WC] = (u & 1) ? rb : ra;
+            uint32_t(&rn)[WC] = (u & 1) ? ra : rb;
+            tmem_wait_ld(rr);
+            if (jj + 1 < GCH) tmem_ld_32x32b_x16(tbase + (c + 2) * WC, rn);
+            // columns 2q, 2q+1 sit in stored word q ^ 4*sw
+            uint32_t hw[8], lw[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              hw[q] = sw ? wh[u][q + 4] : wh[u][q];
+              hw[q + 4] = sw ? wh[u][q] : wh[u][q + 4];
+              lw[q] = sw ? wl[u][q + 4] : wl[u][q];
+              lw[q + 4] = sw ? wl[u][q] : wl[u][q + 4];
+            }
+            if (jj + 3 < GCH) wload(c + 6, wh[(u + 3) & 3], wl[(u + 3) & 3]);
+            uint32_t ho[8], lo8[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float w0, w1;
+              join_w2(hw[q], lw[q], w0, w1);
+              split_w2(fmaf(a.alpha, __uint_as_float(rr[2 * q]), w0), fmaf(a.alpha, __uint_as_float(rr[2 * q + 1]), w1),
+                       ho[q], lo8[q]);
+            }
+            if (!failed && !*abort_flag) {
+              uint32_t hs[8], ls8[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                hs[q] = sw ? ho[q + 4] : ho[q];
+                hs[q + 4] = sw ? ho[q] : ho[q + 4];
+                ls8[q] = sw ? lo8[q + 4] : lo8[q];
+                ls8[q + 4] = sw ? lo8[q] : lo8[q + 4];
+              }
+              st_global_v8_hint(hi + static_cast<int64_t>(c) * kPlaneBlock, hs, pol_hi);
+              st_global_v8_hint(lo + static_cast<int64_t>(c) * kPlaneBlock, ls8, pol_lo);
+            }
+          }
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        // the new rows are read next by TMA copies (the next chunk's applies)
+        fence_proxy_async_global();
+        eng_epi_all_barrier();
+        if (ew == 0 && lane == 0) {
+          fence_acq_rel_gpu();
+          red_add_release_u32(eng_cnt_upd(e, it.s, it.k, it.n, eng_part_of(it.r, a.parts, e.RT)), 1u);
+        }
+      }
+      ++ls;
+    }
+    if (issuer) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  // Teardown: the roles that ran on one lane re-converge; with the pair, the cluster barrier
+  // keeps both CTAs until the last MMAs into either TMEM and the last arrivals on either
+  // CTA's barriers are done; then TMEM is freed.
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace tc
+
+bool engine_mse_supported(int64_t B, int64_t d, int64_t d_ff) {
+  return B > 0 && d > 0 && d_ff > 0 && B % 256 == 0 && d % 256 == 0 && d_ff % 256 == 0;
+}
+
+int64_t engine_counter_words(int64_t batch, int64_t L, int64_t B, int64_t d, int parts) {
+  const int64_t K = L / B, NB = d / 256, MT = B / 256;
+  return batch * K * NB * (2 * MT + 1 + parts);
+}
+
+cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
+  using namespace tc;
+  if (!engine_mse_supported(a.B, a.d, a.d_ff) || a.batch < 1 || a.L < a.B || a.L % a.B || a.parts < 1 ||
+      a.parts > a.d_ff / 256 || !a.counters || !a.w.hi || !a.w.lo)
+    return cudaErrorNotSupported;
+  static std::mutex mu;
+  static uint64_t attr_done = 0;
+  static int max_pairs[64] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (!(attr_done & (1ull << dev))) {
+      cudaError_t err = cudaFuncSetAttribute(engine_mse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kEngSmem);
+      if (err != cudaSuccess) return err;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+      cfg.blockDim = dim3(kEngThreads);
+      cfg.dynamicSmemBytes = kEngSmem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      err = cudaOccupancyMaxActiveClusters(&clusters, engine_mse_kernel, &cfg);
+      if (err != cudaSuccess) return err;
+      if (clusters <= 0) return cudaErrorInvalidConfiguration;
+      max_pairs[dev] = clusters;
+      attr_done |= 1ull << dev;
+    }
+  }
+  CUtensorMap mZk, mZm, mHi, mR, mAcc;
+  const int64_t T = a.batch * a.L, BR = a.batch * a.B;
+  if (!make_map(&mZk, a.Z, T, a.d_ff, a.d_ff, false, 64, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&mZm, a.Z, T, a.d_ff, a.d_ff, false, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_plane_map(&mHi, a.w, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&mR, a.R, BR, a.d, a.d, false, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&mAcc, a.acc, BR, a.d, a.d, true, 32, BM)) return cudaErrorInvalidValue;
+
+  EngParams e;
+  e.a = a;
+  e.K = a.L / a.B;
+  e.NB = a.d / 256;
+  e.MT = a.B / 256;
+  e.RT = a.d_ff / 256;
+  e.NAb = a.batch * e.MT * a.parts;
+  e.NUb = a.batch * e.RT;
+  e.slots = 2 * e.K;
+  const int64_t total = e.K * e.NB * (e.NAb + e.NUb);
+  e.off_apply = 0;
+  e.off_resid = a.batch * e.K * e.NB * e.MT * 2;
+  e.off_upd = e.off_resid + a.batch * e.K * e.NB;
+  const int64_t pairs = std::min<int64_t>(max_pairs[dev], total);
+
+  LaunchMark mark(K_ENGINE, stream);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // all CTAs resident at once: items wait on each other's counters
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(kEngThreads);
+  cfg.dynamicSmemBytes = kEngSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, engine_mse_kernel, mZk, mZm, mHi, mR, mAcc, e);
+  if (err == cudaErrorNotSupported || err == cudaErrorInvalidValue) {
+    // no cooperative launch of clusters here: the grid is sized to what is co-resident anyway
+    cudaGetLastError();
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, engine_mse_kernel, mZk, mZm, mHi, mR, mAcc, e);
+  }
+  return err;
+}
+
+}  // namespace ipttt

@@ -106,4 +106,24 @@ struct GemmProblem {
   int pf_count = 0;
 };
 
+// The MSE chunk loop of every sequence as one persistent kernel (engine_tc.cuh):
+//   for k: O_k = Z_k W_k; R_k = O_k - V_k; W_{k+1} = W_k + alpha Z_k^T R_k
+// split into work items per 256-column block n of W (the rule is independent across columns):
+// apply items (a 256-token tile of O_k[:, n], one of `parts` slices of d_ff), whose fp32 sums
+// meet in `acc` and the last of which forms O_k and R_k of that tile, and update items (256
+// rows x the 256 columns of W).  Items start as soon as what they read is written.
+struct EngineMse {
+  const void* Z = nullptr;       // [batch*L, d_ff] bf16, sequence s in rows s*L ..
+  const void* V = nullptr;       // [batch*L, d] bf16
+  void* O = nullptr;             // [batch*L, d] bf16 (out)
+  float* acc = nullptr;          // [batch*B, d] fp32 scratch, zero on entry and left zero
+  void* R = nullptr;             // [batch*B, d] bf16 scratch
+  uint32_t* counters = nullptr;  // engine_counter_words() words, zero on entry
+  Planes w;                      // the fast weights (entry = sequence), read and rewritten in place
+  int64_t batch = 0, L = 0, B = 0, d = 0, d_ff = 0;
+  int parts = 0;                 // slices of d_ff per apply tile
+  float alpha = 0.0f;            // -eta / B
+  int keep_hi = 0;               // keep the hi planes in L2 (evict last)
+};
+
 }  // namespace ipttt

@@ -45,6 +45,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "launch.h"
+#include "tmap.h"
 
 namespace ipttt {
 
@@ -749,11 +750,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-static EncodeTiledFn get_encode_fn() {
+EncodeTiledFn get_encode_fn() {
   static EncodeTiledFn fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -770,8 +768,8 @@ static EncodeTiledFn get_encode_fn() {
 // 2-D tensor map of a row-major matrix (rows x cols, row stride ld elements);
 // the box is box_cols x box_rows and its rows are box_cols * element size
 // bytes wide, swizzled with the matching pattern (32, 64 or 128 bytes).
-static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32,
-                     int box_cols, int box_rows) {
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool fp32, int box_cols,
+              int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc || !ptr || rows <= 0 || cols <= 0) return false;
   const int esz = fp32 ? 4 : 2;
@@ -798,7 +796,7 @@ static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
 // elements = 512 bytes, 8 rows of 512 bytes per block, blocks of all entries);
 // a box is BK/16 rows x box_cols/16 blocks, no swizzle (the planes are stored
 // swizzled).
-static bool make_plane_map(CUtensorMap* map, const Planes& w, int box_cols) {
+bool make_plane_map(CUtensorMap* map, const Planes& w, int box_cols) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc || !w.hi || w.rb <= 0 || w.cb <= 0 || w.entries <= 0) return false;
   constexpr int kRow = 256;  // elements per 512-byte row
@@ -949,3 +947,5 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
 }
 
 }  // namespace ipttt
+
+#include "engine_tc.cuh"

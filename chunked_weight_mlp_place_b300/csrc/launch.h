@@ -21,7 +21,8 @@ enum KernelKind : int {
   K_SCAN = 7,      // additive scan: exclusive prefix over groups
   K_WEIGHT = 8,    // fast-weight conversions (W_o0 -> split planes -> W_final, W_o0 -> W_final)
   K_SCORES = 9,    // additive rule, block-causal form: (eta/B) mask(Z Z^T)
-  K_COUNT = 10
+  K_ENGINE = 10,   // MSE rule: the whole chunk loop in one persistent kernel
+  K_COUNT = 11
 };
 
 // Every kernel launch of the library sits inside one LaunchMark: it counts the
@@ -72,6 +73,11 @@ cudaError_t read_clear_device_error(int* code);
 cudaError_t set_wait_soft_limit(uint64_t ns);
 
 cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream);    // bf16 operands, tcgen05
+// The persistent MSE chunk engine (gemm.h EngineMse).  Shapes it takes: B, d and d_ff multiples
+// of 256, parts in 1 .. d_ff / 256; cudaErrorNotSupported otherwise (nothing queued).
+bool engine_mse_supported(int64_t B, int64_t d, int64_t d_ff);
+int64_t engine_counter_words(int64_t batch, int64_t L, int64_t B, int64_t d, int parts);
+cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream);
 cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream);  // fp32 operands, CUDA cores
 
 // C = chunk-padded depthwise conv of E (width 4, taps t..t+3), rows = batch*L.
