@@ -41,6 +41,7 @@ KERNEL_SOURCES = {  # source files whose change invalidates a stored ncu traffic
     "proj": ["gemm_tc.cu", "common.cuh", "gemm.h"],
     "apply": ["gemm_tc.cu", "common.cuh", "gemm.h"],
     "update": ["gemm_tc.cu", "common.cuh", "gemm.h"],
+    "engine": ["gemm_tc.cu", "engine_tc.cuh", "common.cuh", "gemm.h"],
     "residual": ["elementwise.cu", "common.cuh"],
     "conv": ["elementwise.cu", "common.cuh"],
 }
@@ -125,6 +126,8 @@ def _kernel_work_one(w, name, cu=None):
         return 2.0 * w.d * w.d_ff * T / steps, 0.0
     if name == "update":
         return 2.0 * w.d * w.d_ff * T / steps, w_bytes / steps
+    if name == "engine":  # the whole chunk loop (apply and update of every chunk) in one launch
+        return 4.0 * w.d * w.d_ff * T, w_bytes
     if name == "conv":
         return 0.0, 2.0 * T * w.d * 2
     if name == "residual":

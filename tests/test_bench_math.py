@@ -23,6 +23,11 @@ def test_per_launch_work_adds_up_to_the_layer():
     # 4 d d_ff (gate+up) + 2 d d_ff (apply) + 2 d d_ff (update) + 2 d^2 (proj) per token
     assert total == pytest.approx((8 * w.d * w.d_ff + 2 * w.d * w.d) * T, rel=1e-12)
     assert bench.kernel_work(w, "update")[1] * K == pytest.approx(K * 2 * w.d_ff * w.d * 4, rel=1e-12)
+    # the persistent engine: the apply and update of every chunk in its one launch
+    launches = {"gate_up": 1, "proj": 1, "engine": 1}
+    total = sum(bench.kernel_work(w, k)[0] * n for k, n in launches.items())
+    assert total == pytest.approx((8 * w.d * w.d_ff + 2 * w.d * w.d) * T, rel=1e-12)
+    assert bench.kernel_work(w, "engine")[1] == pytest.approx(K * 2 * w.d_ff * w.d * 4, rel=1e-12)
 
 
 def test_layer_roofline_at_the_4b_workload():
