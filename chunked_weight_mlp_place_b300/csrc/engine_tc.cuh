@@ -56,7 +56,10 @@ struct EngParams {
   int64_t K, NB, MT, RT;    // chunks; column blocks, token tiles and d_ff tiles of 256
   int64_t NAb, NUb;         // items of one column block's apply phase and update phase
   int64_t slots;            // phase slots of the order: 2K
-  int64_t off_apply, off_resid, off_upd;  // counter regions (words)
+  // counter regions (words): apply slices done per (sequence, chunk, block, token tile, half);
+  // residual halves done per (sequence, chunk, block, token tile); update tiles done per
+  // (sequence, chunk, block, d_ff slice)
+  int64_t off_apply, off_resid, off_upd;
 };
 
 struct EItem {
@@ -139,8 +142,8 @@ __device__ __forceinline__ EItem eng_decode(const EngParams& e, const ECursor& c
 __device__ __forceinline__ uint32_t* eng_cnt_apply(const EngParams& e, const EItem& it, uint32_t rank) {
   return e.a.counters + e.off_apply + (((it.s * e.K + it.k) * e.NB + it.n) * e.MT + it.m) * 2 + rank;
 }
-__device__ __forceinline__ uint32_t* eng_cnt_resid(const EngParams& e, int s, int64_t k, int n) {
-  return e.a.counters + e.off_resid + (s * e.K + k) * e.NB + n;
+__device__ __forceinline__ uint32_t* eng_cnt_resid(const EngParams& e, int s, int64_t k, int n, int m) {
+  return e.a.counters + e.off_resid + ((s * e.K + k) * e.NB + n) * e.MT + m;
 }
 __device__ __forceinline__ uint32_t* eng_cnt_upd(const EngParams& e, int s, int64_t k, int n, int p) {
   return e.a.counters + e.off_upd + ((s * e.K + k) * e.NB + n) * e.a.parts + p;
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
         // what the item reads must be written: the residual of its column block (update), or
         // the previous chunk's update of its d_ff slice (apply)
         if (it.upd) {
-          eng_wait_count(eng_cnt_resid(e, it.s, it.k, it.n), static_cast<uint32_t>(2 * e.MT), abort_flag, soft_ns);
+          // (token tile by token tile, in the k loop below)
         } else if (it.k > 0) {
           const int nt = eng_part_begin(it.p + 1, a.parts, e.RT) - eng_part_begin(it.p, a.parts, e.RT);
           eng_wait_count(eng_cnt_upd(e, it.s, it.k - 1, it.n, it.p), static_cast<uint32_t>(2 * nt), abort_flag,
@@ -294,6 +297,12 @@ __global__ void __launch_bounds__(kEngThreads, 1)
         fence_proxy_async_global();
         const int64_t col = static_cast<int64_t>(it.n) * 256 + rank * 128;  // this CTA's B columns
         for (int kb = it.kb0; kb < it.kb1; ++kb, ++kc) {
+          if (it.upd && kb % 4 == 0) {
+            // an update contracts over the chunk's tokens: those of token tile kb / 4 are ready
+            // once both halves of that tile's residual are written
+            eng_wait_count(eng_cnt_resid(e, it.s, it.k, it.n, kb / 4), 2u, abort_flag, soft_ns);
+            fence_proxy_async_global();
+          }
           const uint32_t st = pst, ph = pph;
           if (++pst == kEngStages) {
             pst = 0;
@@ -330,6 +339,22 @@ __global__ void __launch_bounds__(kEngThreads, 1)
               tma_load_2d_pair(sb + j * (64 * BK * 2), &tmR, bar_cl, static_cast<int>(col + 64 * j),
                                static_cast<int>(rrow), pol_n);
             }
+          }
+        }
+        // An update item of chunk k brings its share of Z_{k+1} (the next applies' A operand)
+        // into L2: the chunk's update items split those rows of every sequence evenly.
+        if (ok && it.upd && it.k + 1 < e.K && rank == 0) {
+          const int64_t seg = a.B * a.d_ff * 2;  // bytes of one sequence's chunk of Z
+          const int64_t total = a.batch * seg, nu = e.NB * e.NUb;
+          const int64_t u = (static_cast<int64_t>(it.n) * a.batch + it.s) * e.RT + it.r;
+          int64_t off = (total * u / nu) & ~int64_t{255};
+          const int64_t end = (u + 1 == nu) ? total : ((total * (u + 1) / nu) & ~int64_t{255});
+          while (off < end) {
+            const int64_t sq = off / seg, in = off - sq * seg;
+            const int64_t n = min(min(end - off, seg - in), int64_t{65536});
+            prefetch_l2_bulk(static_cast<const uint8_t*>(a.Z) + ((sq * a.L + (it.k + 1) * a.B) * a.d_ff) * 2 + in,
+                             static_cast<uint32_t>(n));
+            off += n;
           }
         }
       }
@@ -403,11 +428,29 @@ __global__ void __launch_bounds__(kEngThreads, 1)
     const uint64_t pol_hi = l2_policy(a.keep_hi ? L2_EVICT_LAST : L2_NORMAL);
     const uint64_t pol_lo = l2_policy(a.keep_hi ? L2_EVICT_FIRST : L2_NORMAL);
     const int sw = (trow >> 2) & 1;  // this row's 16-byte halves trade places in a plane block
+    // This thread's row of an update item's plane blocks (the CTA's 128 rows of the tile).
+    auto plane_row = [&](const EItem& x, uint16_t* base) {
+      const int64_t rbk = x.s * a.w.rb + static_cast<int64_t>(x.r) * 2 + rank;
+      return base + plane_index(rbk, static_cast<int64_t>(x.n) * (256 / kPlaneCols), a.w.cb, 0, 0) + trow * kPlaneCols;
+    };
+    uint32_t wh[4][8], wl[4][8];  // plane rows of the chunks in flight, by chunk % 4
+    bool pre = false;             // the first three chunks of this update item are already loaded
     bool failed = false;
     uint32_t ls = 0;
     ECursor cur;
     for (cur.start(e, pair); !cur.done(e); cur.advance(e, npairs)) {
       const EItem it = eng_decode(e, cur);
+      // The next item's planes may be loaded during this one only once what writes them has
+      // finished: a complete residual of the first token tile of its column block means every
+      // apply of that tile is done, and those waited for the previous chunk's updates of all
+      // the block's rows.
+      ECursor nx = cur;
+      nx.advance(e, npairs);
+      bool nx_upd = false;
+      if (it.upd && !nx.done(e)) {
+        const EItem nit = eng_decode(e, nx);
+        nx_upd = nit.upd && ld_acquire_u32(eng_cnt_resid(e, nit.s, nit.k, nit.n, 0)) >= 2u;
+      }
       const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
       if (!failed)
         failed = !__all_sync(0xffffffffu,
@@ -466,7 +509,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
           eng_epi_all_barrier();
           if (ew == 0 && lane == 0) {
             fence_acq_rel_gpu();
-            red_add_release_u32(eng_cnt_resid(e, it.s, it.k, it.n), 1u);
+            red_add_release_u32(eng_cnt_resid(e, it.s, it.k, it.n, it.m), 1u);
           }
         }
       } else {
@@ -475,19 +518,26 @@ __global__ void __launch_bounds__(kEngThreads, 1)
         // thread reads and writes its row's 32 bytes of each plane, three chunks ahead.
         constexpr int WC = kPlaneCols;
         constexpr int GCH = 256 / WC / 2;  // chunks per group
-        const int64_t rbk = it.s * a.w.rb + static_cast<int64_t>(it.r) * 2 + rank;
-        const int64_t cb0 = static_cast<int64_t>(it.n) * (256 / WC);
-        const int64_t off = plane_index(rbk, cb0, a.w.cb, 0, 0) + trow * kPlaneCols;
-        uint16_t* const hi = a.w.hi + off;
-        uint16_t* const lo = a.w.lo + off;
-        uint32_t wh[4][8], wl[4][8];
-        auto wload = [&](int c, uint32_t (&h)[8], uint32_t (&l)[8]) {
-          ld_global_v8_hint(hi + static_cast<int64_t>(c) * kPlaneBlock, h, pol_hi);
-          ld_global_v8_hint(lo + static_cast<int64_t>(c) * kPlaneBlock, l, pol_lo);
+        static_assert(GCH % 4 == 0, "a group's chunks come in fours");
+        uint16_t* const hi = plane_row(it, a.w.hi);
+        uint16_t* const lo = plane_row(it, a.w.lo);
+        auto wload = [&](uint16_t* h0, uint16_t* l0, int c, uint32_t (&h)[8], uint32_t (&l)[8]) {
+          ld_global_v8_hint(h0 + static_cast<int64_t>(c) * kPlaneBlock, h, pol_hi);
+          ld_global_v8_hint(l0 + static_cast<int64_t>(c) * kPlaneBlock, l, pol_lo);
         };
-        wload(grp, wh[0], wl[0]);
-        wload(grp + 2, wh[1], wl[1]);
-        wload(grp + 4, wh[2], wl[2]);
+        if (!pre) {
+          wload(hi, lo, grp, wh[0], wl[0]);
+          wload(hi, lo, grp + 2, wh[1], wl[1]);
+          wload(hi, lo, grp + 4, wh[2], wl[2]);
+        }
+        // the next update item's rows (its first three chunks are loaded during this one's last)
+        uint16_t* nhi = hi;
+        uint16_t* nlo = lo;
+        if (nx_upd) {
+          const EItem nit = eng_decode(e, nx);
+          nhi = plane_row(nit, a.w.hi);
+          nlo = plane_row(nit, a.w.lo);
+        }
         uint32_t ra[WC], rb[WC];
         tmem_ld_32x32b_x16(tbase + grp * WC, ra);
 #pragma unroll 1
@@ -508,7 +558,10 @@ __global__ void __launch_bounds__(kEngThreads, 1)
               lw[q] = sw ? wl[u][q + 4] : wl[u][q];
               lw[q + 4] = sw ? wl[u][q] : wl[u][q + 4];
             }
-            if (jj + 3 < GCH) wload(c + 6, wh[(u + 3) & 3], wl[(u + 3) & 3]);
+            if (jj + 3 < GCH)
+              wload(hi, lo, c + 6, wh[(u + 3) & 3], wl[(u + 3) & 3]);
+            else if (nx_upd)
+              wload(nhi, nlo, grp + 2 * (jj + 3 - GCH), wh[(u + 3) & 3], wl[(u + 3) & 3]);
             uint32_t ho[8], lo8[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -543,6 +596,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
           red_add_release_u32(eng_cnt_upd(e, it.s, it.k, it.n, eng_part_of(it.r, a.parts, e.RT)), 1u);
         }
       }
+      pre = it.upd && nx_upd;
       ++ls;
     }
     if (issuer) bulk_wait_group<0>();
@@ -569,7 +623,7 @@ bool engine_mse_supported(int64_t B, int64_t d, int64_t d_ff) {
 
 int64_t engine_counter_words(int64_t batch, int64_t L, int64_t B, int64_t d, int parts) {
   const int64_t K = L / B, NB = d / 256, MT = B / 256;
-  return batch * K * NB * (2 * MT + 1 + parts);
+  return batch * K * NB * (3 * MT + parts);
 }
 
 cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
@@ -626,7 +680,7 @@ cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
   const int64_t total = e.K * e.NB * (e.NAb + e.NUb);
   e.off_apply = 0;
   e.off_resid = a.batch * e.K * e.NB * e.MT * 2;
-  e.off_upd = e.off_resid + a.batch * e.K * e.NB;
+  e.off_upd = e.off_resid + a.batch * e.K * e.NB * e.MT;
   const int64_t pairs = std::min<int64_t>(max_pairs[dev], total);
 
   LaunchMark mark(K_ENGINE, stream);

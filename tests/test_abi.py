@@ -167,9 +167,9 @@ def test_workspace_size_is_host_only(L):
     T = 131072
     act = T * 9728 * 2 + 2 * T * 2560 * 2
     # fp32 partial sums and bf16 residual of one chunk, the fast weight's split hi/lo planes, and
-    # the persistent engine's counters: per chunk and 256-column block, two per 256-token tile,
-    # one for the residual and one per d_ff slice (4)
-    eng = 1024 * 2560 * 4 + 1024 * 2560 * 2 + 2 * 9728 * 2560 * 2 + 128 * 10 * (2 * 4 + 1 + 4) * 4
+    # the persistent engine's counters: per chunk and 256-column block, three per 256-token tile
+    # (two halves' applies, the residual) and one per d_ff slice (4)
+    eng = 1024 * 2560 * 4 + 1024 * 2560 * 2 + 2 * 9728 * 2560 * 2 + 128 * 10 * (3 * 4 + 4) * 4
     assert act + eng <= out.value <= act + eng + 4096
     assert L.ipttt_workspace_size(ctypes.byref(dm), 131072, 1024, 0, 0, ctypes.byref(out)) == _lib.OK
     assert eng <= out.value <= eng + 4096
