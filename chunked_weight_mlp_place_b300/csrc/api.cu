@@ -331,6 +331,10 @@ ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, 
   p.B2 = mat(W_u, dm->d, dm->d_ff, 1);
   p.epi = EPI_GATE;
   p.kind = K_GATE;
+  // W_g | W_u (2 d d_ff bf16) is read again by every group of row tiles: keep it in L2 while the
+  // Z tiles (written once, read much later) go first
+  p.l2_b = L2_EVICT_LAST;
+  p.l2_d = L2_EVICT_FIRST;
   p.out_bf16 = bf16;
   p.D = out(Z, dm->d_ff);
   IPTTT_CUDA(gemm(p, bf16, st));

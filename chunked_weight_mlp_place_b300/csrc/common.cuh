@@ -88,6 +88,11 @@ __device__ __forceinline__ void st_global_v8_hint(void* g, const uint32_t (&v)[8
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "l"(pol)
                : "memory");
 }
+__device__ __forceinline__ void st_global_v4_hint(void* g, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(g), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
 // Bring `bytes` of global memory at `g` into L2 (both 16-byte aligned); nothing waits for it.
 __device__ __forceinline__ void prefetch_l2_bulk(const void* g, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");

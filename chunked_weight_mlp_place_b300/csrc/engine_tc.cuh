@@ -25,8 +25,8 @@
 // order that mixes the phases of different blocks was measured slower: it
 // spreads the working set over two chunks' activations.)
 // Every dependency points to an earlier item, and a pair finishes an item
-// without waiting for later ones, so the order cannot deadlock; the grid is
-// launched co-resident.
+// without waiting for later ones, so the order cannot deadlock once every CTA
+// is resident (the grid is what fits on the device at once).
 //
 // Roles as in the GEMM template (gemm_tc.cu): warp 0 the TMA producer (it also
 // waits for an item's inputs), warp 1 the MMA issuer (cta_group::2, 256 x 256
@@ -149,8 +149,15 @@ __device__ __forceinline__ uint32_t* eng_cnt_upd(const EngParams& e, int s, int6
   return e.a.counters + e.off_upd + ((s * e.K + k) * e.NB + n) * e.a.parts + p;
 }
 
+// A wait for another CTA's counter gives up after half the hard limit of the pipeline waits: the
+// MMA issuer and the epilogue of this pair, waiting behind it on their mbarriers, then see their
+// data arrive before their own limit, so the pair never takes the hard exit with copies in flight.
+constexpr uint64_t kEngDepLimitNs = kWaitLimitNs / 2;
+
 // Wait until *c >= target (acquire).  Past the soft limit the CTA aborts softly (error code 5);
-// past the hard limit the wait gives up and the item goes ahead on whatever is there.
+// past kEngDepLimitNs the wait gives up and the item goes ahead on whatever is there, the CTA
+// still only softly aborted (no more MMAs or writes, every handshake kept), so that no role of it
+// stops waiting for copies or MMAs already in flight.
 __device__ __forceinline__ void eng_wait_count(const uint32_t* c, uint32_t target, volatile int* abort,
                                                uint64_t soft_ns) {
   if (ld_acquire_u32(c) >= target) return;
@@ -162,8 +169,8 @@ __device__ __forceinline__ void eng_wait_count(const uint32_t* c, uint32_t targe
       atomicMax(const_cast<int*>(abort), kAbortSoft);
       atomicCAS(&g_device_error, 0, 5);
     }
-    if (el > kWaitLimitNs) {
-      atomicMax(const_cast<int*>(abort), kAbortHard);
+    if (el > kEngDepLimitNs) {
+      atomicMax(const_cast<int*>(abort), kAbortSoft);
       atomicCAS(&g_device_error, 0, 5);
       return;
     }
@@ -684,28 +691,23 @@ cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
   const int64_t pairs = std::min<int64_t>(max_pairs[dev], total);
 
   LaunchMark mark(K_ENGINE, stream);
+  // Every CTA must be resident at once (items wait on each other's counters): the grid is the
+  // number of clusters that fit on the device together.  A plain launch of that grid puts them
+  // all on an idle GPU; should other work hold SMs, the late CTAs start as it leaves, and a
+  // counter wait that outlasts its limit ends the call with IPTTT_ERR_TIMEOUT, not a hang.
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // all CTAs resident at once: items wait on each other's counters
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
   cfg.blockDim = dim3(kEngThreads);
   cfg.dynamicSmemBytes = kEngSmem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, engine_mse_kernel, mZk, mZm, mHi, mR, mAcc, e);
-  if (err == cudaErrorNotSupported || err == cudaErrorInvalidValue) {
-    // no cooperative launch of clusters here: the grid is sized to what is co-resident anyway
-    cudaGetLastError();
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, engine_mse_kernel, mZk, mZm, mHi, mR, mAcc, e);
-  }
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, engine_mse_kernel, mZk, mZm, mHi, mR, mAcc, e);
   return err;
 }
 

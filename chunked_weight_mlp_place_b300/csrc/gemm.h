@@ -98,6 +98,7 @@ struct GemmProblem {
   // kept (evict last) and the lo plane's given up first -- the hi plane is read again by
   // the next apply, the lo plane only by the next update.
   int l2_a = 0, l2_b = 0, planes_l2 = 0;
+  int l2_d = 0;  // STORE / GATE epilogues: L2 eviction priority of the output's bf16 stores
   // Tensor-core path: once a CTA has issued all its operand copies it asks L2 to fetch
   // its share of pf_count ranges of pf_bytes bytes, pf_stride bytes apart, from pf_ptr
   // (the next kernel's operand; 16-byte aligned).  No result depends on it.

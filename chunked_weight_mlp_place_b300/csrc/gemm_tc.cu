@@ -259,7 +259,7 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
 // group sums, and the rows of a split-mode tile that a TMA box cannot cover).
 template <int EPI, bool OUT_BF16>
 __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
-                                               const uint32_t (&r)[32], const uint32_t (&u)[32]) {
+                                               const uint32_t (&r)[32], const uint32_t (&u)[32], uint64_t pol_d) {
   const bool full = (n + 32 <= p.N);
   if constexpr (EPI == EPI_STORE || EPI == EPI_GATE) {
     float v[32];
@@ -284,7 +284,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
       __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D.ptr) + row * p.D.ld + n;
       if (full) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(d)[q] = pack8_bf16(v + 8 * q);
+        for (int q = 0; q < 4; ++q) st_global_v4_hint(reinterpret_cast<uint4*>(d) + q, pack8_bf16(v + 8 * q), pol_d);
       } else {
         for (int i = 0; i < 32 && n + i < p.N; ++i) d[i] = __float2bfloat16_rn(v[i]);
       }
@@ -663,6 +663,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       }
     } else {
       uint32_t sc = 0;
+      const uint64_t pol_d = l2_policy(p.l2_d);  // the output's lines
       while (iter.next<EPI == EPI_STORE>(seg)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
@@ -708,7 +709,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
               continue;
             }
           }
-          if (m < p.M && !failed && !*abort_flag) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u);
+          if (m < p.M && !failed && !*abort_flag) epilogue_chunk<EPI, OUT_BF16>(p, b1, b2, m, n, r, u, pol_d);
         }
         // Hand the accumulator back to the MMA issuer (the even CTA's, with pairs).
         tc_fence_before();
