@@ -331,9 +331,12 @@ ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, 
   p.B2 = mat(W_u, dm->d, dm->d_ff, 1);
   p.epi = EPI_GATE;
   p.kind = K_GATE;
-  // W_g | W_u (2 d d_ff bf16) is read again by every group of row tiles: keep it in L2 while the
-  // Z tiles (written once, read much later) go first
-  p.l2_b = L2_EVICT_LAST;
+  // Tiles in dynamic order (pairs take the next tile as they free up), in bands of columns whose
+  // W_g | W_u tiles (4 d bytes a column of Z) take about 34 MB: the band stays in L2 while every
+  // row tile of X streams past it, so X is read once per band and W_g | W_u about once.  The
+  // Z tiles (written once, read much later) leave L2 first.
+  p.dyn_tiles = 1;
+  p.band_n = static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * dm->d * 128)));
   p.l2_d = L2_EVICT_FIRST;
   p.out_bf16 = bf16;
   p.D = out(Z, dm->d_ff);

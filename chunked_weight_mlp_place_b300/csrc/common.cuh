@@ -103,15 +103,27 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* g, uint32_t bytes) 
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// CLUSTER: acquire at cluster scope, for phases completed by arrivals of the peer CTA
+// (mbar_arrive_cluster) whose earlier shared-memory writes the waiter then reads.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if constexpr (CLUSTER)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 
@@ -126,12 +138,13 @@ constexpr int kAbortSoft = 1, kAbortHard = 2;
 // `soft_ns` it raises the abort word to kAbortSoft and records `code` in
 // `*err_word` (if that still holds 0), and keeps waiting; past kWaitLimitNs, or
 // once another role has given up (kAbortHard), it returns false.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort, int code,
                                                   int* err_word, uint64_t soft_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const int a = *abort;
     if (a == kAbortHard) return false;
     const uint64_t el = globaltimer_ns() - t0;
@@ -357,6 +370,10 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cl) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
+}
+// 64-bit store into the shared memory of a CTA of the cluster (cluster address `addr`).
+__device__ __forceinline__ void st_shared_cluster_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 // TMEM allocation shared by the pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {

@@ -99,6 +99,14 @@ struct GemmProblem {
   // the next apply, the lo plane only by the next update.
   int l2_a = 0, l2_b = 0, planes_l2 = 0;
   int l2_d = 0;  // STORE / GATE epilogues: L2 eviction priority of the output's bf16 stores
+  // Tensor-core path, tile order (no split): 0 = groups of 16 row tiles, each swept over all
+  // column tiles (B re-read once per group); band_n > 0 = bands of band_n column tiles, each
+  // swept over all row tiles (A re-read once per band, the band of B held in L2).
+  int band_n = 0;
+  // Tensor-core path, whole tiles with a STORE (no mask) or GATE epilogue: 1 = tiles taken in
+  // increasing order from a device-wide counter as CTA pairs free up, instead of a fixed
+  // share per pair.  The counter is one per device: launches that use it must be ordered.
+  int dyn_tiles = 0;
   // Tensor-core path: once a CTA has issued all its operand copies it asks L2 to fetch
   // its share of pf_count ranges of pf_bytes bytes, pf_stride bytes apart, from pf_ptr
   // (the next kernel's operand; 16-byte aligned).  No result depends on it.

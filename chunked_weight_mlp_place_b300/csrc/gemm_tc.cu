@@ -58,6 +58,9 @@ __device__ int g_device_error = 0;
 // mbar_wait_bounded).  Set from the host (ipttt_set_wait_limit); by default it equals the
 // hard limit, so only a wait that hangs trips it.
 __device__ unsigned long long g_wait_soft_ns = kWaitLimitNs;
+// Next tile of a tensor-core GEMM launched in dynamic tile order (GemmProblem::dyn_tiles);
+// zeroed on the stream before each such launch.
+__device__ unsigned long long g_tile_ticket = 0;
 
 namespace tc {
 
@@ -105,6 +108,7 @@ struct Sched {
   int64_t n_mt, n_nt, tiles_per_batch, total_tiles;
   int kb_total;
   int group_m;
+  int band_n;  // > 0: column-band order (GemmProblem::band_n)
   int split;
   int pair;
   int64_t total_iters;
@@ -116,6 +120,15 @@ struct Sched {
   __device__ void tile_coords(int64_t t, int& bi, int64_t& mt, int64_t& nt) const {
     bi = static_cast<int>(t / tiles_per_batch);
     const int64_t r = t % tiles_per_batch;
+    if (band_n) {
+      const int64_t bsz = static_cast<int64_t>(band_n) * n_mt;
+      const int64_t first_n = (r / bsz) * band_n;
+      const int64_t gn = min(static_cast<int64_t>(band_n), n_nt - first_n);
+      const int64_t q = r % bsz;
+      mt = q / gn;
+      nt = first_n + q % gn;
+      return;
+    }
     const int64_t gsz = static_cast<int64_t>(group_m) * n_nt;
     const int64_t g = r / gsz;
     const int64_t first_m = g * group_m;
@@ -174,9 +187,92 @@ struct SegIter {
   }
 };
 
+// Dynamic tile order (GemmProblem::dyn_tiles).  With the static order each CTA (pair) w
+// takes tiles w, w + G, w + 2G, ...; over a long launch some pairs run ahead of others and
+// the tiles in flight spread over more rows and columns than L2 holds.  Here one thread of
+// the pair (the even CTA's producer) takes tile numbers from a global counter in increasing
+// order, so the tiles in flight stay a window of consecutive ones, and publishes each number
+// in a ring of kRing slots in the shared memory of both CTAs.  Every other role of both CTAs
+// reads the same sequence from its own CTA's ring and releases each slot on the even CTA's
+// barrier; a slot holding -1 ends the sequence.
+constexpr int kRing = 8;
+
 struct KParams {
   GemmProblem p;
   Sched s;
+  unsigned long long* ticket;  // dynamic order: the tile counter (zero at launch)
+};
+
+// The tiles a role walks, in the static order (SegIter) or from the ring.
+template <bool PAIR>
+struct TileSrc {
+  SegIter it;
+  int64_t* ids;        // this CTA's ring (nullptr: static order)
+  uint64_t* full;      // this CTA's ring barriers: one arrival per fill
+  uint64_t* empty;     // the ring's release barriers (the even CTA's are the ones counted)
+  uint32_t j;          // fills consumed
+  int kb_total;
+
+  __device__ void init(const KParams& kp, int64_t* ring_ids, uint64_t* ring_full, uint64_t* ring_empty) {
+    it.init(&kp.s);
+    ids = kp.p.dyn_tiles ? ring_ids : nullptr;
+    full = ring_full;
+    empty = ring_empty;
+    j = 0;
+    kb_total = kp.s.kb_total;
+  }
+  // Consumer: the next tile.  Called by the lanes in `wmask` of one warp together (lane 0
+  // among them); the warp gives up together if any lane's wait did.
+  template <bool MASK>
+  __device__ bool next(Seg& g, uint32_t wmask, volatile int* abort, int code, uint64_t soft_ns) {
+    if (ids == nullptr) return it.template next<MASK>(g);
+    const uint32_t sl = j % kRing, ph = (j / kRing) & 1;
+    ++j;
+    if (!__all_sync(wmask, mbar_wait_bounded<PAIR>(&full[sl], ph, abort, code, &g_device_error, soft_ns)))
+      return false;
+    const int64_t t = *reinterpret_cast<volatile int64_t*>(&ids[sl]);
+    __syncwarp(wmask);
+    if ((threadIdx.x & 31) == 0) {
+      if constexpr (PAIR)
+        mbar_arrive_cluster(mapa_shared(smem_u32(&empty[sl]), 0));
+      else
+        mbar_arrive(&empty[sl]);
+    }
+    if (t < 0) return false;
+    g.tile = t;
+    g.kb0 = 0;
+    g.kb1 = kb_total;
+    return true;
+  }
+  // The even CTA's producer: its next tile.  Tile numbers are published one position ahead
+  // of the producer's own walk, so the peer's producer knows its next tile while this one
+  // still issues the current tile's copies.
+  __device__ bool publish(uint32_t pos, unsigned long long* ticket, int64_t total, volatile int* abort,
+                          uint64_t soft_ns) {
+    const uint32_t sl = pos % kRing, ph = (pos / kRing) & 1;
+    // every consumer of both CTAs has read the slot's previous number
+    if (!mbar_wait_bounded<PAIR>(&empty[sl], ph ^ 1, abort, 1, &g_device_error, soft_ns)) return false;
+    int64_t t = static_cast<int64_t>(atomicAdd(ticket, 1ull));
+    if (t >= total) t = -1;
+    ids[sl] = t;
+    mbar_arrive(&full[sl]);
+    if constexpr (PAIR) {
+      st_shared_cluster_u64(mapa_shared(smem_u32(&ids[sl]), 1), static_cast<uint64_t>(t));
+      mbar_arrive_cluster(mapa_shared(smem_u32(&full[sl]), 1));  // release: the store above first
+    }
+    return true;
+  }
+  __device__ bool fetch(Seg& g, unsigned long long* ticket, int64_t total, volatile int* abort, uint64_t soft_ns) {
+    if (j == 0 && !publish(0, ticket, total, abort, soft_ns)) return false;
+    const int64_t t = ids[j % kRing];  // published by this thread
+    if (t >= 0 && !publish(j + 1, ticket, total, abort, soft_ns)) return false;
+    ++j;
+    if (t < 0) return false;
+    g.tile = t;
+    g.kb0 = 0;
+    g.kb1 = kb_total;
+    return true;
+  }
 };
 
 // Named barrier of a group of four epilogue warps (128 threads; group g uses
@@ -333,6 +429,10 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
   uint64_t* drain_bar = bars + 2 * C::STAGES + 4;   // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* ring_full = bars + 2 * C::STAGES + 6;  // [kRing] dynamic tile order
+  uint64_t* ring_empty = ring_full + kRing;        // [kRing]
+  int64_t* ring_ids = reinterpret_cast<int64_t*>(ring_empty + kRing);
+  static_assert((2 * C::STAGES + 6 + 3 * kRing) * 8 <= C::BAR_BYTES, "barrier area");
 
   const GemmProblem& p = kp.p;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -352,6 +452,12 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         mbar_init(&tempty_bar[i], (PAIR ? 2 : 1) * C::EPI_WARPS);  // one arrival per epilogue warp (of both CTAs)
       }
       mbar_init(drain_bar, 1);
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&ring_full[i], 1);
+        // consumers of a fill: the MMA issuer and the epilogue warps of the even CTA, and
+        // with pairs the producer and epilogue warps of the odd one
+        mbar_init(&ring_empty[i], PAIR ? 2 + 2 * C::EPI_WARPS : 1 + C::EPI_WARPS);
+      }
       *abort_flag = 0;
       fence_mbarrier_init();
       tma_prefetch_desc(&tmA);
@@ -382,6 +488,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
 
   SegIter iter;
   iter.init(&kp.s);
+  TileSrc<PAIR> src;
+  src.init(kp, ring_ids, ring_full, ring_empty);
   Seg seg;
 
   if (warp == 0) {
@@ -391,7 +499,9 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       uint32_t issued_mask = 0;
       bool ok = true;
       const uint64_t pol_a = l2_policy(p.l2_a), pol_b = l2_policy(p.l2_b);
-      while (ok && iter.next<EPI == EPI_STORE>(seg)) {
+      const bool fetcher = p.dyn_tiles && mma_cta;
+      while (ok && (fetcher ? src.fetch(seg, kp.ticket, kp.s.total_tiles, abort_flag, soft_ns)
+                            : src.template next<EPI == EPI_STORE>(seg, 1u, abort_flag, 1, soft_ns))) {
         int bi;
         int64_t mt, nt;
         kp.s.tile_coords(seg.tile, bi, mt, nt);
@@ -476,7 +586,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       const int kb_full = static_cast<int>(p.K / BK);  // k-blocks with all BK/16 steps inside K
       uint32_t ls = 0, st = 0, ph = 0;  // tiles done; stage and phase of the next k-block
       bool ok = true;
-      while (ok && iter.next<EPI == EPI_STORE>(seg)) {
+      while (ok && src.template next<EPI == EPI_STORE>(seg, 1u, abort_flag, 2, soft_ns)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error, soft_ns)) break;
         tc_fence_after();
@@ -664,7 +774,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
     } else {
       uint32_t sc = 0;
       const uint64_t pol_d = l2_policy(p.l2_d);  // the output's lines
-      while (iter.next<EPI == EPI_STORE>(seg)) {
+      while (src.template next<EPI == EPI_STORE>(seg, 0xffffffffu, abort_flag, 3, soft_ns)) {
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         // Every lane waits (each needs the acquire); the warp gives up together if any lane did.
         if (!failed)
@@ -876,6 +986,7 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   s.total_tiles = s.tiles_per_batch * p.nb1 * p.nb2;
   s.kb_total = static_cast<int>((p.K + BK - 1) / BK);
   s.group_m = static_cast<int>(s.n_mt < 16 ? s.n_mt : 16);
+  s.band_n = static_cast<int>(std::min<int64_t>(std::max(p.band_n, 0), s.n_nt));
   s.split = p.split_k ? 1 : 0;
   s.total_iters = s.total_tiles * s.kb_total;
   s.mask_chunk = (EPI == EPI_STORE && !s.split) ? p.causal : 0;
@@ -884,6 +995,17 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   const int64_t workers =
       std::min<int64_t>(max_workers[dev], s.split ? s.total_iters : s.total_tiles);
   if (workers <= 0) return cudaSuccess;
+  kp.ticket = nullptr;
+  if (p.dyn_tiles) {
+    // whole tiles with a plain epilogue only: the split and masked schedules and the update's
+    // look-ahead walk the static order
+    if (s.split || s.mask_chunk || C::RED || C::W_UPD) return cudaErrorInvalidValue;
+    void* t = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&t, g_tile_ticket);
+    if (e == cudaSuccess) e = cudaMemsetAsync(t, 0, sizeof(unsigned long long), stream);
+    if (e != cudaSuccess) return e;
+    kp.ticket = static_cast<unsigned long long*>(t);
+  }
   LaunchMark mark(p.kind, stream);
   return launch_overlapped(kern, dim3(static_cast<unsigned>((PAIR ? 2 : 1) * workers)), dim3(C::THREADS),
                            C::SMEM_BYTES, stream, PAIR ? 2 : 1, mA, mB, mB2, mD, kp);

@@ -40,6 +40,8 @@
  *   with cudaMalloc on first need (a call that needs to grow it synchronises
  *   the device), reused by later calls, freed by ipttt_release().  Calls that
  *   share the pool must be ordered (one stream, or the caller's own events).
+ *   So must calls that run the gated up-projection (ipttt_gate_up and the
+ *   layer calls): its tiles are handed out by one counter per device.
  *   ipttt_workspace_size reports the need of ipttt_layer_forward and
  *   ipttt_chunk_forward; the packed-document and multi-layer calls need the
  *   same per document or per layer and sequence.
