@@ -16,17 +16,18 @@
 //
 // and an item waits only for what it reads: an update for the residual of its
 // column block, an apply of chunk k+1 for the update rows of its slice.  Items
-// run in a fixed order of phases A_0, U_0, A_1, U_1, ... (the applies of a chunk,
-// then its updates), each phase column block by column block, and CTA pair w
-// takes items w, w + P, w + 2P, ... of it.  So the updates of the first column
-// blocks start while the last applies of the chunk are still running, the
-// applies of the next chunk while its last updates are, and no kernel boundary,
-// wave tail or separate residual pass stands between the steps.  (A staggered
-// order that mixes the phases of different blocks was measured slower: it
-// spreads the working set over two chunks' activations.)
-// Every dependency points to an earlier item, and a pair finishes an item
-// without waiting for later ones, so the order cannot deadlock once every CTA
-// is resident (the grid is what fits on the device at once).
+// are numbered in an order of phases A_0, U_0, A_1, U_1, ... (the applies of a
+// chunk, then its updates), each phase column block by column block, and CTA
+// pairs take them in that order as they free up (a device-wide counter).  So the
+// updates of the first column blocks start while the last applies of the chunk
+// are still running, the applies of the next chunk while its last updates are,
+// and no kernel boundary, wave tail or separate residual pass stands between the
+// steps.  (A staggered order that mixes the phases of different blocks was
+// measured slower: it spreads the working set over two chunks' activations; a
+// fixed share of items per pair, w, w + P, ..., 4% slower: pairs that run ahead
+// of others wait on them.)  Every dependency points to an earlier item, a pair
+// finishes an item without waiting for later ones, and every item taken is held
+// by a pair already running, so the order cannot deadlock.
 //
 // Roles as in the GEMM template (gemm_tc.cu): warp 0 the TMA producer (it also
 // waits for an item's inputs), warp 1 the MMA issuer (cta_group::2, 256 x 256
@@ -55,11 +56,12 @@ struct EngParams {
   EngineMse a;
   int64_t K, NB, MT, RT;    // chunks; column blocks, token tiles and d_ff tiles of 256
   int64_t NAb, NUb;         // items of one column block's apply phase and update phase
-  int64_t slots;            // phase slots of the order: 2K
   // counter regions (words): apply slices done per (sequence, chunk, block, token tile, half);
   // residual halves done per (sequence, chunk, block, token tile); update tiles done per
   // (sequence, chunk, block, d_ff slice)
   int64_t off_apply, off_resid, off_upd;
+  int64_t total;                  // items
+  unsigned long long* ticket;     // the item counter (zero at launch)
 };
 
 struct EItem {
@@ -81,33 +83,81 @@ __device__ __forceinline__ int eng_part_of(int r, int P, int64_t RT) {
 
 __device__ __forceinline__ int64_t eng_phase_items(const EngParams& e, int64_t ph) { return (ph & 1) ? e.NUb : e.NAb; }
 
-// Items of slot tau: every column block's phase tau (applies at even slots).
-__device__ __forceinline__ int64_t eng_slot_items(const EngParams& e, int64_t tau) {
-  return e.NB * eng_phase_items(e, tau);
-}
-
 // Position in the order: item j of phase slot tau (slot 2k: the applies of chunk k, every
-// column block's in turn; slot 2k + 1: its updates).  Each role walks its pair's items, w, w + P, ...
+// column block's in turn; slot 2k + 1: its updates).
 struct ECursor {
   int64_t tau, j;
-  __device__ void normalize(const EngParams& e) {
-    while (tau < e.slots) {
-      const int64_t c = eng_slot_items(e, tau);
-      if (j < c) return;
-      j -= c;
-      ++tau;
-    }
+  // Item g of the whole order (every chunk has the same two slots).
+  __device__ void at(const EngParams& e, int64_t g) {
+    const int64_t sa = e.NB * e.NAb, su = e.NB * e.NUb;
+    const int64_t k = g / (sa + su), rem = g - k * (sa + su);
+    tau = 2 * k + (rem >= sa ? 1 : 0);
+    j = rem >= sa ? rem - sa : rem;
   }
-  __device__ void start(const EngParams& e, int64_t first) {
-    tau = 0;
-    j = first;
-    normalize(e);
+};
+
+// The items a role of a pair walks.  The even CTA's producer takes item numbers from the
+// counter in increasing order, one ahead of its own walk, and publishes each in a ring of
+// kRing slots in both CTAs' shared memory (as gemm_tc.cu's TileSrc does for tiles); the other
+// roles of both CTAs read the same sequence and release each slot on the even CTA's barrier;
+// -1 ends it.
+struct EngSrc {
+  int64_t* ids;     // this CTA's ring
+  uint64_t* full;   // this CTA's ring barriers
+  uint64_t* empty;  // release barriers (the even CTA's are the ones counted)
+  uint32_t j;       // ring positions walked
+
+  __device__ void init(int64_t* ring_ids, uint64_t* ring_full, uint64_t* ring_empty) {
+    ids = ring_ids;
+    full = ring_full;
+    empty = ring_empty;
+    j = 0;
   }
-  __device__ void advance(const EngParams& e, int64_t step) {
-    j += step;
-    normalize(e);
+  // Consumer: the next item.  Called by the lanes of `wmask` of one warp together (lane 0
+  // among them), which give up together.
+  __device__ bool next(const EngParams& e, ECursor& c, uint32_t wmask, volatile int* abort, int code,
+                       uint64_t soft_ns) {
+    const uint32_t sl = j % kRing, ph = (j / kRing) & 1;
+    ++j;
+    if (!__all_sync(wmask, mbar_wait_bounded<true>(&full[sl], ph, abort, code, &g_device_error, soft_ns)))
+      return false;
+    const int64_t g = *reinterpret_cast<volatile int64_t*>(&ids[sl]);
+    __syncwarp(wmask);
+    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&empty[sl]), 0));
+    if (g < 0) return false;
+    c.at(e, g);
+    return true;
   }
-  __device__ bool done(const EngParams& e) const { return tau >= e.slots; }
+  // The item after the one `next` returned last, if already published.  Consumes nothing.
+  __device__ bool peek(const EngParams& e, ECursor& c) const {
+    const uint32_t sl = j % kRing, ph = (j / kRing) & 1;
+    if (!mbar_try_wait<true>(&full[sl], ph)) return false;
+    const int64_t g = *reinterpret_cast<volatile int64_t*>(&ids[sl]);
+    if (g < 0) return false;
+    c.at(e, g);
+    return true;
+  }
+  __device__ bool publish(const EngParams& e, uint32_t pos, volatile int* abort, uint64_t soft_ns) {
+    const uint32_t sl = pos % kRing, ph = (pos / kRing) & 1;
+    if (!mbar_wait_bounded<true>(&empty[sl], ph ^ 1, abort, 1, &g_device_error, soft_ns)) return false;
+    int64_t g = static_cast<int64_t>(atomicAdd(e.ticket, 1ull));
+    if (g >= e.total) g = -1;
+    ids[sl] = g;
+    mbar_arrive(&full[sl]);
+    st_shared_cluster_u64(mapa_shared(smem_u32(&ids[sl]), 1), static_cast<uint64_t>(g));
+    mbar_arrive_cluster(mapa_shared(smem_u32(&full[sl]), 1));  // release: the store above first
+    return true;
+  }
+  // The even CTA's producer: its next item (the item after it is published first).
+  __device__ bool fetch(const EngParams& e, ECursor& c, volatile int* abort, uint64_t soft_ns) {
+    if (j == 0 && !publish(e, 0, abort, soft_ns)) return false;
+    const int64_t g = ids[j % kRing];
+    if (g >= 0 && !publish(e, j + 1, abort, soft_ns)) return false;
+    ++j;
+    if (g < 0) return false;
+    c.at(e, g);
+    return true;
+  }
 };
 
 __device__ __forceinline__ EItem eng_decode(const EngParams& e, const ECursor& cur) {
@@ -244,12 +294,15 @@ __global__ void __launch_bounds__(kEngThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kEngStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
+  uint64_t* ring_full = bars + 2 * kEngStages + 7;  // [kRing] item numbers
+  uint64_t* ring_empty = ring_full + kRing;          // [kRing]
+  int64_t* ring_ids = reinterpret_cast<int64_t*>(ring_empty + kRing);
+  static_assert((2 * kEngStages + 7 + 3 * kRing) * 8 <= 512, "barrier area");
 
   const EngineMse& a = e.a;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
   const bool mma_cta = (rank == 0);
-  const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -262,6 +315,11 @@ __global__ void __launch_bounds__(kEngThreads, 1)
         mbar_init(&tempty_bar[i], 2 * kEngEpiWarps);  // every epilogue warp of both CTAs
       }
       mbar_init(drain_bar, 1);
+      for (int i = 0; i < kRing; ++i) {
+        mbar_init(&ring_full[i], 1);
+        // the even CTA's MMA issuer and epilogue warps, the odd CTA's producer and epilogue warps
+        mbar_init(&ring_empty[i], 2 + 2 * kEngEpiWarps);
+      }
       *abort_flag = 0;
       *last_flag = 0;
       fence_mbarrier_init();
@@ -281,6 +339,8 @@ __global__ void __launch_bounds__(kEngThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t soft_ns = g_wait_soft_ns;
+  EngSrc src;
+  src.init(ring_ids, ring_full, ring_empty);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -290,7 +350,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
       const uint64_t pol_hi = l2_policy(a.keep_hi ? L2_EVICT_LAST : L2_NORMAL);
       const uint64_t pol_n = l2_policy(L2_NORMAL);
       ECursor cur;
-      for (cur.start(e, pair); ok && !cur.done(e); cur.advance(e, npairs)) {
+      while (ok && (mma_cta ? src.fetch(e, cur, abort_flag, soft_ns) : src.next(e, cur, 1u, abort_flag, 1, soft_ns))) {
         const EItem it = eng_decode(e, cur);
         // what the item reads must be written: the residual of its column block (update), or
         // the previous chunk's update of its d_ff slice (apply)
@@ -388,7 +448,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
       uint32_t ls = 0, st = 0, ph = 0;
       bool ok = true;
       ECursor cur;
-      for (cur.start(e, pair); ok && !cur.done(e); cur.advance(e, npairs)) {
+      while (ok && src.next(e, cur, 1u, abort_flag, 2, soft_ns)) {
         const EItem it = eng_decode(e, cur);
         const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], aph ^ 1, abort_flag, 2, &g_device_error, soft_ns)) break;
@@ -445,19 +505,19 @@ __global__ void __launch_bounds__(kEngThreads, 1)
     bool failed = false;
     uint32_t ls = 0;
     ECursor cur;
-    for (cur.start(e, pair); !cur.done(e); cur.advance(e, npairs)) {
+    while (src.next(e, cur, 0xffffffffu, abort_flag, 3, soft_ns)) {
       const EItem it = eng_decode(e, cur);
       // The next item's planes may be loaded during this one only once what writes them has
       // finished: a complete residual of the first token tile of its column block means every
       // apply of that tile is done, and those waited for the previous chunk's updates of all
-      // the block's rows.
-      ECursor nx = cur;
-      nx.advance(e, npairs);
+      // the block's rows.  (Only if the next item is already published.)
+      ECursor nx;
       bool nx_upd = false;
-      if (it.upd && !nx.done(e)) {
+      if (it.upd && src.peek(e, nx)) {
         const EItem nit = eng_decode(e, nx);
         nx_upd = nit.upd && ld_acquire_u32(eng_cnt_resid(e, nit.s, nit.k, nit.n, 0)) >= 2u;
       }
+      nx_upd = __all_sync(0xffffffffu, nx_upd);
       const uint32_t acc = ls & 1, aph = (ls >> 1) & 1;
       if (!failed)
         failed = !__all_sync(0xffffffffu,
@@ -683,18 +743,23 @@ cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
   e.RT = a.d_ff / 256;
   e.NAb = a.batch * e.MT * a.parts;
   e.NUb = a.batch * e.RT;
-  e.slots = 2 * e.K;
   const int64_t total = e.K * e.NB * (e.NAb + e.NUb);
   e.off_apply = 0;
   e.off_resid = a.batch * e.K * e.NB * e.MT * 2;
   e.off_upd = e.off_resid + a.batch * e.K * e.NB * e.MT;
   const int64_t pairs = std::min<int64_t>(max_pairs[dev], total);
+  e.total = total;
+  {
+    void* t = nullptr;
+    cudaError_t err = cudaGetSymbolAddress(&t, g_tile_ticket);
+    if (err == cudaSuccess) err = cudaMemsetAsync(t, 0, sizeof(unsigned long long), stream);
+    if (err != cudaSuccess) return err;
+    e.ticket = static_cast<unsigned long long*>(t);
+  }
 
   LaunchMark mark(K_ENGINE, stream);
-  // Every CTA must be resident at once (items wait on each other's counters): the grid is the
-  // number of clusters that fit on the device together.  A plain launch of that grid puts them
-  // all on an idle GPU; should other work hold SMs, the late CTAs start as it leaves, and a
-  // counter wait that outlasts its limit ends the call with IPTTT_ERR_TIMEOUT, not a hang.
+  // The grid is the number of clusters that fit on the device together; should other work
+  // hold SMs, the late pairs start as it leaves and take whatever items are left.
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -120,7 +120,8 @@ struct GemmProblem {
 // split into work items per 256-column block n of W (the rule is independent across columns):
 // apply items (a 256-token tile of O_k[:, n], one of `parts` slices of d_ff), whose fp32 sums
 // meet in `acc` and the last of which forms O_k and R_k of that tile, and update items (256
-// rows x the 256 columns of W).  Items start as soon as what they read is written.
+// rows x the 256 columns of W).  Items start as soon as what they read is written.  CTA pairs
+// take items in order from a device-wide counter: launches that use it must be ordered.
 struct EngineMse {
   const void* Z = nullptr;       // [batch*L, d_ff] bf16, sequence s in rows s*L ..
   const void* V = nullptr;       // [batch*L, d] bf16
