@@ -87,6 +87,31 @@ def chunk_counts(w, cu=None):
     return (np.diff(np.asarray(cu, np.int64)) + w.B - 1) // w.B
 
 
+def window_tokens(w, rule="mse", cu=None):
+    """Tokens of the windows the library runs the MSE rule in (bf16, whole sequences, chunks
+    below 1024 tokens): the largest of 1024, 768, 512, 256 holding at least two chunks and
+    dividing L, with d and d_ff multiples of 256; 0 where the chunks run one by one."""
+    if rule != "mse" or cu is not None or w.dtype != "bf16" or w.d % 256 or w.d_ff % 256:
+        return 0
+    for W in (1024, 768, 512, 256):
+        if W % (2 * w.B) == 0 and w.L % W == 0:
+            return W
+    return 0
+
+
+def window_flops(w):
+    """FLOPs of the window GEMMs of a step: the masked Gram (kept pairs), the rows of the
+    inverse, Zt = X^T Z and the output X Y (dense W x W operands)."""
+    W = window_tokens(w)
+    if not W:
+        return 0.0
+    m, B = W // w.B, w.B
+    nwin = w.batch * (w.L // W)
+    gram = 2.0 * w.d_ff * B * B * m * (m - 1) / 2
+    inv = sum(2.0 * B * (j * B) * (j * B) for j in range(1, m))
+    return nwin * (gram + inv + 2.0 * W * W * w.d_ff + 2.0 * W * W * w.d)
+
+
 def roofline_tokens_per_s(w, peaks, cu=None):
     """The layer's roofline: the slower of all GEMM FLOPs at the dense bf16 peak
     and one fp32 read + write of W_o per chunk at the HBM bandwidth (per layer:
@@ -127,7 +152,12 @@ def _kernel_work_one(w, name, cu=None):
     if name == "update":
         return 2.0 * w.d * w.d_ff * T / steps, w_bytes / steps
     if name == "engine":  # the whole chunk loop (apply and update of every chunk) in one launch
+        W = window_tokens(w, cu=cu)
+        if W:  # windows of chunks: the fast weight is read and written once per window
+            w_bytes = w.batch * (w.L // W) * 2.0 * w.d_ff * w.d * 4
         return 4.0 * w.d * w.d_ff * T, w_bytes
+    if name == "window":
+        return window_flops(w), 0.0
     if name == "conv":
         return 0.0, 2.0 * T * w.d * 2
     if name == "residual":
@@ -574,6 +604,15 @@ def main():
         "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
+    W = window_tokens(w, args.rule, cu)
+    if W and not nl:
+        # the windowed form's own bound: its FLOPs (the window GEMMs added) at the tensor peak,
+        # and the fast weight read and written once per window
+        t_f = (flops_per_token(w) * T + window_flops(w)) / (peaks["bf16_tflops"] * 1e12)
+        t_b = w.batch * (w.L // W) * 2 * w.d_ff * w.d * 4 / (peaks["hbm_gbs"] * 1e9)
+        out["window_form"] = {"window_tokens": W, "chunks_per_window": W // w.B,
+                              "roofline_tokens_per_s": T / max(t_f, t_b),
+                              "pct_roofline": 100.0 * value / world / (T / max(t_f, t_b))}
     if nl:
         out["unit"] = "(token x layer)/s"
         out["one_call_per_layer"] = sequential

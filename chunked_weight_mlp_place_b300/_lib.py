@@ -31,7 +31,7 @@ EXPORTS = (
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20  # IPTTT_NOALLOC_SCRATCH_BYTES
 KERNEL_KINDS = ("gate_up", "conv", "proj", "apply", "residual", "update", "group_sum", "scan", "weight_copy",
-                "scores", "engine")
+                "scores", "engine", "window")
 
 
 class Dims(ctypes.Structure):

@@ -83,7 +83,7 @@ void reset_launch_count() { t_launches = 0; }
 
 const char* kind_name(int k) {
   static const char* names[K_COUNT] = {"gate_up", "conv",  "proj",        "apply",  "residual", "update",
-                                       "group_sum", "scan", "weight_copy", "scores", "engine"};
+                                       "group_sum", "scan", "weight_copy", "scores", "engine", "window"};
   return (k >= 0 && k < K_COUNT) ? names[k] : "unknown";
 }
 
@@ -335,8 +335,8 @@ ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, 
   // W_g | W_u tiles (4 d bytes a column of Z) take about 34 MB: the band stays in L2 while every
   // row tile of X streams past it, so X is read once per band and W_g | W_u about once.  The
   // Z tiles (written once, read much later) leave L2 first.
-  p.dyn_tiles = 1;
-  p.band_n = static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * dm->d * 128)));
+  p.dyn_tiles = bf16 ? 1 : 0;
+  p.band_n = bf16 ? static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * dm->d * 128))) : 0;
   p.l2_d = L2_EVICT_FIRST;
   p.out_bf16 = bf16;
   p.D = out(Z, dm->d_ff);
@@ -374,13 +374,22 @@ int64_t scan_groups(int64_t K) {
 }
 
 struct EngineLayout {
-  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, ac = 0, bc = 0, cnt = 0, total = 0;
+  size_t o_acc = 0, r = 0, d = 0, hi = 0, lo = 0, ac = 0, bc = 0, cnt = 0, g = 0, x = 0, zt = 0, total = 0;
 };
 
 // Slices of d_ff per apply tile in the persistent MSE engine.
 int engine_parts(const ipttt_dims* dm) { return static_cast<int>(std::min<int64_t>(4, dm->d_ff / 256)); }
 bool use_engine(const ipttt_dims* dm, int64_t B) {
   return dm->dtype == IPTTT_BF16 && engine_mse_supported(B, dm->d, dm->d_ff);
+}
+// The MSE rule in windows of m = W/B chunks (bf16, chunks below 1024 tokens): the tokens of a
+// window W, the largest of 1024, 768, 512 and 256 that is a multiple of 2B and divides L, on
+// which the engine runs; 0 where none fits.
+int64_t window_tokens(const ipttt_dims* dm, int64_t L, int64_t B) {
+  if (dm->dtype != IPTTT_BF16) return 0;
+  for (int64_t w = 1024; w >= 256; w -= 256)
+    if (w % (2 * B) == 0 && L % w == 0 && engine_mse_supported(w, dm->d, dm->d_ff)) return w;
+  return 0;
 }
 
 // Plane geometry of one d_ff x d fast weight (tile-major blocks, see common.cuh).
@@ -421,6 +430,18 @@ EngineLayout engine_layout(const ipttt_dims* dm, int64_t L, int64_t B, ipttt_rul
     e.ac = c.take<uint8_t>(dm->batch * L * kc * es);
     e.bc = c.take<uint8_t>(dm->batch * kc * dm->d * es);
     e.d = c.take<float>(dm->batch * nw);
+  } else if (rule == IPTTT_RULE_MSE && window_tokens(dm, L, B)) {
+    // windows: per window X = (I - A)^-1 and the masked Gram A (W x W bf16), Zt = X^T Z,
+    // every chunk's R kept (the output pass reads it)
+    const int64_t W = window_tokens(dm, L, B), nwin = dm->batch * (L / W);
+    e.o_acc = c.take<float>(dm->batch * W * dm->d);
+    e.r = c.take<uint16_t>(dm->batch * L * dm->d);
+    e.hi = c.take<uint16_t>(dm->batch * np);
+    e.lo = c.take<uint16_t>(dm->batch * np);
+    e.cnt = c.take<uint32_t>(engine_counter_words(dm->batch, L, W, dm->d, engine_parts(dm)));
+    e.g = c.take<uint16_t>(nwin * W * W);
+    e.x = c.take<uint16_t>(nwin * W * W);
+    e.zt = c.take<uint16_t>(dm->batch * L * dm->d_ff);
   } else if (rule == IPTTT_RULE_MSE) {
     e.o_acc = c.take<float>(dm->batch * B * dm->d);
     e.r = bf16 ? c.take<uint16_t>(dm->batch * B * dm->d) : c.take<float>(dm->batch * B * dm->d);
@@ -515,6 +536,118 @@ ipttt_status run_quadratic(const void* Z, const void* V, const float* W0, int64_
   return IPTTT_OK;
 }
 
+// The MSE rule over windows of m = W/B chunks (bf16).  Inside a window starting at chunk k the
+// steps unroll to  O_j = Z_j W_k + alpha sum_{i<j} (Z_j Z_i^T) R_i  and  R_j = O_j - V_j
+// (alpha = -eta/B), so with Y_j = Z_j W_k - V_j the window's residuals solve the block lower
+// triangular system  R = Y + A R,  A = alpha mask(Z Z^T) (the blocks i < j), that is R = X Y
+// with X = (I - A)^-1; and  W_{k+m} = W_k + alpha Z^T R = W_k + alpha (X^T Z)^T Y.  X depends on
+// Z alone, so for every window at once:
+//   A = alpha mask(Z Z^T)             one masked GEMM, bf16
+//   X = I; X_j = A_{j,<j} X_{<j}      row block by row block (m - 1 GEMMs over all windows)
+//   Zt = X^T Z                        one GEMM
+// then the persistent engine runs on windows as its chunks (apply Z W_k, R = Y, update with Zt:
+// the fast weight is read and written once per window), and last  O = X Y + V  for every window
+// at once.  The same O and W_final as m chunk steps, up to rounding.
+ipttt_status run_windows(const void* Z, const void* V, const float* W0, int64_t L, int64_t B, float eta, void* O,
+                         float* Wf, const ipttt_dims* dm, uint8_t* ws, const EngineLayout& lay, cudaStream_t st) {
+  const int64_t batch = dm->batch, d = dm->d, dff = dm->d_ff, nw = dff * d;
+  const int64_t W = window_tokens(dm, L, B), m = W / B, nwin = batch * (L / W);
+  const int nwi = static_cast<int>(nwin);
+  const float alpha = -eta / static_cast<float>(B);
+  uint16_t* G = reinterpret_cast<uint16_t*>(ws + lay.g);
+  uint16_t* X = reinterpret_cast<uint16_t*>(ws + lay.x);
+  uint16_t* Zt = reinterpret_cast<uint16_t*>(ws + lay.zt);
+  void* R = ws + lay.r;
+  IPTTT_CUDA(launch_eye_bf16(X, W, nwin, st));
+  {  // A = alpha mask(Z Z^T) per window (tiles the mask clears are skipped; X_j reads none of them)
+    GemmProblem p;
+    p.M = W;
+    p.N = W;
+    p.K = dff;
+    p.nb1 = nwi;
+    p.A = mat(Z, batch * L, dff, 0, 0, W);
+    p.B = p.A;
+    p.epi = EPI_STORE;
+    p.kind = K_WINDOW;
+    p.out_bf16 = 1;
+    p.alpha = alpha;
+    p.causal = B;
+    p.D = out(G, W, 0, W, 0, nwin * W);
+    IPTTT_CUDA(gemm(p, true, st));
+  }
+  for (int64_t j = 1; j < m; ++j) {  // X[jB .. jB+B, 0 .. jB] = A[jB .. jB+B, 0 .. jB] X[0 .. jB, 0 .. jB]
+    GemmProblem p;
+    p.M = B;
+    p.N = j * B;
+    p.K = j * B;
+    p.nb1 = nwi;
+    p.A = mat(G, nwin * W, W, 0, j * B, W);
+    p.B = mat(X, nwin * W, W, 1, 0, W);
+    p.epi = EPI_STORE;
+    p.kind = K_WINDOW;
+    p.out_bf16 = 1;
+    p.D = out(X, W, j * B, W, 0, nwin * W);
+    IPTTT_CUDA(gemm(p, true, st));
+  }
+  {  // Zt = X^T Z per window
+    GemmProblem p;
+    p.M = W;
+    p.N = dff;
+    p.K = W;
+    p.nb1 = nwi;
+    p.A = mat(X, nwin * W, W, 1, 0, W);
+    p.B = mat(Z, batch * L, dff, 1, 0, W);
+    p.epi = EPI_STORE;
+    p.kind = K_WINDOW;
+    p.out_bf16 = 1;
+    p.D = out(Zt, dff, 0, W, 0, batch * L);
+    IPTTT_CUDA(gemm(p, true, st));
+  }
+  const Planes w = planes_of(dm, reinterpret_cast<uint16_t*>(ws + lay.hi), reinterpret_cast<uint16_t*>(ws + lay.lo),
+                             batch, 1, 0);
+  IPTTT_CUDA(launch_split_planes(W0, dm->w0_per_seq ? nw : 0, w, dff, d, st));
+  float* o_acc = reinterpret_cast<float*>(ws + lay.o_acc);
+  IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * batch * W * d, st));
+  EngineMse em;
+  em.Z = Z;
+  em.Zu = Zt;
+  em.V = V;
+  em.O = O;  // Z_w W_k here; the output pass below writes O
+  em.acc = o_acc;
+  em.R = R;  // Y, every window's kept
+  em.r_seq = L;
+  em.r_chunk = W;
+  em.counters = reinterpret_cast<uint32_t*>(ws + lay.cnt);
+  em.w = w;
+  em.batch = batch;
+  em.L = L;
+  em.B = W;
+  em.d = d;
+  em.d_ff = dff;
+  em.parts = engine_parts(dm);
+  em.alpha = alpha;
+  em.keep_hi = planes_fit_l2(w) ? 1 : 0;
+  IPTTT_CUDA(cudaMemsetAsync(em.counters, 0, sizeof(uint32_t) * engine_counter_words(batch, L, W, d, em.parts), st));
+  IPTTT_CUDA(launch_engine_mse(em, st));
+  IPTTT_CUDA(launch_merge_planes(w, Wf, dff, d, st));
+  {  // O = X Y + V per window
+    GemmProblem p;
+    p.M = W;
+    p.N = d;
+    p.K = W;
+    p.nb1 = nwi;
+    p.A = mat(X, nwin * W, W, 0, 0, W);
+    p.B = mat(R, batch * L, d, 1, 0, W);
+    p.epi = EPI_STORE;
+    p.kind = K_WINDOW;
+    p.out_bf16 = 1;
+    p.add = out(const_cast<void*>(V), d, 0, W);
+    p.D = out(O, d, 0, W, 0, batch * L);
+    IPTTT_CUDA(gemm(p, true, st));
+  }
+  return IPTTT_OK;
+}
+
 ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L, int64_t B, float eta,
                         ipttt_rule rule, void* O, float* Wf, const ipttt_dims* dm, uint8_t* ws, const EngineLayout& lay,
                         cudaStream_t st) {
@@ -528,6 +661,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
   uint16_t* lo = bf16 ? reinterpret_cast<uint16_t*>(ws + lay.lo) : nullptr;
 
   if (rule == IPTTT_RULE_ADD_BLOCKCAUSAL) return run_quadratic(Z, V, W0, L, B, eta, O, Wf, dm, ws, lay, st);
+  if (rule == IPTTT_RULE_MSE && window_tokens(dm, L, B)) return run_windows(Z, V, W0, L, B, eta, O, Wf, dm, ws, lay, st);
   if (rule == IPTTT_RULE_MSE) {
     void* R = ws + lay.r;
     const Planes w = planes_of(dm, hi, lo, batch, 1, 0);
@@ -544,6 +678,7 @@ ipttt_status run_engine(const void* Z, const void* V, const float* W0, int64_t L
       em.O = O;
       em.acc = o_acc;
       em.R = R;
+      em.r_seq = B;
       em.counters = reinterpret_cast<uint32_t*>(ws + lay.cnt);
       em.w = w;
       em.batch = batch;

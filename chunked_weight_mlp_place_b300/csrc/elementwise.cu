@@ -558,6 +558,31 @@ cudaError_t launch_to_act(const float* src, int64_t src_stride, void* dst, int64
   return cudaGetLastError();
 }
 
+// entries n x n bf16 identity matrices, 8 elements (16 bytes) a thread.
+__global__ void __launch_bounds__(kThreads) eye_bf16_kernel(uint4* __restrict__ X, int64_t n, int64_t total8) {
+  const uint32_t one = 0x3F80u;  // bf16 1.0
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e0 = (i * 8) % (n * n);  // first element of the 8 within its matrix
+    const int64_t r = e0 / n, c0 = e0 % n;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (r >= c0 && r < c0 + 8) {
+      const int q = static_cast<int>(r - c0);
+      w[q / 2] = (q & 1) ? (one << 16) : one;
+    }
+    X[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+cudaError_t launch_eye_bf16(void* X, int64_t n, int64_t entries, cudaStream_t stream) {
+  if (n % 8) return cudaErrorInvalidValue;
+  const int64_t total8 = entries * n * n / 8;
+  if (total8 <= 0) return cudaSuccess;
+  LaunchMark mark(K_WEIGHT, stream);
+  eye_bf16_kernel<<<grid_for(total8), kThreads, 0, stream>>>(static_cast<uint4*>(X), n, total8);
+  return cudaGetLastError();
+}
+
 __global__ void __launch_bounds__(kThreads) axpy_kernel(float* __restrict__ W, const float* __restrict__ S,
                                                         float alpha, int64_t n) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;

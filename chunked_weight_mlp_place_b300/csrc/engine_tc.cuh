@@ -240,7 +240,8 @@ __device__ __forceinline__ void eng_epi_all_barrier() {
 __device__ __forceinline__ void eng_residual(const EngParams& e, const EItem& it, uint32_t rank, int ew, int lane) {
   const EngineMse& a = e.a;
   const int64_t row0 = it.m * 256 + rank * 128;           // in the chunk
-  const int64_t arow0 = it.s * a.B + row0;                  // acc and R rows
+  const int64_t arow0 = it.s * a.B + row0;                  // acc rows
+  const int64_t rrow0 = it.s * a.r_seq + it.k * a.r_chunk + row0;  // R rows
   const int64_t trow0 = it.s * a.L + it.k * a.B + row0;     // O and V rows
   const int64_t c0 = static_cast<int64_t>(it.n) * 256 + lane * 8;
   const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(a.V);
@@ -271,7 +272,7 @@ __device__ __forceinline__ void eng_residual(const EngParams& e, const EItem& it
         r4[q] = pack_bf16x2(s0 - t.x, s1 - t.y);
       }
       *reinterpret_cast<uint4*>(O + (trow0 + ii) * a.d + c0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-      *reinterpret_cast<uint4*>(R + (arow0 + ii) * a.d + c0) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
+      *reinterpret_cast<uint4*>(R + (rrow0 + ii) * a.d + c0) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
     }
   }
 }
@@ -394,11 +395,12 @@ __global__ void __launch_bounds__(kEngThreads, 1)
             const int c2 = static_cast<int>((it.s * a.w.rb + k0 / kPlaneRows) * a.w.cb + col / kPlaneCols);
             tma_load_3d_pair(sb, &tmHi, bar_cl, 0, c1, c2, pol_hi);
           } else {
-            // A: Z_k^T, tokens k0 .. of the chunk, this CTA's 128 d_ff rows of tile r
+            // A: Z_k^T (or the Zu operand's rows of the chunk), tokens k0 .., this CTA's 128 d_ff
+            // rows of tile r
             const int64_t trow = it.s * a.L + it.k * a.B + k0;
             const int64_t frow = static_cast<int64_t>(it.r) * 256 + rank * 128;
             // B: R_k, the same tokens, this CTA's 128 columns of block n
-            const int64_t rrow = it.s * a.B + k0;
+            const int64_t rrow = it.s * a.r_seq + it.k * a.r_chunk + k0;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               tma_load_2d_pair(sa + j * (64 * BK * 2), &tmZm, bar_cl, static_cast<int>(frow + 64 * j),
@@ -730,9 +732,11 @@ cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
   CUtensorMap mZk, mZm, mHi, mR, mAcc;
   const int64_t T = a.batch * a.L, BR = a.batch * a.B;
   if (!make_map(&mZk, a.Z, T, a.d_ff, a.d_ff, false, 64, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&mZm, a.Z, T, a.d_ff, a.d_ff, false, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_map(&mZm, a.Zu ? a.Zu : a.Z, T, a.d_ff, a.d_ff, false, 64, 64)) return cudaErrorInvalidValue;
   if (!make_plane_map(&mHi, a.w, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&mR, a.R, BR, a.d, a.d, false, 64, 64)) return cudaErrorInvalidValue;
+  if (a.r_seq < a.B || a.r_chunk < 0) return cudaErrorInvalidValue;
+  const int64_t RR = (a.batch - 1) * a.r_seq + (a.L / a.B - 1) * a.r_chunk + a.B;  // rows of R
+  if (!make_map(&mR, a.R, RR, a.d, a.d, false, 64, 64)) return cudaErrorInvalidValue;
   if (!make_map(&mAcc, a.acc, BR, a.d, a.d, true, 32, BM)) return cudaErrorInvalidValue;
 
   EngParams e;

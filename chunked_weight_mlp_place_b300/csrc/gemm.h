@@ -20,7 +20,7 @@ namespace ipttt {
 enum L2Hint : int { L2_NORMAL = 0, L2_EVICT_FIRST = 1, L2_EVICT_LAST = 2 };
 
 enum EpiKind : int {
-  EPI_STORE = 0,  // D = alpha * acc, block-causal mask if set   (D in the act dtype or fp32)
+  EPI_STORE = 0,  // D = alpha * acc (+ add), block-causal mask if set   (D in the act dtype or fp32)
   EPI_GATE = 1,   // D = SiLU(acc_g) * acc_u, acc_u from B2   (D in the act dtype)
   EPI_ACCUM = 2,  // D += acc, fp32 reductions in L2          (D fp32; partial sums)
   EPI_AXPY = 3,   // D = src + alpha * acc, fp32 (CUDA cores) or split hi/lo planes (tensor cores)
@@ -81,6 +81,7 @@ struct GemmProblem {
   int out_bf16 = 0;  // element type of D for STORE / GATE
   OutRef D;          // primary output (CUDA-core AXPY: fp32 W)
   OutRef src;        // CUDA-core AXPY: fp32 source (may equal D)
+  OutRef add;        // tensor-core STORE: a matrix of D's type and rows added to alpha * acc (null: none)
   // Tensor-core AXPY: the fast weight's tile-major hi/lo planes (split_w, plane_index in
   // common.cuh), read and rewritten in place.  Tensor-core ACCUM with b_planes: its B
   // operand is w.hi.
@@ -127,7 +128,9 @@ struct EngineMse {
   const void* V = nullptr;       // [batch*L, d] bf16
   void* O = nullptr;             // [batch*L, d] bf16 (out)
   float* acc = nullptr;          // [batch*B, d] fp32 scratch, zero on entry and left zero
-  void* R = nullptr;             // [batch*B, d] bf16 scratch
+  void* R = nullptr;             // bf16 R_k: row s*r_seq + k*r_chunk + i of sequence s, chunk k, token i
+  int64_t r_seq = 0, r_chunk = 0;  // (B, 0): a [batch*B, d] scratch reused by every chunk
+  const void* Zu = nullptr;      // the update's contraction operand in Z's layout (null: Z itself)
   uint32_t* counters = nullptr;  // engine_counter_words() words, zero on entry
   Planes w;                      // the fast weights (entry = sequence), read and rewritten in place
   int64_t batch = 0, L = 0, B = 0, d = 0, d_ff = 0;

@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(const GemmProblem p
 cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t stream) {
   if (p.M <= 0 || p.N <= 0 || p.nb1 <= 0 || p.nb2 <= 0) return cudaSuccess;
   if (p.out_bf16) return cudaErrorInvalidValue;  // fp32 mode writes fp32 activations
+  if (p.add.ptr || p.dyn_tiles) return cudaErrorNotSupported;  // tensor-core features
   const int64_t gx = (p.N + kBN - 1) / kBN, gy = (p.M + kBM - 1) / kBM, gz = static_cast<int64_t>(p.nb1) * p.nb2;
   if (gy > 65535 || gz > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy), static_cast<unsigned>(gz));

@@ -375,6 +375,32 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
           if (n + i >= lim) v[i] = 0.0f;
       }
     }
+    if constexpr (EPI == EPI_STORE) {
+      if (p.add.ptr) {  // + the addend's elements (m, n .. n + 31)
+        const int64_t arow = row_of(p.add, b1, b2) + m;
+        if constexpr (OUT_BF16) {
+          const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.add.ptr) + arow * p.add.ld + n;
+          if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 w = reinterpret_cast<const uint4*>(x)[q];
+              const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h[i]);
+                v[8 * q + 2 * i] += f.x;
+                v[8 * q + 2 * i + 1] += f.y;
+              }
+            }
+          } else {
+            for (int i = 0; i < 32 && n + i < p.N; ++i) v[i] += __bfloat162float(x[i]);
+          }
+        } else {
+          const float* x = static_cast<const float*>(p.add.ptr) + arow * p.add.ld + n;
+          for (int i = 0; i < 32 && n + i < p.N; ++i) v[i] += x[i];
+        }
+      }
+    }
     const int64_t row = row_of(p.D, b1, b2) + m;
     if constexpr (OUT_BF16) {
       __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D.ptr) + row * p.D.ld + n;
@@ -1055,7 +1081,9 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, cudaStream_t stream) {
       if (!a_mn && b_mn)
         return p.out_bf16 ? run_any<256, 1, false, true, EPI_STORE, true>(p, stream)
                           : run_any<256, 1, false, true, EPI_STORE, false>(p, stream);
-      if (a_mn && b_mn && !p.out_bf16) return run_any<256, 1, true, true, EPI_STORE, false>(p, stream);
+      if (a_mn && b_mn)
+        return p.out_bf16 ? run_any<256, 1, true, true, EPI_STORE, true>(p, stream)
+                          : run_any<256, 1, true, true, EPI_STORE, false>(p, stream);
       break;
     case EPI_ACCUM:
       if (!a_mn && b_mn)

@@ -22,7 +22,8 @@ enum KernelKind : int {
   K_WEIGHT = 8,    // fast-weight conversions (W_o0 -> split planes -> W_final, W_o0 -> W_final)
   K_SCORES = 9,    // additive rule, block-causal form: (eta/B) mask(Z Z^T)
   K_ENGINE = 10,   // MSE rule: the whole chunk loop in one persistent kernel
-  K_COUNT = 11
+  K_WINDOW = 11,   // MSE rule in windows of chunks: Gram, inverse, transformed-Z and output GEMMs
+  K_COUNT = 12
 };
 
 // Every kernel launch of the library sits inside one LaunchMark: it counts the
@@ -123,6 +124,8 @@ cudaError_t launch_merge_planes(const Planes& w, float* W, int64_t R, int64_t C,
 // dst[e*dst_stride + i] = act(src[e*src_stride + i]) (act = bf16 or fp32) for e < entries, i < n.
 cudaError_t launch_to_act(const float* src, int64_t src_stride, void* dst, int64_t dst_stride, int64_t entries,
                           int64_t n, bool bf16, cudaStream_t stream);
+// X (entries x n x n bf16, n a multiple of 8) = identity matrices.
+cudaError_t launch_eye_bf16(void* X, int64_t n, int64_t entries, cudaStream_t stream);
 // W[i] += alpha * S[i] for i < n (fp32).
 cudaError_t launch_axpy(float* W, const float* S, float alpha, int64_t n, cudaStream_t stream);
 // W[s] = W0[s or 0] (fp32 copy) for s < batch.

@@ -315,7 +315,8 @@ int64_t ipttt_last_launch_count(void);
  * for the recorded events and returns, for one kernel kind, the launches and
  * their summed device time in milliseconds since the last start.  Kinds:
  * 0 gate_up, 1 conv, 2 proj, 3 apply, 4 residual, 5 update, 6 group_sum,
- * 7 scan, 8 weight_copy, 9 scores (names from ipttt_kernel_name).  Host only. */
+ * 7 scan, 8 weight_copy, 9 scores, 10 engine, 11 window (names from
+ * ipttt_kernel_name).  Host only. */
 ipttt_status ipttt_kernel_timing(int32_t enable);
 ipttt_status ipttt_kernel_timing_read(int32_t kind, int64_t* launches, double* total_ms);
 const char* ipttt_kernel_name(int32_t kind);

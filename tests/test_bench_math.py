@@ -59,3 +59,22 @@ def test_several_layers_and_the_block_causal_form():
     pairs = w.B * w.B * K * (K - 1) / 2  # kept (query, key) pairs: keys of earlier chunks only
     assert pairs == pytest.approx(sum(q * w.B * w.B for q in range(K)), rel=1e-12)
     assert bench.kernel_work(w, "scores", rule="add_blockcausal")[0] == pytest.approx(2 * w.d_ff * pairs)
+
+
+def test_windowed_form_accounting():
+    """Chunks below 1024 tokens run in windows (the MSE rule, bf16): the engine then moves
+    the fast weight once per window, and the window GEMMs add FLOPs counted here by brute
+    force over the chunk pairs of a window."""
+    for B, W in [(64, 1024), (128, 1024), (256, 1024), (512, 1024), (1024, 0), (4096, 0)]:
+        assert bench.window_tokens(inputs.workload("4b_sweep", B=B)) == W
+    assert bench.window_tokens(inputs.workload("4b_sweep", B=64), rule="add") == 0
+    assert bench.window_tokens(inputs.workload("4b", L=1536, B=128)) == 768
+    w = inputs.workload("4b_sweep", B=64)
+    W, B = 1024, 64
+    nwin = w.L // W
+    assert bench.kernel_work(w, "engine")[1] == pytest.approx(nwin * 2 * w.d_ff * w.d * 4, rel=1e-12)
+    m = W // B
+    gram = sum(2 * w.d_ff * B * B for j in range(m) for i in range(j))  # chunk i < chunk j
+    inv = sum(2 * B * (j * B) * (j * B) for j in range(1, m))  # row block j: B x jB times jB x jB
+    per_window = gram + inv + 2 * W * W * w.d_ff + 2 * W * W * w.d
+    assert bench.kernel_work(w, "window")[0] == pytest.approx(nwin * per_window, rel=1e-12)

@@ -21,9 +21,9 @@ from oracle import ipttt_oracle as orc
 pytestmark = pytest.mark.gpu
 
 
-def _engine_case(B):
+def _engine_case(B, L):
     rng = np.random.default_rng(7)
-    L, d, d_ff = 1024, 512, 1024
+    d, d_ff = 512, 1024
     Z = inputs.round_to_bf16((rng.standard_normal((L, d_ff)) * 0.6).astype(np.float32))
     V = inputs.round_to_bf16((rng.standard_normal((L, d)) * 0.5).astype(np.float32))
     W0 = (rng.standard_normal((d_ff, d)) * d_ff ** -0.5).astype(np.float32)
@@ -37,11 +37,13 @@ def _run(L, B, Z, V, W0, rule):
     return O, Wf
 
 
-@pytest.mark.parametrize("rule,B", [("mse", 128), ("add", 128), ("mse", 256)])
-def test_a_wait_past_the_limit_is_reported_and_the_next_call_is_exact(rule, B):
-    """B = 128: the per-chunk GEMM kernels; B = 256 with the MSE rule: the persistent
-    chunk engine (its waits on other CTAs' counters included)."""
-    L, B, Z, V, W0 = _engine_case(B)
+@pytest.mark.parametrize("rule,B,L", [("mse", 128, 1152), ("add", 128, 1024), ("mse", 256, 768), ("mse", 64, 1024)])
+def test_a_wait_past_the_limit_is_reported_and_the_next_call_is_exact(rule, B, L):
+    """MSE with 9 chunks of 128 (no window fits) and the additive rule: the per-chunk
+    GEMM kernels; MSE with 3 chunks of 256: the persistent chunk engine on chunks (its
+    waits on other CTAs' counters included); MSE with chunks of 64: windows of 1024
+    tokens (the window GEMMs, then the engine on windows)."""
+    L, B, Z, V, W0 = _engine_case(B, L)
     assert ip.sync_status() == ip._lib.OK
     ip.set_wait_limit(200)  # ns: far below the waits of a real pipeline
     try:

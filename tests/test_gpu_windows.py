@@ -1,0 +1,99 @@
+"""GPU parity of the MSE rule run in windows of chunks (bf16, chunks below 1024
+tokens: the residuals of a window from one block-triangular solve, the
+persistent engine on windows) against the float64 oracle's chunk-by-chunk loop
+(itsolotime §2.2: apply, then one gradient step, chunk after chunk).
+
+Totals: relative Frobenius error <= 1e-2 on O (whole and per window), W_final
+and W_final - W_o0 (bf16 operands, fp32 accumulation).  In the first window of a
+sequence the fast weight at the window's start is W_o0, so there the fast-weight
+part of the output, D = O - O_0 with O_0 the eta = 0 output (the plain gated
+MLP), consists of the in-window corrections alone.  The test asserts that D is
+at least 3e-2 of O there, so dropping the corrections fails the per-window
+bound threefold, and that D is as accurate as rounding O to bf16 allows, within
+a factor of 3: that rounding alone (2^-9 relative on O) moves D by
+||bf16(O_ref) - O_ref|| / ||D_ref||, and the bf16 operands of the window's GEMMs
+(Z, the hi plane, G, X, Zt, R) by about as much again."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_weight_mlp_place_b300 as ip
+from chunked_weight_mlp_place_b300 import inputs
+from gpu_util import TOL, rel, run_layer
+from oracle import ipttt_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def window_of(L, B):
+    """The window the library picks: the largest of 1024, 768, 512, 256 tokens that
+    holds at least two chunks and divides L."""
+    for w in (1024, 768, 512, 256):
+        if w % (2 * B) == 0 and L % w == 0:
+            return w
+    return 0
+
+
+# eta: large enough that the first window's corrections are a sizable part of its output
+@pytest.mark.parametrize("batch,L,B,d,d_ff,eta", [
+    (2, 2048, 64, 256, 512, 0.05),    # 16 chunks a window, two windows a sequence, two sequences
+    (1, 2048, 128, 512, 768, 0.05),   # 8 chunks a window, two column blocks
+    (1, 3072, 256, 256, 1024, 0.05),  # 4 chunks a window, three windows
+    (1, 2048, 512, 256, 512, 0.2),    # 2 chunks a window
+    (1, 1536, 128, 256, 512, 0.05),   # windows of 768 tokens (6 chunks)
+    (1, 512, 64, 256, 256, 0.05),     # one window of 512 tokens
+    (1, 1024, 16, 256, 256, 0.05),    # B = 16: 64 chunks a window
+])
+def test_windows_match_the_chunk_loop(batch, L, B, d, d_ff, eta):
+    W = window_of(L, B)
+    assert W
+    w = inputs.workload("500m", batch=batch, L=L, B=B, d=d, d_ff=d_ff, eta=eta, vocab=512)
+    a = inputs.generate(w, seed=B + d + L)
+    O, Wf = run_layer(w, a, "mse")
+    args = (a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"], L, B)
+    Oref, Wref = orc.layer_forward(*args, w.eta, "mse")
+    O0, _ = orc.layer_forward(*args, 0.0, "mse")
+    tol = TOL["bf16"]
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(Wf))
+    assert rel(O, Oref) <= tol, rel(O, Oref)
+    assert rel(Wf, Wref) <= tol, rel(Wf, Wref)
+    W0 = a["W_o0"][None]
+    assert rel(Wf - W0, Wref - W0) <= tol, rel(Wf - W0, Wref - W0)
+    # window by window: the output, and its fast-weight part against the bf16 rounding of O
+    Ow, Orw = O.reshape(-1, W, d), Oref.reshape(-1, W, d)
+    assert max(rel(Ow[i], Orw[i]) for i in range(Ow.shape[0])) <= tol
+    Ob = torch.from_numpy(Oref).to(torch.bfloat16).double().numpy()
+    D, Dref, Db = ((x - O0).reshape(-1, W, d) for x in (O, Oref, Ob))
+    errs = [rel(D[i], Dref[i]) / rel(Db[i], Dref[i]) for i in range(D.shape[0])]
+    assert max(errs) <= 3.0, errs
+    share = np.linalg.norm(Dref[0]) / np.linalg.norm(Orw[0])
+    assert share >= 3 * tol, share
+    # gate, conv, proj, identity, Gram, m - 1 rows of the inverse, Zt, split, engine, merge, output
+    assert ip.last_launch_count() <= 9 + W // B
+
+
+def test_windows_with_per_sequence_initial_weights():
+    w = inputs.workload("500m", batch=2, L=2048, B=256, d=256, d_ff=512, eta=0.05)
+    a = inputs.generate(w, seed=9)
+    rng = np.random.default_rng(1)
+    W0 = (rng.standard_normal((2, w.d_ff, w.d)) * w.d_ff ** -0.5).astype(np.float32)
+    O, Wf = run_layer(w, a, "mse", W0=W0)
+    Oref, Wref = orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], W0, a["conv_w"], a["P"], w.L, w.B, w.eta,
+                                   "mse")
+    tol = TOL["bf16"]
+    assert rel(O, Oref) <= tol
+    assert rel(Wf, Wref) <= tol
+    assert rel(Wf - W0, Wref - W0) <= tol
+
+
+def test_windows_repeated_runs_agree():
+    """The engine's reductions add in whatever order the slices finish: every run
+    matches the oracle."""
+    w = inputs.workload("500m", batch=1, L=2048, B=64, d=256, d_ff=512, eta=0.05)
+    a = inputs.generate(w, seed=5)
+    Oref, Wref = orc.layer_forward(a["X"], a["E"], a["W_g"], a["W_u"], a["W_o0"], a["conv_w"], a["P"], w.L, w.B,
+                                   w.eta, "mse")
+    for _ in range(3):
+        O, Wf = run_layer(w, a, "mse")
+        assert rel(O, Oref) <= TOL["bf16"]
+        assert rel(Wf, Wref) <= TOL["bf16"]
