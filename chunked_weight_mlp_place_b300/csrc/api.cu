@@ -597,6 +597,7 @@ ipttt_status run_windows(const void* Z, const void* V, const float* W0, int64_t 
     p.nb1 = nwi;
     p.A = mat(X, nwin * W, W, 1, 0, W);
     p.B = mat(Z, batch * L, dff, 1, 0, W);
+    p.tri = -1;  // A = X^T is upper triangular
     p.epi = EPI_STORE;
     p.kind = K_WINDOW;
     p.out_bf16 = 1;
@@ -638,6 +639,7 @@ ipttt_status run_windows(const void* Z, const void* V, const float* W0, int64_t 
     p.nb1 = nwi;
     p.A = mat(X, nwin * W, W, 0, 0, W);
     p.B = mat(R, batch * L, d, 1, 0, W);
+    p.tri = 1;  // X is lower triangular
     p.epi = EPI_STORE;
     p.kind = K_WINDOW;
     p.out_bf16 = 1;

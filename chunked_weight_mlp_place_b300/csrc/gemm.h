@@ -108,6 +108,10 @@ struct GemmProblem {
   // increasing order from a device-wide counter as CTA pairs free up, instead of a fixed
   // share per pair.  The counter is one per device: launches that use it must be ordered.
   int dyn_tiles = 0;
+  // Tensor-core path, whole tiles: A triangular (M = K), its zeros skipped.  1: lower (A[m][k] = 0
+  // for k > m), a tile's contraction stops after its last row; -1: upper (A[m][k] = 0 for k < m),
+  // it starts at the k-block of its first row.
+  int tri = 0;
   // Tensor-core path: once a CTA has issued all its operand copies it asks L2 to fetch
   // its share of pf_count ranges of pf_bytes bytes, pf_stride bytes apart, from pf_ptr
   // (the next kernel's operand; 16-byte aligned).  No result depends on it.

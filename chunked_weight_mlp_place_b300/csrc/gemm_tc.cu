@@ -109,6 +109,7 @@ struct Sched {
   int kb_total;
   int group_m;
   int band_n;  // > 0: column-band order (GemmProblem::band_n)
+  int tri;     // GemmProblem::tri
   int split;
   int pair;
   int64_t total_iters;
@@ -182,6 +183,17 @@ struct SegIter {
     g.tile = t;
     g.kb0 = 0;
     g.kb1 = s->kb_total;
+    if (s->tri) {  // the k-blocks that hold the tile's rows' nonzeros (M = K)
+      int bi;
+      int64_t mt, nt;
+      s->tile_coords(t, bi, mt, nt);
+      const int64_t rows = s->pair ? 2 * BM : BM;
+      const int64_t r0 = mt * rows, r1 = min(r0 + rows, s->mask_m);
+      if (s->tri > 0)
+        g.kb1 = static_cast<int>(min(static_cast<int64_t>(s->kb_total), (r1 + BK - 1) / BK));
+      else
+        g.kb0 = static_cast<int>(r0 / BK);
+    }
     t += s->workers();
     return true;
   }
@@ -1013,6 +1025,7 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   s.kb_total = static_cast<int>((p.K + BK - 1) / BK);
   s.group_m = static_cast<int>(s.n_mt < 16 ? s.n_mt : 16);
   s.band_n = static_cast<int>(std::min<int64_t>(std::max(p.band_n, 0), s.n_nt));
+  s.tri = p.tri;
   s.split = p.split_k ? 1 : 0;
   s.total_iters = s.total_tiles * s.kb_total;
   s.mask_chunk = (EPI == EPI_STORE && !s.split) ? p.causal : 0;
@@ -1021,11 +1034,12 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   const int64_t workers =
       std::min<int64_t>(max_workers[dev], s.split ? s.total_iters : s.total_tiles);
   if (workers <= 0) return cudaSuccess;
+  if (p.tri && (p.M != p.K || s.split)) return cudaErrorInvalidValue;
   kp.ticket = nullptr;
   if (p.dyn_tiles) {
     // whole tiles with a plain epilogue only: the split and masked schedules and the update's
     // look-ahead walk the static order
-    if (s.split || s.mask_chunk || C::RED || C::W_UPD) return cudaErrorInvalidValue;
+    if (s.split || s.mask_chunk || s.tri || C::RED || C::W_UPD) return cudaErrorInvalidValue;
     void* t = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&t, g_tile_ticket);
     if (e == cudaSuccess) e = cudaMemsetAsync(t, 0, sizeof(unsigned long long), stream);
