@@ -90,12 +90,13 @@ def chunk_counts(w, cu=None):
 def window_tokens(w, rule="mse", cu=None):
     """Tokens of the windows the library runs the MSE rule in (bf16, whole sequences, chunks
     below 1024 tokens): the largest of 1024, 768, 512, 256 holding at least two chunks and
-    dividing L, with d and d_ff multiples of 256; 0 where the chunks run one by one."""
+    dividing L, with d and d_ff multiples of 256, where d (m - 1) >= 2 W for its m = W / B
+    chunks; 0 where the chunks run one by one."""
     if rule != "mse" or cu is not None or w.dtype != "bf16" or w.d % 256 or w.d_ff % 256:
         return 0
     for W in (1024, 768, 512, 256):
         if W % (2 * w.B) == 0 and w.L % W == 0:
-            return W
+            return W if w.d * (W // w.B - 1) >= 2 * W else 0
     return 0
 
 

@@ -69,6 +69,8 @@ def test_windowed_form_accounting():
         assert bench.window_tokens(inputs.workload("4b_sweep", B=B)) == W
     assert bench.window_tokens(inputs.workload("4b_sweep", B=64), rule="add") == 0
     assert bench.window_tokens(inputs.workload("4b", L=1536, B=128)) == 768
+    assert bench.window_tokens(inputs.workload("500m")) == 0  # d = 1024, two chunks a window: not taken
+    assert bench.window_tokens(inputs.workload("500m", B=256)) == 1024
     w = inputs.workload("4b_sweep", B=64)
     W, B = 1024, 64
     nwin = w.L // W

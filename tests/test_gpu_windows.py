@@ -25,12 +25,12 @@ from oracle import ipttt_oracle as orc
 pytestmark = pytest.mark.gpu
 
 
-def window_of(L, B):
+def window_of(L, B, d):
     """The window the library picks: the largest of 1024, 768, 512, 256 tokens that
-    holds at least two chunks and divides L."""
+    holds at least two chunks and divides L, taken where d (m - 1) >= 2 W."""
     for w in (1024, 768, 512, 256):
         if w % (2 * B) == 0 and L % w == 0:
-            return w
+            return w if d * (w // B - 1) >= 2 * w else 0
     return 0
 
 
@@ -38,14 +38,14 @@ def window_of(L, B):
 @pytest.mark.parametrize("batch,L,B,d,d_ff,eta", [
     (2, 2048, 64, 256, 512, 0.05),    # 16 chunks a window, two windows a sequence, two sequences
     (1, 2048, 128, 512, 768, 0.05),   # 8 chunks a window, two column blocks
-    (1, 3072, 256, 256, 1024, 0.05),  # 4 chunks a window, three windows
-    (1, 2048, 512, 256, 512, 0.2),    # 2 chunks a window
-    (1, 1536, 128, 256, 512, 0.05),   # windows of 768 tokens (6 chunks)
+    (1, 3072, 256, 1024, 512, 0.05),  # 4 chunks a window, three windows, four column blocks
+    (1, 2048, 512, 2048, 512, 0.2),   # 2 chunks a window
+    (1, 1536, 128, 512, 512, 0.05),   # windows of 768 tokens (6 chunks)
     (1, 512, 64, 256, 256, 0.05),     # one window of 512 tokens
     (1, 1024, 16, 256, 256, 0.05),    # B = 16: 64 chunks a window
 ])
 def test_windows_match_the_chunk_loop(batch, L, B, d, d_ff, eta):
-    W = window_of(L, B)
+    W = window_of(L, B, d)
     assert W
     w = inputs.workload("500m", batch=batch, L=L, B=B, d=d, d_ff=d_ff, eta=eta, vocab=512)
     a = inputs.generate(w, seed=B + d + L)
@@ -73,7 +73,7 @@ def test_windows_match_the_chunk_loop(batch, L, B, d, d_ff, eta):
 
 
 def test_windows_with_per_sequence_initial_weights():
-    w = inputs.workload("500m", batch=2, L=2048, B=256, d=256, d_ff=512, eta=0.05)
+    w = inputs.workload("500m", batch=2, L=2048, B=256, d=1024, d_ff=512, eta=0.05)
     a = inputs.generate(w, seed=9)
     rng = np.random.default_rng(1)
     W0 = (rng.standard_normal((2, w.d_ff, w.d)) * w.d_ff ** -0.5).astype(np.float32)
