@@ -602,7 +602,8 @@ ipttt_status run_windows(const void* Z, const void* V, const float* W0, int64_t 
     p.nb1 = nwi;
     p.A = mat(X, nwin * W, W, 1, 0, W);
     p.B = mat(Z, batch * L, dff, 1, 0, W);
-    p.tri = -1;  // A = X^T is upper triangular
+    p.tri = -1;       // A = X^T is upper triangular
+    p.dyn_tiles = 1;  // tiles of unequal contractions: pairs take them as they free up
     p.epi = EPI_STORE;
     p.kind = K_WINDOW;
     p.out_bf16 = 1;
@@ -645,6 +646,7 @@ ipttt_status run_windows(const void* Z, const void* V, const float* W0, int64_t 
     p.A = mat(X, nwin * W, W, 0, 0, W);
     p.B = mat(R, batch * L, d, 1, 0, W);
     p.tri = 1;  // X is lower triangular
+    p.dyn_tiles = 1;
     p.epi = EPI_STORE;
     p.kind = K_WINDOW;
     p.out_bf16 = 1;
@@ -1206,6 +1208,9 @@ ipttt_status ipttt_layers_forward(const void* X, const void* E, const void* W_g,
     p.epi = EPI_GATE;
     p.kind = K_GATE;
     p.out_bf16 = bf16;
+    p.dyn_tiles = bf16 ? 1 : 0;  // tile order as in run_gate
+    p.band_n = bf16 ? static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * d * 128))) : 0;
+    p.l2_d = L2_EVICT_FIRST;
     p.D = out(ws + z_off, dff, 0, T, 0, NT);
     IPTTT_CUDA(gemm(p, bf16, st));
   }

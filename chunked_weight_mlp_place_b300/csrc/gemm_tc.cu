@@ -69,7 +69,7 @@ constexpr int BK = 64;
 constexpr int kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns between the two accumulator buffers
 
-template <int BN, int NB, int EPI, bool PAIR>
+template <int BN, int NB, int EPI, bool PAIR, bool OUT_BF16>
 struct Cfg {
   static constexpr bool W_UPD = (EPI == EPI_AXPY);  // update epilogue on the tile-major planes
   static constexpr bool RED = (EPI == EPI_ACCUM);
@@ -81,8 +81,11 @@ struct Cfg {
   static constexpr int B_COLS = PAIR ? N_MMA / 2 : N_MMA;  // B columns held by one CTA per stage
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_COLS * BK * 2;
-  // apply: two staging buffers of the tile's 128 rows x 32 fp32 for the TMA reductions
-  static constexpr int STG_BYTES = RED ? BM * 32 * 4 : 0;
+  // bf16 STORE: the tile's 64-column chunks go out through TMA stores from shared memory
+  static constexpr bool TMA_ST = (EPI == EPI_STORE) && OUT_BF16;
+  // apply: two staging buffers of the tile's 128 rows x 32 fp32 for the TMA reductions; bf16
+  // STORE: two of 128 rows x 64 bf16 for the TMA stores
+  static constexpr int STG_BYTES = (RED || TMA_ST) ? BM * 32 * 4 : 0;
   static constexpr int STG_TOTAL = 2 * STG_BYTES;
   static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int BAR_BYTES = 512;
@@ -138,6 +141,22 @@ struct Sched {
     mt = first_m + q % gm;
     nt = q / gm;
   }
+  // The k-blocks of tile t: all of K, or with a triangular A those that hold the tile's rows'
+  // nonzeros (M = K).
+  __device__ void kb_range(int64_t t, int& kb0, int& kb1) const {
+    kb0 = 0;
+    kb1 = kb_total;
+    if (!tri) return;
+    int bi;
+    int64_t mt, nt;
+    tile_coords(t, bi, mt, nt);
+    const int64_t rows = pair ? 2 * BM : BM;
+    const int64_t r0 = mt * rows, r1 = min(r0 + rows, mask_m);
+    if (tri > 0)
+      kb1 = static_cast<int>(min(static_cast<int64_t>(kb_total), (r1 + BK - 1) / BK));
+    else
+      kb0 = static_cast<int>(r0 / BK);
+  }
   __device__ bool masked(int64_t t) const {
     if (!mask_chunk) return false;
     int bi;
@@ -181,19 +200,7 @@ struct SegIter {
       while (t < s->total_tiles && s->masked(t)) t += s->workers();
     if (t >= s->total_tiles) return false;
     g.tile = t;
-    g.kb0 = 0;
-    g.kb1 = s->kb_total;
-    if (s->tri) {  // the k-blocks that hold the tile's rows' nonzeros (M = K)
-      int bi;
-      int64_t mt, nt;
-      s->tile_coords(t, bi, mt, nt);
-      const int64_t rows = s->pair ? 2 * BM : BM;
-      const int64_t r0 = mt * rows, r1 = min(r0 + rows, s->mask_m);
-      if (s->tri > 0)
-        g.kb1 = static_cast<int>(min(static_cast<int64_t>(s->kb_total), (r1 + BK - 1) / BK));
-      else
-        g.kb0 = static_cast<int>(r0 / BK);
-    }
+    s->kb_range(t, g.kb0, g.kb1);
     t += s->workers();
     return true;
   }
@@ -223,7 +230,6 @@ struct TileSrc {
   uint64_t* full;      // this CTA's ring barriers: one arrival per fill
   uint64_t* empty;     // the ring's release barriers (the even CTA's are the ones counted)
   uint32_t j;          // fills consumed
-  int kb_total;
 
   __device__ void init(const KParams& kp, int64_t* ring_ids, uint64_t* ring_full, uint64_t* ring_empty) {
     it.init(&kp.s);
@@ -231,7 +237,6 @@ struct TileSrc {
     full = ring_full;
     empty = ring_empty;
     j = 0;
-    kb_total = kp.s.kb_total;
   }
   // Consumer: the next tile.  Called by the lanes in `wmask` of one warp together (lane 0
   // among them); the warp gives up together if any lane's wait did.
@@ -252,8 +257,7 @@ struct TileSrc {
     }
     if (t < 0) return false;
     g.tile = t;
-    g.kb0 = 0;
-    g.kb1 = kb_total;
+    it.s->kb_range(t, g.kb0, g.kb1);
     return true;
   }
   // The even CTA's producer: its next tile.  Tile numbers are published one position ahead
@@ -281,8 +285,7 @@ struct TileSrc {
     ++j;
     if (t < 0) return false;
     g.tile = t;
-    g.kb0 = 0;
-    g.kb1 = kb_total;
+    it.s->kb_range(t, g.kb0, g.kb1);
     return true;
   }
 };
@@ -363,14 +366,13 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   return w;
 }
 
-// Row-per-lane epilogue of 32 consecutive columns n.. of row m (gate, proj,
-// group sums, and the rows of a split-mode tile that a TMA box cannot cover).
+// Output values of 32 consecutive columns n.. of row m (STORE: alpha * acc, the mask, the
+// addend; GATE: SiLU(acc_g) * acc_u); columns past N are left as computed.
 template <int EPI, bool OUT_BF16>
-__device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
-                                               const uint32_t (&r)[32], const uint32_t (&u)[32], uint64_t pol_d) {
+__device__ __forceinline__ void epilogue_values(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
+                                                const uint32_t (&r)[32], const uint32_t (&u)[32], float (&v)[32]) {
   const bool full = (n + 32 <= p.N);
-  if constexpr (EPI == EPI_STORE || EPI == EPI_GATE) {
-    float v[32];
+  {
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float a = __uint_as_float(r[i]);
@@ -413,6 +415,18 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
         }
       }
     }
+  }
+}
+
+// Row-per-lane epilogue of 32 consecutive columns n.. of row m (gate, proj,
+// group sums, and the rows of a tile that a TMA box cannot cover).
+template <int EPI, bool OUT_BF16>
+__device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int b2, int64_t m, int64_t n,
+                                               const uint32_t (&r)[32], const uint32_t (&u)[32], uint64_t pol_d) {
+  const bool full = (n + 32 <= p.N);
+  if constexpr (EPI == EPI_STORE || EPI == EPI_GATE) {
+    float v[32];
+    epilogue_values<EPI, OUT_BF16>(p, b1, b2, m, n, r, u, v);
     const int64_t row = row_of(p.D, b1, b2) + m;
     if constexpr (OUT_BF16) {
       __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D.ptr) + row * p.D.ld + n;
@@ -445,11 +459,11 @@ __device__ __forceinline__ void epilogue_chunk(const GemmProblem& p, int b1, int
 }
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR, bool B_PL>
-__global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR, OUT_BF16>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ KParams kp) {
-  using C = Cfg<BN, NB, EPI, PAIR>;
+  using C = Cfg<BN, NB, EPI, PAIR, OUT_BF16>;
   static_assert(!PAIR || B_MN, "pairs split an MN-major B operand by columns");
   static_assert(!B_PL || (B_MN && NB == 1), "a plane B operand is MN-major and single");
   static_assert(B_PL ? C::B_COLS % kPlaneCols == 0 : C::B_COLS % 64 == 0,
@@ -501,7 +515,7 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       if constexpr (NB == 2) tma_prefetch_desc(&tmB2);
-      if constexpr (C::RED) tma_prefetch_desc(&tmD);
+      if (C::RED || (C::TMA_ST && p.D.rows > 0)) tma_prefetch_desc(&tmD);
     }
     __syncwarp();
     if constexpr (PAIR) {
@@ -835,6 +849,28 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
           tmem_wait_ld();
           const int64_t n = nt * BN + c * 32;
           if (n >= p.N) continue;
+          if constexpr (C::TMA_ST) {
+            if (box_rows && p.D.rows > 0) {
+              // 64-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ ((t / 2) % 4)
+              uint8_t* sbuf = stg + (sc & 1) * C::STG_BYTES;
+              uint4* srow = reinterpret_cast<uint4*>(sbuf + trow * 64);
+              if (!failed) {
+                float v[32];
+                epilogue_values<EPI, OUT_BF16>(p, b1, b2, m, n, r, u, v);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) srow[j ^ ((trow >> 1) & 3)] = pack8_bf16(v + 8 * j);
+              }
+              fence_proxy_async_shared();
+              if (issuer) bulk_wait_group_read<0>();  // the other buffer, written next chunk, is free
+              epi_barrier(0);
+              if (issuer && !failed && !*abort_flag) {
+                tma_store_2d(&tmD, sbuf, static_cast<int>(n), static_cast<int>(row_of(p.D, b1, b2) + mt * BM));
+                bulk_commit_group();
+              }
+              ++sc;
+              continue;
+            }
+          }
           if constexpr (C::RED) {
             if (box_rows) {
               // 128-byte swizzle: 16-byte chunk j of row t sits at chunk j ^ (t % 8)
@@ -870,8 +906,8 @@ __global__ void __launch_bounds__(Cfg<BN, NB, EPI, PAIR>::THREADS, 1)
         }
         ++ls;
       }
-      // Every bulk reduction has completed before the CTA exits.
-      if constexpr (C::RED) {
+      // Every bulk reduction or store has completed before the CTA exits.
+      if constexpr (C::RED || C::TMA_ST) {
         if (issuer) bulk_wait_group<0>();
         __syncwarp();
       }
@@ -962,7 +998,7 @@ bool make_plane_map(CUtensorMap* map, const Planes& w, int box_cols) {
 
 template <int BN, int NB, bool A_MN, bool B_MN, int EPI, bool OUT_BF16, bool PAIR, bool B_PL>
 static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
-  using C = Cfg<BN, NB, EPI, PAIR>;
+  using C = Cfg<BN, NB, EPI, PAIR, OUT_BF16>;
   auto kern = tc_gemm_kernel<BN, NB, A_MN, B_MN, EPI, OUT_BF16, PAIR, B_PL>;
   static std::mutex mu;
   static uint64_t attr_done = 0;  // bit per device: shared-memory size attribute set
@@ -1011,6 +1047,9 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   if (NB == 2 && !make_map(&mB2, p.B2.ptr, p.B2.rows, p.B2.cols, p.B2.ld, false, 64, B_MN ? 64 : BN))
     return cudaErrorInvalidValue;
   if (C::RED && !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, true, 32, BM)) return cudaErrorInvalidValue;
+  // bf16 STORE with the output's rows known: 32-column boxes (64 bytes a row) for the TMA stores
+  if (C::TMA_ST && p.D.rows > 0 && !make_map(&mD, p.D.ptr, p.D.rows, p.N, p.D.ld, false, 32, BM))
+    return cudaErrorInvalidValue;
   if (C::W_UPD && (!p.w.hi || !p.w.lo || p.w.rb <= 0 || p.w.cb <= 0)) return cudaErrorInvalidValue;
 
   KParams kp;
@@ -1039,7 +1078,7 @@ static cudaError_t run(const GemmProblem& p, cudaStream_t stream) {
   if (p.dyn_tiles) {
     // whole tiles with a plain epilogue only: the split and masked schedules and the update's
     // look-ahead walk the static order
-    if (s.split || s.mask_chunk || s.tri || C::RED || C::W_UPD) return cudaErrorInvalidValue;
+    if (s.split || s.mask_chunk || C::RED || C::W_UPD) return cudaErrorInvalidValue;
     void* t = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&t, g_tile_ticket);
     if (e == cudaSuccess) e = cudaMemsetAsync(t, 0, sizeof(unsigned long long), stream);
