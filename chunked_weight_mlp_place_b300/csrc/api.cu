@@ -319,6 +319,15 @@ OutRef out(void* ptr, int64_t ld, int64_t y0 = 0, int64_t ys1 = 0, int64_t ys2 =
 size_t act_size(const ipttt_dims* d) { return d->dtype == IPTTT_BF16 ? 2 : 4; }
 
 // ---------------------------------------------------------------- steps
+// The gate's tile order: dynamic (pairs take the next tile as they free up), in bands of columns
+// whose W_g | W_u tiles (4 d bytes a column of Z, 128 columns a tile) take about 34 MB, so the
+// band stays in L2 while every row tile of X streams past it: X is read once per band and
+// W_g | W_u about once.
+void gate_tile_order(GemmProblem& p, int64_t d, bool bf16) {
+  p.dyn_tiles = bf16 ? 1 : 0;
+  p.band_n = bf16 ? static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * d * 128))) : 0;
+}
+
 ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, int64_t T, const ipttt_dims* dm,
                       cudaStream_t st) {
   const bool bf16 = dm->dtype == IPTTT_BF16;
@@ -331,13 +340,8 @@ ipttt_status run_gate(const void* X, const void* W_g, const void* W_u, void* Z, 
   p.B2 = mat(W_u, dm->d, dm->d_ff, 1);
   p.epi = EPI_GATE;
   p.kind = K_GATE;
-  // Tiles in dynamic order (pairs take the next tile as they free up), in bands of columns whose
-  // W_g | W_u tiles (4 d bytes a column of Z) take about 34 MB: the band stays in L2 while every
-  // row tile of X streams past it, so X is read once per band and W_g | W_u about once.  The
-  // Z tiles (written once, read much later) leave L2 first.
-  p.dyn_tiles = bf16 ? 1 : 0;
-  p.band_n = bf16 ? static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * dm->d * 128))) : 0;
-  p.l2_d = L2_EVICT_FIRST;
+  gate_tile_order(p, dm->d, bf16);
+  p.l2_d = L2_EVICT_FIRST;  // the Z tiles (written once, read much later) leave L2 first
   p.out_bf16 = bf16;
   p.D = out(Z, dm->d_ff);
   IPTTT_CUDA(gemm(p, bf16, st));
@@ -1208,8 +1212,7 @@ ipttt_status ipttt_layers_forward(const void* X, const void* E, const void* W_g,
     p.epi = EPI_GATE;
     p.kind = K_GATE;
     p.out_bf16 = bf16;
-    p.dyn_tiles = bf16 ? 1 : 0;  // tile order as in run_gate
-    p.band_n = bf16 ? static_cast<int>(std::max<int64_t>(1, (int64_t{33} << 20) / (4 * d * 128))) : 0;
+    gate_tile_order(p, d, bf16);
     p.l2_d = L2_EVICT_FIRST;
     p.D = out(ws + z_off, dff, 0, T, 0, NT);
     IPTTT_CUDA(gemm(p, bf16, st));
