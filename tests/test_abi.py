@@ -181,6 +181,18 @@ def test_workspace_size_is_host_only(L):
     kc = 9728 + 32768
     quad = 32768 * kc * 2 + kc * 2560 * 2 + 9728 * 2560 * 4
     assert quad <= out.value <= quad + 4096
+    # MSE with chunks of 64 tokens: windows of 1024 tokens (16 chunks): the engine's sums, counters
+    # and planes for 1024-token chunks, every window's Y, Zt, and the Gram and X of each of the 32
+    # windows (1024 x 1024 bf16)
+    assert L.ipttt_workspace_size(ctypes.byref(dm), 32768, 64, 0, 0, ctypes.byref(out)) == _lib.OK
+    win = (1024 * 2560 * 4 + 32768 * 2560 * 2 + 2 * 9728 * 2560 * 2 + 32 * 10 * (3 * 4 + 4) * 4
+           + 2 * 32 * 1024 * 1024 * 2 + 32768 * 9728 * 2)
+    assert win <= out.value <= win + 4096
+    # d = 1024 with two chunks a window: no windows (d (m - 1) < 2 W), the engine on 512-token chunks
+    dm5 = _dims(batch=8, d=1024, d_ff=4096)
+    assert L.ipttt_workspace_size(ctypes.byref(dm5), 4096, 512, 0, 0, ctypes.byref(out)) == _lib.OK
+    eng5 = 8 * (512 * 1024 * 4 + 512 * 1024 * 2 + 2 * 4096 * 1024 * 2) + 8 * 8 * 4 * (3 * 2 + 4) * 4
+    assert eng5 <= out.value <= eng5 + 4096
     assert L.ipttt_workspace_size(ctypes.byref(dm), 100, 64, 0, 0, ctypes.byref(out)) == _lib.ERR_INVALID_ARG
     assert L.ipttt_workspace_size(None, 128, 64, 0, 0, ctypes.byref(out)) == _lib.ERR_INVALID_ARG
 
