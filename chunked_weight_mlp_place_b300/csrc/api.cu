@@ -915,6 +915,14 @@ ipttt_status run_varlen(const void* X, const void* E, const void* W_g, const voi
   const size_t st_off = c.take<int64_t>(n);
   const size_t ln_off = c.take<int64_t>(n);
   const size_t wt_off = c.take<int64_t>(n);
+  // the persistent engine (bf16 MSE, engine shapes): documents running per chunk, items before
+  // each chunk, counters
+  const bool eng = bf16 && rule == IPTTT_RULE_MSE && engine_mse_supported(B, d, dff) && n > 0;
+  const int parts = engine_parts(dm);
+  const int64_t Lmax = pl.k_max * B;
+  const size_t ac_off = eng ? c.take<int64_t>(pl.k_max) : 0;
+  const size_t ic_off = eng ? c.take<int64_t>(pl.k_max + 1) : 0;
+  const size_t cn_off = eng ? c.take<uint32_t>(engine_counter_words(n, Lmax, B, d, parts)) : 0;
   void* wsv = nullptr;
   IPTTT_TRY(pool_reserve(c.off, &wsv));
   uint8_t* ws = static_cast<uint8_t*>(wsv);
@@ -966,7 +974,43 @@ ipttt_status run_varlen(const void* X, const void* E, const void* W_g, const voi
   }
   IPTTT_CUDA(cudaMemsetAsync(o_acc, 0, sizeof(float) * n * B * d, st));
   const float alpha = (rule == IPTTT_RULE_MSE ? -eta : eta) / static_cast<float>(B);
-  for (int64_t i = 0; i < pl.k_max; ++i) {
+  if (eng) {
+    // the whole chunk loop of every document in one persistent kernel; chunk k's items cover the
+    // documents still running (a prefix of the longest-first order)
+    const int64_t NB = d / 256, MT = B / 256, RT = dff / 256;
+    std::vector<int64_t> icum(pl.k_max + 1, 0);
+    for (int64_t k = 0; k < pl.k_max; ++k) icum[k + 1] = icum[k] + NB * pl.active[k] * (MT * parts + RT);
+    int64_t* act_d = reinterpret_cast<int64_t*>(ws + ac_off);
+    int64_t* icum_d = reinterpret_cast<int64_t*>(ws + ic_off);
+    IPTTT_CUDA(cudaMemcpyAsync(act_d, pl.active.data(), sizeof(int64_t) * pl.k_max, cudaMemcpyHostToDevice, st));
+    IPTTT_CUDA(cudaMemcpyAsync(icum_d, icum.data(), sizeof(int64_t) * (pl.k_max + 1), cudaMemcpyHostToDevice, st));
+    EngineMse em;
+    em.Z = Z;
+    em.V = V;
+    em.O = O;
+    em.acc = o_acc;
+    em.R = R;
+    em.r_seq = B;
+    em.counters = reinterpret_cast<uint32_t*>(ws + cn_off);
+    em.w = w;
+    em.batch = n;
+    em.L = Lmax;
+    em.B = B;
+    em.d = d;
+    em.d_ff = dff;
+    em.parts = parts;
+    em.alpha = alpha;
+    em.keep_hi = planes_fit_l2(w) ? 1 : 0;
+    em.starts = starts_d;
+    em.lens = lens_d;
+    em.active = act_d;
+    em.icum = icum_d;
+    em.icum_total = icum[pl.k_max];
+    em.rows = T;
+    IPTTT_CUDA(cudaMemsetAsync(em.counters, 0, sizeof(uint32_t) * engine_counter_words(n, Lmax, B, d, parts), st));
+    IPTTT_CUDA(launch_engine_mse(em, st));
+  }
+  for (int64_t i = 0; i < (eng ? 0 : pl.k_max); ++i) {
     const int na = static_cast<int>(pl.active[i]);
     GemmProblem a;
     a.M = B;

@@ -17,8 +17,9 @@
 // and an item waits only for what it reads: an update for the residual of its
 // column block, an apply of chunk k+1 for the update rows of its slice.  Items
 // are numbered in an order of phases A_0, U_0, A_1, U_1, ... (the applies of a
-// chunk, then its updates), each phase column block by column block, and CTA
-// pairs take them in that order as they free up (a device-wide counter).  So the
+// chunk, then its updates), each phase sequence by sequence and, within one, column
+// block by column block, and CTA pairs take them in that order as they free up (a
+// device-wide counter).  So the
 // updates of the first column blocks start while the last applies of the chunk
 // are still running, the applies of the next chunk while its last updates are,
 // and no kernel boundary, wave tail or separate residual pass stands between the
@@ -81,16 +82,37 @@ __device__ __forceinline__ int eng_part_of(int r, int P, int64_t RT) {
   return p;
 }
 
-__device__ __forceinline__ int64_t eng_phase_items(const EngParams& e, int64_t ph) { return (ph & 1) ? e.NUb : e.NAb; }
+
+// First row of sequence (document) s in Z, V and O.
+__device__ __forceinline__ int64_t eng_row0(const EngineMse& a, int s) {
+  return a.starts ? a.starts[s] : static_cast<int64_t>(s) * a.L;
+}
 
 // Position in the order: item j of phase slot tau (slot 2k: the applies of chunk k, every
 // column block's in turn; slot 2k + 1: its updates).
 struct ECursor {
   int64_t tau, j;
-  // Item g of the whole order (every chunk has the same two slots).
+  // Item g of the whole order.
   __device__ void at(const EngParams& e, int64_t g) {
-    const int64_t sa = e.NB * e.NAb, su = e.NB * e.NUb;
-    const int64_t k = g / (sa + su), rem = g - k * (sa + su);
+    int64_t k, base, act;
+    if (e.a.icum) {  // packed documents: chunk k holds items icum[k] .. icum[k+1] - 1
+      int64_t lo = 0, hi = e.K - 1;
+      while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) / 2;
+        if (e.a.icum[mid] <= g)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      k = lo;
+      base = e.a.icum[k];
+      act = e.a.active[k];
+    } else {
+      act = e.a.batch;
+      k = g / (e.NB * (e.NAb + e.NUb));
+      base = k * e.NB * (e.NAb + e.NUb);
+    }
+    const int64_t sa = e.NB * act * e.MT * e.a.parts, rem = g - base;
     tau = 2 * k + (rem >= sa ? 1 : 0);
     j = rem >= sa ? rem - sa : rem;
   }
@@ -160,28 +182,29 @@ struct EngSrc {
   }
 };
 
+// Within a phase the items run sequence by sequence, each sequence's column block by column
+// block: one sequence's Z_k rows serve all its column blocks while they are in L2 (with many
+// sequences or documents, a chunk's rows of all of them exceed it).
 __device__ __forceinline__ EItem eng_decode(const EngParams& e, const ECursor& cur) {
   EItem it;
-  const int64_t c = eng_phase_items(e, cur.tau);
-  const int64_t n = cur.j / c;
-  int64_t rem = cur.j - n * c;
   const int64_t ph = cur.tau;
-  it.k = ph / 2;
-  it.n = static_cast<int>(n);
   const int P = e.a.parts;
+  const int64_t per = (ph & 1) ? e.RT : e.MT * P;  // items of one column block of one sequence
+  it.s = static_cast<int>(cur.j / (e.NB * per));
+  int64_t rem = cur.j - it.s * (e.NB * per);
+  it.n = static_cast<int>(rem / per);
+  rem -= it.n * per;
+  it.k = ph / 2;
   if (!(ph & 1)) {
     it.upd = 0;
     it.p = static_cast<int>(rem % P);
-    rem /= P;
-    it.m = static_cast<int>(rem % e.MT);
-    it.s = static_cast<int>(rem / e.MT);
+    it.m = static_cast<int>(rem / P);
     it.r = 0;
     it.kb0 = eng_part_begin(it.p, P, e.RT) * 4;
     it.kb1 = eng_part_begin(it.p + 1, P, e.RT) * 4;
   } else {
     it.upd = 1;
-    it.r = static_cast<int>(rem % e.RT);
-    it.s = static_cast<int>(rem / e.RT);
+    it.r = static_cast<int>(rem);
     it.m = it.p = 0;
     it.kb0 = 0;
     it.kb1 = static_cast<int>(e.a.B / BK);
@@ -235,14 +258,18 @@ __device__ __forceinline__ void eng_epi_all_barrier() {
 }
 
 // O_k and R_k of this CTA's 128 rows x 256 columns of an apply tile, from the finished fp32
-// sums, which are cleared for the next chunk.  Warp ew takes rows ew, ew + 8, ...; lane l
-// columns 8l .. 8l+7, so every row is one coalesced pass.
+// sums, which are cleared for the next chunk.  A packed document's last chunk may hold n < B
+// tokens: past them O is not written and R is zero, and R is scaled by B/n, so the step is the
+// mean over the chunk's n tokens.  Warp ew takes rows ew, ew + 8, ...; lane l columns
+// 8l .. 8l+7, so every row is one coalesced pass.
 __device__ __forceinline__ void eng_residual(const EngParams& e, const EItem& it, uint32_t rank, int ew, int lane) {
   const EngineMse& a = e.a;
   const int64_t row0 = it.m * 256 + rank * 128;           // in the chunk
   const int64_t arow0 = it.s * a.B + row0;                  // acc rows
   const int64_t rrow0 = it.s * a.r_seq + it.k * a.r_chunk + row0;  // R rows
-  const int64_t trow0 = it.s * a.L + it.k * a.B + row0;     // O and V rows
+  const int64_t trow0 = eng_row0(a, it.s) + it.k * a.B + row0;  // O and V rows
+  const int64_t ntok = a.lens ? min(a.B, a.lens[it.s] - it.k * a.B) : a.B;
+  const float scale = static_cast<float>(a.B) / static_cast<float>(ntok);
   const int64_t c0 = static_cast<int64_t>(it.n) * 256 + lane * 8;
   const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(a.V);
   __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.O);
@@ -255,7 +282,7 @@ __device__ __forceinline__ void eng_residual(const EngParams& e, const EItem& it
     for (int h = 0; h < 2; ++h) {
       const int64_t ii = i + h * kEngEpiWarps;
       ld_global_v8(a.acc + (arow0 + ii) * a.d + c0, x[h]);
-      v[h] = *reinterpret_cast<const uint4*>(V + (trow0 + ii) * a.d + c0);
+      v[h] = (row0 + ii < ntok) ? *reinterpret_cast<const uint4*>(V + (trow0 + ii) * a.d + c0) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -263,15 +290,16 @@ __device__ __forceinline__ void eng_residual(const EngParams& e, const EItem& it
       const uint32_t zero8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
       st_global_v8(a.acc + (arow0 + ii) * a.d + c0, zero8);
       const __nv_bfloat162* vh = reinterpret_cast<const __nv_bfloat162*>(&v[h]);
+      const bool valid = (row0 + ii < ntok);
       uint32_t o4[4], r4[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float s0 = __uint_as_float(x[h][2 * q]), s1 = __uint_as_float(x[h][2 * q + 1]);
         const float2 t = __bfloat1622float2(vh[q]);
         o4[q] = pack_bf16x2(s0, s1);
-        r4[q] = pack_bf16x2(s0 - t.x, s1 - t.y);
+        r4[q] = valid ? pack_bf16x2(scale * (s0 - t.x), scale * (s1 - t.y)) : 0u;
       }
-      *reinterpret_cast<uint4*>(O + (trow0 + ii) * a.d + c0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      if (valid) *reinterpret_cast<uint4*>(O + (trow0 + ii) * a.d + c0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       *reinterpret_cast<uint4*>(R + (rrow0 + ii) * a.d + c0) = make_uint4(r4[0], r4[1], r4[2], r4[3]);
     }
   }
@@ -388,7 +416,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
           const int64_t k0 = static_cast<int64_t>(kb) * BK;
           if (!it.upd) {
             // A: rows of Z_k (this CTA's 128 of the 256-token tile), d_ff columns k0 ..
-            const int64_t zrow = it.s * a.L + it.k * a.B + it.m * 256 + rank * 128;
+            const int64_t zrow = eng_row0(a, it.s) + it.k * a.B + it.m * 256 + rank * 128;
             tma_load_2d_pair(sa, &tmZk, bar_cl, static_cast<int>(k0), static_cast<int>(zrow), pol_n);
             // B: the hi plane, d_ff rows k0 .., this CTA's 128 columns of block n
             const int c1 = static_cast<int>((k0 % kPlaneRows) / 16);
@@ -397,7 +425,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
           } else {
             // A: Z_k^T (or the Zu operand's rows of the chunk), tokens k0 .., this CTA's 128 d_ff
             // rows of tile r
-            const int64_t trow = it.s * a.L + it.k * a.B + k0;
+            const int64_t trow = eng_row0(a, it.s) + it.k * a.B + k0;
             const int64_t frow = static_cast<int64_t>(it.r) * 256 + rank * 128;
             // B: R_k, the same tokens, this CTA's 128 columns of block n
             const int64_t rrow = it.s * a.r_seq + it.k * a.r_chunk + k0;
@@ -412,7 +440,7 @@ __global__ void __launch_bounds__(kEngThreads, 1)
         }
         // An update item of chunk k brings its share of Z_{k+1} (the next applies' A operand)
         // into L2: the chunk's update items split those rows of every sequence evenly.
-        if (ok && it.upd && it.k + 1 < e.K && rank == 0) {
+        if (ok && it.upd && it.k + 1 < e.K && rank == 0 && !a.starts) {
           const int64_t seg = a.B * a.d_ff * 2;  // bytes of one sequence's chunk of Z
           const int64_t total = a.batch * seg, nu = e.NB * e.NUb;
           const int64_t u = (static_cast<int64_t>(it.n) * a.batch + it.s) * e.RT + it.r;
@@ -730,7 +758,9 @@ cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
     }
   }
   CUtensorMap mZk, mZm, mHi, mR, mAcc;
-  const int64_t T = a.batch * a.L, BR = a.batch * a.B;
+  const int64_t T = a.rows > 0 ? a.rows : a.batch * a.L, BR = a.batch * a.B;
+  if ((a.starts || a.lens || a.active || a.icum) && !(a.starts && a.lens && a.active && a.icum && a.icum_total > 0))
+    return cudaErrorInvalidValue;
   if (!make_map(&mZk, a.Z, T, a.d_ff, a.d_ff, false, 64, BM)) return cudaErrorInvalidValue;
   if (!make_map(&mZm, a.Zu ? a.Zu : a.Z, T, a.d_ff, a.d_ff, false, 64, 64)) return cudaErrorInvalidValue;
   if (!make_plane_map(&mHi, a.w, 128)) return cudaErrorInvalidValue;
@@ -747,7 +777,7 @@ cudaError_t launch_engine_mse(const EngineMse& a, cudaStream_t stream) {
   e.RT = a.d_ff / 256;
   e.NAb = a.batch * e.MT * a.parts;
   e.NUb = a.batch * e.RT;
-  const int64_t total = e.K * e.NB * (e.NAb + e.NUb);
+  const int64_t total = a.icum ? a.icum_total : e.K * e.NB * (e.NAb + e.NUb);
   e.off_apply = 0;
   e.off_resid = a.batch * e.K * e.NB * e.MT * 2;
   e.off_upd = e.off_resid + a.batch * e.K * e.NB * e.MT;

@@ -141,6 +141,17 @@ struct EngineMse {
   int parts = 0;                 // slices of d_ff per apply tile
   float alpha = 0.0f;            // -eta / B
   int keep_hi = 0;               // keep the hi planes in L2 (evict last)
+  // Packed documents (sequence s = document s, longest first; L = the longest's chunks x B):
+  // starts[s] = its first row of Z, V and O, lens[s] its tokens (its last chunk may be short: R is
+  // zero past its end and scaled by B/n, O written only inside it), active[k] = the documents with
+  // a chunk k (a prefix), icum[k] = the items of the chunks before k (device tables, icum[K] =
+  // all); rows = the rows of Z, V and O.  Null: sequence s in rows s*L .. s*L+L-1.
+  const int64_t* starts = nullptr;
+  const int64_t* lens = nullptr;
+  const int64_t* active = nullptr;
+  const int64_t* icum = nullptr;
+  int64_t icum_total = 0;  // icum[K], known on the host
+  int64_t rows = 0;
 };
 
 }  // namespace ipttt
