@@ -166,8 +166,9 @@ ipttt_status ipttt_layer_forward_varlen(const void* X, const void* E, const void
 /*
  * Several layers' fast-weight MLPs over the same tokens in one call: every
  * step is one launch for all layers (the gate and projection GEMMs batched over
- * the layers, one conv launch, and each chunk's apply / residual / update over
- * all layers and sequences).  Layer l takes its own hidden states and weights;
+ * the layers, one conv launch, and the chunk loop over all layers and sequences:
+ * in bf16 mode with d, d_ff and B multiples of 256 one persistent kernel for
+ * the whole MSE loop, else each chunk's apply / residual / update).  Layer l takes its own hidden states and weights;
  * every layer's target is built from the same token embeddings E (the In-Place
  * TTT layer is the MLP block of each layer it is put in, itsolotime §2.1; its
  * target reads the token embeddings, §2.3).  Layers do not interact.
