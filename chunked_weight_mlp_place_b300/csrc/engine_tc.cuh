@@ -1,6 +1,9 @@
 // The MSE chunk loop of the In-Place TTT layer (itsolotime §2.2 and Fig. 1:
 // apply the fast weight to a chunk, then take one gradient step on it) as one
-// persistent kernel over every chunk of every sequence, for sm_103a.
+// persistent kernel over every chunk of every sequence, for sm_103a.  A sequence
+// may also be a packed document (itsolotime §3.2, the fast weight reset at every
+// boundary: each document has its own), or a run of windows of chunks whose
+// residuals were solved up front (the window form in api.cu).
 //
 // The rule is independent across the columns of W_o: column block n (256
 // columns) of O_k, R_k and W_{k+1} depends only on column block n of W_k.  So

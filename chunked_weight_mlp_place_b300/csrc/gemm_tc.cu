@@ -25,14 +25,17 @@
 //               output row) and apply the fused epilogue.
 // Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
 // the main loop of the next.  Work is either whole output tiles, strided over
-// the CTAs, or (split mode, for GEMMs with few tiles and a long K) an even
-// share of the (tile, k-block) iteration space per CTA.
+// the CTAs or (dynamic order) taken from a device-wide counter as CTA pairs free
+// up, or (split mode, for GEMMs with few tiles and a long K) an even share of
+// the (tile, k-block) iteration space per CTA.
 //
-// The two epilogues that move much data keep global accesses whole lines:
+// The epilogues that move much data keep global accesses whole lines:
 //   apply (split mode)  the epilogue stages the tile's 128 rows x 32 columns of
 //                       fp32 partial sums and adds them into the fp32 sums in L2
 //                       with one TMA reduce (the residual kernel then turns the
 //                       sums into O and R = O - V);
+//   bf16 STORE          32-column chunks staged in shared memory, one TMA store
+//                       each;
 //   update              no staging: a plane block's row is 32 contiguous bytes,
 //                       so each thread reads and writes its row of the hi and lo
 //                       planes directly and a warp moves 1 KB contiguous.
