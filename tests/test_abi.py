@@ -292,3 +292,27 @@ def test_binding_checks_shapes_before_the_call():
     with pytest.raises(ValueError, match="shape"):
         _lib.chunk_forward(Z, torch.zeros(256, 64, dtype=torch.bfloat16), torch.zeros(128, 64), 128, 64, 0.1, "mse",
                            torch.zeros(256, 64, dtype=torch.bfloat16), torch.zeros(1, 128, 64))  # W_final: batch 2
+
+
+@pytest.mark.parametrize("d,d_ff,Lseq,B", [
+    (2560, 9728, 32768, 64), (2560, 9728, 32768, 512), (1024, 4096, 4096, 512), (1024, 4096, 4096, 256),
+    (512, 1024, 1536, 128), (256, 512, 1536, 128), (256, 256, 512, 64), (2560, 9728, 4096, 1024),
+    (384, 1024, 2048, 64), (256, 768, 768, 256),
+])
+def test_the_benchmark_sees_the_windows_the_library_takes(L, d, d_ff, Lseq, B):
+    """bench.py's mirror of the window rule (its roofline accounting depends on it) against the
+    library's own choice, read off the MSE workspace: besides the fast weight's planes (at least
+    4 d d_ff bytes) a window's layout holds every chunk's Y and Zt (L (d + d_ff) bf16), where the
+    chunk layout holds one chunk's sums and R and the counters."""
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from chunked_weight_mlp_place_b300 import inputs
+
+    W = bench.window_tokens(inputs.workload("4b", L=Lseq, B=B, d=d, d_ff=d_ff))
+    out = ctypes.c_size_t()
+    assert L.ipttt_workspace_size(ctypes.byref(_dims(batch=1, d=d, d_ff=d_ff)), Lseq, B, 0, 0,
+                                  ctypes.byref(out)) == _lib.OK
+    assert (out.value >= 4 * d * d_ff + Lseq * (d + d_ff) * 2) == bool(W), (W, out.value)
