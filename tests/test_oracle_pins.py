@@ -171,6 +171,41 @@ def test_additive_closed_form_and_block_causal_form():
         np.testing.assert_allclose(Wk, W0 + eta / B * Z[p].T @ V[p], rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("B,m", [(4, 6), (8, 2), (1, 5)])
+def test_mse_loop_equals_its_window_solve(B, m):
+    """The MSE rule over m consecutive chunks from the window's start weight W_k, restated as one
+    solve: with alpha = -eta/B, A = alpha mask(Z Z^T) (token pairs in different chunks, the later
+    row), Y = Z W_k - V and X = (I - A)^-1, the window's residuals are R = X Y, its outputs O = R + V
+    and the next weight W_k + alpha (X^T Z)^T Y.  X is built row block by row block as
+    X_j = e_j + A_{j,<j} X_{<j} and checked against a dense inverse.  Equal to the oracle's chunk
+    loop up to float64 rounding (the same identity the GPU's windowed form computes in bf16)."""
+    rng = np.random.default_rng(9 + B)
+    W, d_ff, d, eta = B * m, 7, 5, 0.3
+    nwin = 3
+    L = W * nwin
+    Z, V, W0 = rng.standard_normal((L, d_ff)) * 0.5, rng.standard_normal((L, d)), rng.standard_normal((d_ff, d))
+    O_ref, W_ref = orc.chunk_engine(Z, V, W0, B, eta, "mse")
+    alpha = -eta / B
+    chunk = np.arange(W) // B
+    later = chunk[:, None] > chunk[None, :]
+    Wk = W0.copy()
+    O = np.zeros_like(V)
+    for w in range(nwin):
+        s = slice(w * W, (w + 1) * W)
+        Zw, Vw = Z[s], V[s]
+        A = alpha * (Zw @ Zw.T) * later
+        X = np.eye(W)
+        for j in range(1, m):
+            r = slice(j * B, (j + 1) * B)
+            X[r, :j * B] = A[r, :j * B] @ X[:j * B, :j * B]
+        np.testing.assert_allclose(X, np.linalg.inv(np.eye(W) - A), rtol=1e-10, atol=1e-12)
+        Y = Zw @ Wk - Vw
+        O[s] = X @ Y + Vw
+        Wk = Wk + alpha * (X.T @ Zw).T @ Y
+    np.testing.assert_allclose(O, O_ref, rtol=1e-9, atol=1e-10)
+    np.testing.assert_allclose(Wk, W_ref, rtol=1e-9, atol=1e-10)
+
+
 def test_eta_zero_is_the_plain_gated_mlp():
     t = _tiny(batch=2)
     O, W = orc.layer_forward(t["X"], t["E"], t["W_g"], t["W_u"], t["W_o0"], t["conv_w"], t["P"],
