@@ -127,6 +127,13 @@ typedef void* ipttt_stream; /* a cudaStream_t */
  *   W_final[batch, d_ff, d] fp32   out: the fast weight after the last chunk
  *
  * O and W_final must not overlap any input.  L == 0 copies W_o0 to W_final.
+ *
+ * In bf16 mode the MSE rule takes chunks below 1024 tokens a window of m = W/B
+ * chunks at a time when d, d_ff are multiples of 256, a window W (1024, 768,
+ * 512 or 256 tokens) holds m >= 2 chunks and divides L, and d (m - 1) >= 2 W:
+ * within a window the m steps unroll to one triangular solve for the
+ * residuals, so the fast weight is read and written once per window.  O and
+ * W_final are those of the m chunk steps, up to rounding.
  */
 ipttt_status ipttt_layer_forward(const void* X, const void* E, const void* W_g, const void* W_u,
                                  const float* W_o0, const float* conv_w, const void* P, int64_t L,
